@@ -1,0 +1,207 @@
+/*
+ * qmm.h -- C ABI of libqmm.so: quantized weight-by-activation matmul on GB300
+ * (sm_103a).
+ *
+ * The operation (llama.cpp visual guide, lesson 31 "The CPU backend", section
+ * "How the quantized dot product works"): weights are Q4_0 blocks of 32
+ * four-bit values with one fp16 scale each (value = (nibble - 8) * dw),
+ * activations are Q8_0 blocks of 32 int8 values with one fp16 scale each
+ * (value = q * da).  For every output the kernels form the exact integer dot
+ * of each block pair, sumi = sum_j (nibble_j - 8) * q_j, and accumulate
+ * sumi * (dw * da) in f32.  The ternary variant (Loom docs, "Plan 9 SIMD
+ * Forward", section "BitNet ternary MAD kernel") packs weights in {-1,0,+1}
+ * as 2-bit codes 16 per uint32 and computes dot = sum(code*q) - sum(q),
+ * then y = dot * weight_absmean / activation_scale.
+ *
+ * Conventions shared by every entry point
+ *  - Every data pointer is a DEVICE pointer owned by the caller (allocated
+ *    through any CUDA allocator); the library never allocates, frees or
+ *    keeps a pointer after the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it; the library never
+ *    synchronizes the host.  Outputs are valid once the stream reaches the
+ *    point after the call.
+ *  - All argument checks run on the host before anything is launched.  A
+ *    failed check returns a non-zero qmm_status and launches nothing.  The
+ *    kernels themselves check nothing (the caller-validated contract of the
+ *    Fucina course, chapter 06, section 6.3).
+ *  - Sizes are int64_t element counts.  m = activation rows (tokens),
+ *    n = output columns (weight rows), k = reduction length.
+ *  - Layouts are row-major and dense:
+ *      x   f32  [m, k] (row stride ldx where given)
+ *      aq  int8 [m, k]          ad  fp16 (raw bits) [m, k/32]
+ *      wq  u8   [n, k/2]        wd  fp16 (raw bits) [n, k/32]
+ *      y   f32  [m, n]
+ *    wq/wd are the two planes of an array of block_q4_0: byte j of a block
+ *    holds element j in its low nibble and element j+16 in its high nibble;
+ *    the 16 bytes of block b of row r start at wq + r*k/2 + 16*b.
+ *  - Rounding: quantizers divide in IEEE f32 and round half away from zero;
+ *    stored scales are fp16 round-to-nearest-even of the f32 scale.
+ *  - Requires a device of compute capability 10.3 (GB300); any other device
+ *    gives QMM_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qmm_status {
+    QMM_OK = 0,
+    QMM_ERR_NULL = 1,               /* a required pointer is NULL */
+    QMM_ERR_SHAPE = 2,              /* a size is <= 0, too large, or not a block multiple */
+    QMM_ERR_ALIGN = 3,              /* a pointer lacks the alignment stated for it */
+    QMM_ERR_WORKSPACE = 4,          /* workspace NULL or smaller than qmm_workspace_bytes() */
+    QMM_ERR_UNSUPPORTED_DEVICE = 5, /* the current device is not compute capability 10.3 */
+    QMM_ERR_CUDA = 6,               /* a CUDA runtime call or a kernel launch failed */
+    QMM_ERR_TIMEOUT = 7,            /* a bounded device-side wait gave up (see qmm_check_device_error) */
+    QMM_ERR_ARG = 8                 /* another invalid argument (split_k, op id, path id) */
+} qmm_status;
+
+/* Workspace-taking operations, for qmm_workspace_bytes(). */
+enum {
+    QMM_OP_GEMV_Q4_0_Q8_0 = 1,
+    QMM_OP_GEMM_Q4_0_Q8_0 = 2
+};
+
+/* Largest m accepted by the GEMV entry points (decode and small batches). */
+#define QMM_GEMV_MAX_M 16
+
+/* ---------------------------------------------------------------------- */
+/* Activation quantization to Q8_0 (lesson 31, "How the quantized dot product
+ * works": activations are Q8_0 int8 blocks with an fp16 scale).  For every
+ * row i and block b: amax = max |x|, d = amax / 127 (f32), q = 0 if d == 0
+ * else clamp(round(x / d), -127, 127); ad = fp16(d).
+ *   x    f32 [m, ldx] (only the first k columns are read); 4-byte aligned
+ *   aq   int8 [m, k] output;  ad  fp16 bits [m, k/32] output, 2-byte aligned
+ *   k % 32 == 0, ldx >= k.  Inputs must be finite. */
+qmm_status qmm_quantize_act_q8_0(const float *x, int64_t m, int64_t k, int64_t ldx,
+                                 int8_t *aq, uint16_t *ad, void *stream);
+
+/* Weight quantization to Q4_0 (load-time, not on the per-token path).  For
+ * every row and block: the element of largest |w| (first one on ties) keeps
+ * its sign as `max`; d = max / -8; q = 8 if d == 0 else
+ * clamp(round(w / d) + 8, 0, 15); packed as described above; wd = fp16(d).
+ *   w   f32 [n, k], 4-byte aligned;  wq u8 [n, k/2];  wd fp16 bits [n, k/32]
+ *   k % 32 == 0.  Inputs must be finite. */
+qmm_status qmm_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
+                                    uint8_t *wq, uint16_t *wd, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Q4_0 x Q8_0 matrix-vector product for decode (1 <= m <= QMM_GEMV_MAX_M):
+ *   y[i, r] = sum over blocks b of sumi[i, r, b] * (dw[r, b] * da[i, b]),
+ * sumi exact in int32, the scaled terms accumulated in f32 (the order differs
+ * from a serial loop; results agree to f32 rounding).  Weights stream once
+ * from HBM for all m rows.
+ *   wq 16-byte aligned; aq 16-byte aligned; wd, ad 2-byte aligned; y 4-byte.
+ *   k % 32 == 0.
+ *   split_k: 1 = no split; S > 1 = the k range is cut into S slices whose f32
+ *   partials go to the workspace and are summed in slice order by a second
+ *   kernel on the same stream (deterministic); 0 = the library picks S from
+ *   the shape.  S may not exceed k/32.  workspace: device memory of at least
+ *   qmm_workspace_bytes(QMM_OP_GEMV_Q4_0_Q8_0, m, n, k, split_k) bytes,
+ *   16-byte aligned (NULL allowed when that size is 0). */
+qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
+                              const int8_t *aq, const uint16_t *ad, float *y,
+                              int64_t m, int64_t n, int64_t k, int split_k,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Q4_0 x Q8_0 matrix product for prefill (m >= 1, any n, k % 32 == 0), same
+ * result definition as the GEMV.  The block sums run on the tensor cores
+ * (tcgen05.mma kind::f16 with f32 accumulators in TMEM): the int4 and int8
+ * values are exact in fp16 and every partial sum is an integer below 2^24,
+ * so each block sum is exact; each f32 output then accumulates
+ * fma(sumi, dw*da, acc) over blocks in ascending order.  The workspace holds
+ * an fp16 copy of the activations and the transposed activation scales.
+ *   wq 16-byte aligned; aq 16-byte aligned; wd, ad 2-byte aligned; y 4-byte;
+ *   workspace 256-byte aligned, at least
+ *   qmm_workspace_bytes(QMM_OP_GEMM_Q4_0_Q8_0, m, n, k, 0) bytes.
+ *   Not reentrant on one workspace: calls that share a workspace must be
+ *   ordered on one stream. */
+qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
+                              const int8_t *aq, const uint16_t *ad, float *y,
+                              int64_t m, int64_t n, int64_t k,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* BitNet activation quantization (Loom, "BitNet ternary MAD kernel"): per row
+ * s = 127 / max|x| (s = 0 for an all-zero row), q = clamp(round(x * s),
+ * -127, 127), act_sum = sum q.
+ *   x f32 [m, k] 4-byte aligned; aq int8 [m, k]; act_scale f32 [m];
+ *   act_sum int32 [m].  k % 16 == 0.  Inputs must be finite. */
+qmm_status qmm_quantize_act_bitnet(const float *x, int64_t m, int64_t k,
+                                   int8_t *aq, float *act_scale, int32_t *act_sum,
+                                   void *stream);
+
+/* Pack ternary weights t in {-1, 0, +1} (int8 [n, k]) as code = t + 1,
+ * 16 codes per uint32, element i of each word at bits [2i, 2i+1] (load-time).
+ * Values outside {-1, 0, 1} give unspecified codes.  k % 16 == 0;
+ * w uint32 [n, k/16], 4-byte aligned. */
+qmm_status qmm_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t *w,
+                            void *stream);
+
+/* BitNet ternary matrix-vector product (1 <= m <= QMM_GEMV_MAX_M):
+ *   dot[i, r] = sum_j code[r, j] * aq[i, j] - act_sum[i]   (exact int32)
+ *   y[i, r]   = act_scale[i] == 0 ? 0 : ((float)dot * weight_absmean) / act_scale[i]
+ * (two IEEE f32 operations, left to right, so y is reproducible bit for bit).
+ *   w uint32 [n, k/16] 16-byte aligned; aq 16-byte aligned; k % 16 == 0,
+ *   k <= 2^21 (so |dot| fits int32). */
+qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean,
+                           const int8_t *aq, const float *act_scale, const int32_t *act_sum,
+                           float *y, int64_t m, int64_t n, int64_t k, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Workspace size in bytes for `op` (QMM_OP_*) at this shape; 0 when none is
+ * needed; SIZE_MAX for an invalid op or shape. */
+size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k);
+
+/* The split-K factor qmm_gemv_q4_0_q8_0 uses for split_k = 0 at this shape. */
+int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k);
+
+/* Reads and clears the library's device error word after synchronizing
+ * `stream`.  QMM_OK if no kernel reported an error since the last call;
+ * QMM_ERR_TIMEOUT if a bounded wait inside a kernel gave up (the kernel then
+ * stopped early and its outputs are unspecified); QMM_ERR_CUDA if the
+ * synchronization itself failed.  This is the only entry point that blocks
+ * the host. */
+qmm_status qmm_check_device_error(void *stream);
+
+/* A static, human-readable name for a status code. */
+const char *qmm_status_string(qmm_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qmm_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* Test entry points.  They run the same kernels as the product entry points
+ * compiled to also emit their intermediate integers, so tests can compare
+ * them bit for bit with a reference.  Not for production use. */
+
+/* Per-block sums sumi int32 [m, n, k/32] = sum_j (nibble_j - 8) * q_j.
+ * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the tensor-
+ * core GEMM kernel (needs the GEMM workspace).  Same alignment rules as the
+ * product entry points; sumi 4-byte aligned. */
+qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int8_t *aq,
+                                          int32_t *sumi, int64_t m, int64_t n, int64_t k,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream);
+
+/* BitNet integer dots dot int32 [m, n] from the ternary GEMV kernel. */
+qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32_t *act_sum,
+                                int32_t *dot, int64_t m, int64_t n, int64_t k, void *stream);
+
+/* Upper bound on the polling iterations of every bounded wait inside the
+ * GEMM kernel (default 1 << 26; 0 restores the default).  Tests lower it to
+ * make a wait give up on purpose and check that QMM_ERR_TIMEOUT comes back
+ * while the device stays usable.  Affects kernels launched after the call. */
+void qmm_debug_set_wait_limit(uint32_t iterations);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

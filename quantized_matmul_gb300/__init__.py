@@ -1,0 +1,298 @@
+"""quantized_matmul_gb300 -- Q4_0 x Q8_0 and BitNet ternary matmul on GB300.
+
+A thin ctypes binding over the C ABI of ``libqmm.so`` (declared in
+``include/qmm.h``).  Every function marshals torch tensors (device memory,
+dtype and shape checks) and the current CUDA stream into one C call; all
+arithmetic runs in the library's CUDA kernels.  There is no CPU fallback:
+if the library is missing or does not load, every call raises.
+
+Tensor conventions (row-major, contiguous, on the current CUDA device):
+  x   float32 [m, k]            activations
+  aq  int8    [m, k]            Q8_0 codes;  ad float16 [m, k/32] scales
+  wq  uint8   [n, k/2]          Q4_0 nibbles; wd float16 [n, k/32] scales
+  y   float32 [m, n]
+  tw  int32   [n, k/16]         packed ternary codes (uint32 bit patterns)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqmm.so")
+
+QK = 32
+GEMV_MAX_M = 16
+OP_GEMV = 1
+OP_GEMM = 2
+
+STATUS_NAMES = {0: "ok", 1: "null pointer", 2: "invalid shape", 3: "misaligned pointer",
+                4: "workspace missing or too small", 5: "unsupported device", 6: "CUDA error",
+                7: "device-side wait timed out", 8: "invalid argument"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: qmm status {status} ({STATUS_NAMES.get(status, '?')})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libqmm.so (built in-tree by ``quantized_matmul_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m quantized_matmul_gb300.build` (there is no fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I64, I, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+        F, SZ = ctypes.c_float, ctypes.c_size_t
+        sigs = {
+            "qmm_quantize_act_q8_0": (I, [P, I64, I64, I64, P, P, P]),
+            "qmm_quantize_weight_q4_0": (I, [P, I64, I64, P, P, P]),
+            "qmm_gemv_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
+            "qmm_gemm_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+            "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
+            "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
+            "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
+            "qmm_workspace_bytes": (SZ, [I, I64, I64, I64, I]),
+            "qmm_gemv_auto_split": (I, [I64, I64, I64]),
+            "qmm_check_device_error": (I, [P]),
+            "qmm_status_string": (ctypes.c_char_p, [I]),
+            "qmm_version": (I, []),
+            "qmm_debug_block_sums_q4_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
+            "qmm_debug_bitnet_dot": (I, [P, P, P, P, I64, I64, I64, P]),
+            "qmm_debug_set_wait_limit": (None, [U32]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise QmmError(status, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream() -> int:
+    torch = _torch()
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dev(t, dtype, name: str, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _empty(shape, dtype, like):
+    return _torch().empty(shape, dtype=dtype, device=like.device)
+
+
+# ---------------------------------------------------------------------------
+# Q4_0 x Q8_0
+
+def quantize_act_q8_0(x, aq=None, ad=None):
+    """f32 [m, k] -> (aq int8 [m, k], ad fp16 [m, k/32])."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    m, k = x.shape
+    aq = _empty((m, k), torch.int8, x) if aq is None else aq
+    ad = _empty((m, k // QK), torch.float16, x) if ad is None else ad
+    st = load().qmm_quantize_act_q8_0(_dev(x, torch.float32, "x"), m, k, k,
+                                      _dev(aq, torch.int8, "aq", (m, k)),
+                                      _dev(ad, torch.float16, "ad", (m, k // QK)), _stream())
+    _check(st, "qmm_quantize_act_q8_0")
+    return aq, ad
+
+
+def quantize_weight_q4_0(w, wq=None, wd=None):
+    """f32 [n, k] -> (wq uint8 [n, k/2], wd fp16 [n, k/32])."""
+    torch = _torch()
+    n, k = w.shape
+    wq = _empty((n, k // 2), torch.uint8, w) if wq is None else wq
+    wd = _empty((n, k // QK), torch.float16, w) if wd is None else wd
+    st = load().qmm_quantize_weight_q4_0(_dev(w, torch.float32, "w"), n, k,
+                                         _dev(wq, torch.uint8, "wq", (n, k // 2)),
+                                         _dev(wd, torch.float16, "wd", (n, k // QK)), _stream())
+    _check(st, "qmm_quantize_weight_q4_0")
+    return wq, wd
+
+
+def workspace_bytes(op: int, m: int, n: int, k: int, split_k: int = 0) -> int:
+    v = load().qmm_workspace_bytes(op, m, n, k, split_k)
+    if v == ctypes.c_size_t(-1).value:
+        raise ValueError(f"invalid workspace query op={op} m={m} n={n} k={k} split_k={split_k}")
+    return int(v)
+
+
+def gemv_auto_split(m: int, n: int, k: int) -> int:
+    return int(load().qmm_gemv_auto_split(m, n, k))
+
+
+def _workspace(ws, need, like):
+    torch = _torch()
+    if need == 0:
+        return None, 0
+    if ws is None:
+        ws = _empty((need,), torch.uint8, like)
+    if ws.numel() < need:
+        raise ValueError(f"workspace has {ws.numel()} bytes, needs {need}")
+    return ws, ws.numel()
+
+
+def _q4_shapes(wq, wd, aq, ad):
+    torch = _torch()
+    n = wq.shape[0]
+    m, k = aq.shape
+    _dev(wq, torch.uint8, "wq", (n, k // 2))
+    _dev(wd, torch.float16, "wd", (n, k // QK))
+    _dev(aq, torch.int8, "aq", (m, k))
+    _dev(ad, torch.float16, "ad", (m, k // QK))
+    return m, n, k
+
+
+def gemv_q4_0_q8_0(wq, wd, aq, ad, y=None, split_k: int = 0, workspace=None):
+    """Decode GEMV (m <= 16): y f32 [m, n]."""
+    torch = _torch()
+    m, n, k = _q4_shapes(wq, wd, aq, ad)
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMV, m, n, k, split_k)
+                              if m <= GEMV_MAX_M else 0, aq)
+    st = load().qmm_gemv_q4_0_q8_0(wq.data_ptr(), wd.data_ptr(), aq.data_ptr(), ad.data_ptr(),
+                                   _dev(y, torch.float32, "y", (m, n)), m, n, k, split_k,
+                                   ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
+    _check(st, "qmm_gemv_q4_0_q8_0")
+    return y
+
+
+def gemm_q4_0_q8_0(wq, wd, aq, ad, y=None, workspace=None):
+    """Prefill GEMM on the tensor cores: y f32 [m, n]."""
+    torch = _torch()
+    m, n, k = _q4_shapes(wq, wd, aq, ad)
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM, m, n, k), aq)
+    st = load().qmm_gemm_q4_0_q8_0(wq.data_ptr(), wd.data_ptr(), aq.data_ptr(), ad.data_ptr(),
+                                   _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                   ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
+    _check(st, "qmm_gemm_q4_0_q8_0")
+    return y
+
+
+def linear_q4_0(x, wq, wd, y=None, gemv_max_m: int = GEMV_MAX_M):
+    """y = x @ dequant(W)^T: quantize x to Q8_0, then the GEMV for m <=
+    gemv_max_m and the tensor-core GEMM above it."""
+    aq, ad = quantize_act_q8_0(x)
+    if aq.shape[0] <= gemv_max_m:
+        return gemv_q4_0_q8_0(wq, wd, aq, ad, y=y)
+    return gemm_q4_0_q8_0(wq, wd, aq, ad, y=y)
+
+
+# ---------------------------------------------------------------------------
+# BitNet ternary
+
+def quantize_act_bitnet(x):
+    """f32 [m, k] -> (aq int8 [m, k], act_scale f32 [m], act_sum int32 [m])."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    m, k = x.shape
+    aq = _empty((m, k), torch.int8, x)
+    s = _empty((m,), torch.float32, x)
+    asum = _empty((m,), torch.int32, x)
+    st = load().qmm_quantize_act_bitnet(_dev(x, torch.float32, "x"), m, k, aq.data_ptr(),
+                                        s.data_ptr(), asum.data_ptr(), _stream())
+    _check(st, "qmm_quantize_act_bitnet")
+    return aq, s, asum
+
+
+def pack_ternary(t):
+    """int8 {-1,0,1} [n, k] -> int32 [n, k/16] (uint32 bit patterns)."""
+    torch = _torch()
+    n, k = t.shape
+    w = _empty((n, k // 16), torch.int32, t)
+    st = load().qmm_pack_ternary(_dev(t, torch.int8, "t"), n, k, w.data_ptr(), _stream())
+    _check(st, "qmm_pack_ternary")
+    return w
+
+
+def bitnet_gemv(tw, weight_absmean: float, aq, act_scale, act_sum, y=None):
+    torch = _torch()
+    n = tw.shape[0]
+    m, k = aq.shape
+    _dev(tw, torch.int32, "tw", (n, k // 16))
+    _dev(aq, torch.int8, "aq", (m, k))
+    _dev(act_scale, torch.float32, "act_scale", (m,))
+    _dev(act_sum, torch.int32, "act_sum", (m,))
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    st = load().qmm_bitnet_gemv(tw.data_ptr(), float(weight_absmean), aq.data_ptr(),
+                                act_scale.data_ptr(), act_sum.data_ptr(),
+                                _dev(y, torch.float32, "y", (m, n)), m, n, k, _stream())
+    _check(st, "qmm_bitnet_gemv")
+    return y
+
+
+# ---------------------------------------------------------------------------
+# errors and test hooks
+
+def check_device_error() -> int:
+    """Synchronizes the current stream and returns (and clears) the device
+    error status: 0 ok, 7 a bounded wait gave up."""
+    return int(load().qmm_check_device_error(_stream()))
+
+
+def debug_block_sums(path: int, wq, aq, workspace=None):
+    """int32 [m, n, k/32] block sums from the GEMV (path 0) or GEMM (path 1) kernel."""
+    torch = _torch()
+    n = wq.shape[0]
+    m, k = aq.shape
+    _dev(wq, torch.uint8, "wq", (n, k // 2))
+    _dev(aq, torch.int8, "aq", (m, k))
+    sumi = _empty((m, n, k // QK), torch.int32, aq)
+    ws, ws_bytes = (None, 0)
+    if path == 1:
+        ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM, m, n, k), aq)
+    st = load().qmm_debug_block_sums_q4_0_q8_0(path, wq.data_ptr(), aq.data_ptr(), sumi.data_ptr(),
+                                               m, n, k, ws.data_ptr() if ws is not None else None,
+                                               ws_bytes, _stream())
+    _check(st, "qmm_debug_block_sums_q4_0_q8_0")
+    return sumi
+
+
+def debug_bitnet_dot(tw, aq, act_sum):
+    torch = _torch()
+    n = tw.shape[0]
+    m, k = aq.shape
+    dot = _empty((m, n), torch.int32, aq)
+    st = load().qmm_debug_bitnet_dot(tw.data_ptr(), aq.data_ptr(), act_sum.data_ptr(),
+                                     dot.data_ptr(), m, n, k, _stream())
+    _check(st, "qmm_debug_bitnet_dot")
+    return dot
+
+
+def set_wait_limit(iterations: int) -> None:
+    load().qmm_debug_set_wait_limit(int(iterations))

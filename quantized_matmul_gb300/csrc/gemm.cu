@@ -1,0 +1,685 @@
+// Prefill-shaped Q4_0 x Q8_0 product on the 5th-generation tensor cores.
+//
+// What it computes (llama.cpp visual guide, lesson 31 "The CPU backend",
+// section "How the quantized dot product works"): for every output
+// y[t, n] = sum over blocks b of sumi[t, n, b] * (dw[n, b] * da[t, b]) where
+// sumi is the exact integer dot of the 32 nibbles (minus 8) with the 32 int8
+// activations of the block.
+//
+// How (GB300, sm_103a).  There is no int8 MMA on sm_103a, but every operand
+// value is a small integer that fp16 holds exactly (weights -8..7,
+// activations -127..127) and every partial sum of one block is an integer of
+// magnitude <= 32 * 8 * 127 < 2^24, so tcgen05.mma kind::f16 with an f32
+// accumulator produces each block sum exactly.  The scales differ per block,
+// so each block gets its own accumulator in TMEM and is drained and scaled
+// by CUDA cores while the tensor core already computes the next block.
+//
+// One CTA computes a tile of 128 weight rows (the MMA's M, TMEM lanes) by BN
+// tokens (the MMA's N, TMEM columns).  Roles (384 threads):
+//   warp 0      TMA producer: per stage of 2 blocks (64 k-elements) it loads
+//               the 128 x 32 B nibble tile, the BN x 64 fp16 activation tile
+//               (128-byte swizzle) and the 2 x BN f32 activation scales.
+//   warp 1      allocates TMEM; one thread issues the MMAs (2 x K=16 per
+//               block into accumulator buffer b % NACC) and commits.
+//   warps 2-3   convert nibbles to fp16 (value - 8) into the 128-byte-swizzled
+//               K-major A tile the MMA reads.
+//   warps 4-11  epilogue: thread (warp % 4, lane) owns weight row n; each of
+//               the two warp groups owns half of the BN columns.  For every
+//               block it loads the accumulator from TMEM and applies
+//               acc = fma(sumi, dw * da, acc), blocks in ascending order -- the
+//               same order and operations as the serial definition, so the
+//               result is reproducible bit for bit.
+// An activation prepass (same stream) writes the fp16 copy of the int8
+// activations and the transposed f32 activation scales into the workspace.
+//
+// Every mbarrier wait is bounded.  On expiry a kernel raises a CTA-wide abort
+// flag, records QMM_ERR_TIMEOUT in a device error word, waits (bounded) for
+// its own TMA copies and MMAs still in flight, releases TMEM and returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kBM = 128;               // weight rows per tile (MMA M)
+constexpr int kBK = 64;                // k-elements per pipeline stage (two blocks)
+constexpr int kStages = 4;
+constexpr int kNacc = 4;               // TMEM accumulator buffers
+constexpr int kThreads = 384;
+constexpr int kConvWarps = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 4;
+constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kDrainLimit = 1u << 22;
+
+__device__ unsigned int g_gemm_error = 0;
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase completed; false after `limit` polls or
+// when another role raised the abort flag (the error word is then set).
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                             volatile int *abort_flag) {
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag || it >= limit) {
+            *abort_flag = 1;
+            atomicOr(&g_gemm_error, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait for roles whose lanes all wait and then run
+// warp-collective code: if any lane gave up, every lane sees failure.
+__device__ __forceinline__ bool wait_bounded_warp(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                                  volatile int *abort_flag) {
+    const bool ok = wait_bounded(bar, parity, limit, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tcgen05 descriptor format:
+// start >> 4 at bits 0-13, leading offset >> 4 at 16-29, stride offset >> 4
+// at 32-45, version 1 at bit 46, swizzle mode 2 (128B) at bits 61-63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator (bits 4-5 = 1), A and B
+// fp16 (format 0), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ float h2f(unsigned short h) { return __half2float(__ushort_as_half(h)); }
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+// 16 nibble bytes of one block -> 32 fp16 values (nibble - 8) in element
+// order: element j is the low nibble of byte j, element j+16 the high one.
+// Exact: fp16 holds every integer in [-8, 7].  The fp16 bit pattern
+// 0x6400 | v is the value 1024 + v (v < 1024), so a low nibble becomes
+// (0x6400 | v) - 1032 and a high nibble, left at bits 4..7, becomes
+// (0x6400 | 16 v) / 16 - 72; every step is exact.
+__device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const __half2 off = u32_as_h2(0x64086408u);        // (1032, 1032)
+    const __half2 sixteenth = u32_as_h2(0x2C002C00u);  // (1/16, 1/16)
+    const __half2 m72 = u32_as_h2(0xD480D480u);        // (-72, -72)
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bytes (b0, b1) and (b2, b3) of word i spread to the two 16-bit halves
+        const uint32_t p0 = __byte_perm(w[i], 0, 0x4140);
+        const uint32_t p1 = __byte_perm(w[i], 0, 0x4342);
+        lo[2 * i] = h2_as_u32(__hsub2(u32_as_h2((p0 & 0x000F000Fu) | 0x64006400u), off));
+        lo[2 * i + 1] = h2_as_u32(__hsub2(u32_as_h2((p1 & 0x000F000Fu) | 0x64006400u), off));
+        hi[2 * i] = h2_as_u32(__hfma2(u32_as_h2((p0 & 0x00F000F0u) | 0x64006400u), sixteenth, m72));
+        hi[2 * i + 1] = h2_as_u32(__hfma2(u32_as_h2((p1 & 0x00F000F0u) | 0x64006400u), sixteenth, m72));
+    }
+    out[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);  // elements 0..7
+    out[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);  // elements 8..15
+    out[2] = make_uint4(hi[0], hi[1], hi[2], hi[3]);  // elements 16..23
+    out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // elements 24..31
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory plan (dynamic; the base is rounded up to 1024 bytes)
+
+template <int BN>
+struct Smem {
+    static constexpr int kA = kBM * kBK * 2;        // fp16 weights, 16 KB
+    static constexpr int kB = BN * kBK * 2;         // fp16 activations
+    static constexpr int kNib = kBM * (kBK / 2);    // nibble bytes, 4 KB
+    static constexpr int kDa = 2 * BN * 4;          // f32 activation scales
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kA;
+    static constexpr int kOffNib = kOffB + kStages * kB;
+    static constexpr int kOffDa = kOffNib + kStages * kNib;
+    static constexpr int kOffBar = kOffDa + kStages * kDa;
+    static constexpr int kNumBars = 3 * kStages + 2 * kNacc + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte round-up
+    static constexpr uint32_t kTx = kNib + kB + kDa;
+};
+
+template <int BN, bool EMIT>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
+                      const __grid_constant__ CUtensorMap tm_act,
+                      const __grid_constant__ CUtensorMap tm_da,
+                      const unsigned short *__restrict__ wd, float *__restrict__ y,
+                      int32_t *__restrict__ sumi, int m, int n, int kb_total,
+                      uint32_t wait_limit) {
+    using S = Smem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
+    uint64_t *bar_load = bar;                  // TMA landed (tx) + producer arrive
+    uint64_t *bar_conv = bar + kStages;        // A tile converted (conv warps)
+    uint64_t *bar_empty = bar + 2 * kStages;   // MMA done + epilogue read scales
+    uint64_t *bar_accf = bar + 3 * kStages;    // accumulator buffer full
+    uint64_t *bar_acce = bar_accf + kNacc;     // accumulator buffer drained
+    uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * BN;   // first token of the tile
+    const int n0 = blockIdx.y * kBM;  // first weight row of the tile
+    const int num_stages = (kb_total + 1) / 2;
+    constexpr uint32_t kTmemCols = (uint32_t)(kNacc * BN) < 32 ? 32 : (uint32_t)(kNacc * BN);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar_load[s], 1);
+            mbar_init(&bar_conv[s], kConvWarps);
+            mbar_init(&bar_empty[s], 1 + kEpiWarps);
+        }
+        for (int b = 0; b < kNacc; ++b) {
+            mbar_init(&bar_accf[b], 1);
+            mbar_init(&bar_acce[b], kEpiWarps);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tmap_prefetch(&tm_nib);
+        tmap_prefetch(&tm_act);
+        tmap_prefetch(&tm_da);
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int issued = 0;
+        if (lane == 0) {
+            for (int it = 0; it < num_stages; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                if (!wait_bounded(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_load[s], S::kTx);
+                tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * (kBK / 2), n0);
+                tma_load_2d(smem + S::kOffB + s * S::kB, &tm_act, &bar_load[s], it * kBK, t0);
+                tma_load_2d(smem + S::kOffDa + s * S::kDa, &tm_da, &bar_load[s], t0, 2 * it);
+                issued = it + 1;
+            }
+            // Never leave a copy in flight: wait for every stage still pending.
+            for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it) {
+                volatile int no_abort = 0;
+                wait_bounded(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
+                             &no_abort);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kBM, BN);
+            bool ok = true;
+            int issued_any = 0;
+            for (int it = 0; it < num_stages && ok; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + S::kOffA + s * S::kA);
+                const uint32_t b_base = smem_u32(smem + S::kOffB + s * S::kB);
+                for (int h = 0; h < 2; ++h) {
+                    const int kbi = 2 * it + h;
+                    if (kbi >= kb_total) break;
+                    const int buf = kbi % kNacc;
+                    const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
+                    if (!wait_bounded(&bar_acce[buf], aph ^ 1u, wait_limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t koff = (uint32_t)(h * 64 + u * 32);  // bytes along k
+                        mma_f16(d_tmem, smem_desc_sw128(a_base + koff), smem_desc_sw128(b_base + koff),
+                                idesc, (uint32_t)u);
+                    }
+                    mma_commit(&bar_accf[buf]);
+                    issued_any = 1;
+                }
+                if (ok) mma_commit(&bar_empty[s]);
+            }
+            // Wait until every MMA issued by this thread has finished.
+            if (issued_any) {
+                mma_commit(bar_drain);
+                volatile int no_abort = 0;
+                wait_bounded(bar_drain, 0, kDrainLimit, &no_abort);
+            }
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - 64;  // 0..63
+        for (int it = 0; it < num_stages; ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
+            const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
+            uint8_t *a_tile = smem + S::kOffA + s * S::kA;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int unit = ct + 64 * j;  // (row, block) pair, contiguous in the nibble tile
+                const int row = unit >> 1, blk = unit & 1;
+                const uint4 v = *reinterpret_cast<const uint4 *>(nib + unit * 16);
+                uint4 out[4];
+                unpack_block_f16(v, out);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = (blk * 4 + c) ^ (row & 7);
+                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + chunk * 16) = out[c];
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_conv[s]);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        constexpr int kCols = BN / 2;            // columns per thread
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int half = (warp - kEpiWarp0) >> 2;
+        const int row = n0 + 32 * q + lane;      // weight row owned by this thread
+        const int c0 = half * kCols;             // first column (token) in the tile
+        const bool row_ok = row < n;
+        float acc[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) acc[c] = 0.0f;
+        bool ok = true;
+        for (int it = 0; it < num_stages && ok; ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
+            const float *da_tile = reinterpret_cast<const float *>(smem + S::kOffDa + s * S::kDa);
+            for (int h = 0; h < 2; ++h) {
+                const int kbi = 2 * it + h;
+                if (kbi >= kb_total) break;
+                const int buf = kbi % kNacc;
+                const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
+                const float dw =
+                    (!EMIT && row_ok) ? h2f(__ldg(wd + (int64_t)row * kb_total + kbi)) : 0.0f;
+                if (!wait_bounded_warp(&bar_accf[buf], aph, wait_limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + c0);
+                uint32_t v[kCols];
+                if constexpr (kCols >= 16) {
+#pragma unroll
+                    for (int g = 0; g < kCols / 16; ++g) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + 16 * g, r);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[16 * g + i] = r[i];
+                    }
+                } else {
+                    uint32_t r[8];
+                    tmem_ld8(taddr, r);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = r[i];
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_acce[buf]);
+                if constexpr (EMIT) {
+                    if (row_ok) {
+#pragma unroll
+                        for (int c = 0; c < kCols; ++c) {
+                            const int t = t0 + c0 + c;
+                            if (t < m)
+                                sumi[((int64_t)t * n + row) * kb_total + kbi] =
+                                    __float2int_rn(__uint_as_float(v[c]));
+                        }
+                    }
+                } else {
+                    const float *dar = da_tile + h * BN + c0;
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) {
+                        const float sc = __fmul_rn(dw, dar[c]);
+                        acc[c] = fmaf(__uint_as_float(v[c]), sc, acc[c]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&bar_empty[s]);
+        }
+        if (!EMIT && ok && !*abort_flag && row_ok) {
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                const int t = t0 + c0 + c;
+                if (t < m) y[(int64_t)t * n + row] = acc[c];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// Activation prepass: int8 -> fp16 (exact) and fp16 scales -> transposed f32.
+__global__ void gemm_prep_kernel(const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
+                                 __half *__restrict__ a16, float *__restrict__ daT, int64_t m,
+                                 int64_t k, int64_t m4) {
+    const int64_t kb = k / kQK;
+    const int64_t n16 = m * k / 16;  // 16-element groups
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n16; g += stride) {
+        const int4 v = reinterpret_cast<const int4 *>(aq)[g];
+        const int w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int lo = (int)(int8_t)((w[i] >> (16 * j)) & 0xff);
+                const int hi = (int)(int8_t)((w[i] >> (16 * j + 8)) & 0xff);
+                __half2 hv = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+                o[2 * i + j] = *reinterpret_cast<uint32_t *>(&hv);
+            }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(a16) + 2 * g;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    const int64_t nda = kb * m4;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < nda; g += stride) {
+        const int64_t b = g / m4, t = g - b * m4;
+        daT[g] = (t < m && ad != nullptr) ? h2f(ad[t * kb + b]) : 0.0f;  // no scales: block-sum variant
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle sw) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int choose_bn(int64_t m) {
+    if (m <= 16) return 16;
+    if (m <= 32) return 32;
+    if (m <= 64) return 64;
+    return 128;
+}
+
+struct WsPlan {
+    size_t a16_off, a16_bytes, da_off, da_bytes, total;
+    int64_t m4;
+};
+
+WsPlan plan_ws(int64_t m, int64_t k) {
+    WsPlan p;
+    p.m4 = (m + 3) / 4 * 4;
+    p.a16_off = 0;
+    p.a16_bytes = (size_t)m * (size_t)k * 2;
+    p.da_off = (p.a16_bytes + 255) / 256 * 256;
+    p.da_bytes = (size_t)(k / kQK) * (size_t)p.m4 * 4;
+    p.total = p.da_off + (p.da_bytes + 255) / 256 * 256;
+    return p;
+}
+
+uint32_t g_wait_limit = 1u << 24;
+
+template <int BN>
+cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &da,
+                        const uint16_t *wd, float *y, int32_t *sumi, int64_t m, int64_t n,
+                        int64_t k, cudaStream_t s) {
+    using S = Smem<BN>;
+    const int kb = (int)(k / kQK);
+    dim3 grid((unsigned)((m + BN - 1) / BN), (unsigned)((n + kBM - 1) / kBM));
+    const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
+    if (sumi) {
+        auto kern = gemm_q4_0_q8_0_kernel<BN, true>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
+        kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
+                                               g_wait_limit);
+    } else {
+        auto kern = gemm_q4_0_q8_0_kernel<BN, false>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
+        kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
+                                               g_wait_limit);
+    }
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t m, int64_t /*n*/, int64_t k) { return plan_ws(m, k).total; }
+
+void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : (1u << 24); }
+
+cudaError_t gemm_read_and_clear_error(unsigned int *word, cudaStream_t s) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_gemm_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*word) {
+        e = cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    const WsPlan p = plan_ws(m, k);
+    auto *ws = static_cast<uint8_t *>(workspace);
+    __half *a16 = reinterpret_cast<__half *>(ws + p.a16_off);
+    float *daT = reinterpret_cast<float *>(ws + p.da_off);
+    {
+        const int threads = 256;
+        const int64_t work = std::max<int64_t>(m * k / 16, (k / kQK) * p.m4);
+        const int64_t blocks = std::min<int64_t>((work + threads - 1) / threads, 152 * 8);
+        gemm_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(
+            aq, reinterpret_cast<const unsigned short *>(ad), a16, daT, m, k, p.m4);
+        cudaError_t e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int bn = choose_bn(m);
+    CUtensorMap tm_nib, tm_act, tm_da;
+    // nibbles: u8 [n rows, k/2 bytes], box 32 bytes x 128 rows
+    if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)(k / 2), (uint64_t)n,
+                     (uint64_t)(k / 2), kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    // activations: fp16 [m rows, k], box 64 x BN, 128-byte swizzle
+    if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, (uint64_t)k, (uint64_t)m,
+                     (uint64_t)k * 2, kBK, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // activation scales: f32 [k/32 rows, m4], box BN x 2
+    if (!make_map_2d(&tm_da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, daT, (uint64_t)m, (uint64_t)(k / kQK),
+                     (uint64_t)p.m4 * 4, (uint32_t)bn, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    switch (bn) {
+        case 16: return launch_tile<16>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
+        case 32: return launch_tile<32>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
+        case 64: return launch_tile<64>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
+        default: return launch_tile<128>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
+    }
+}
+
+}  // namespace qmm

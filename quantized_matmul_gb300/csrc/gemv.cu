@@ -1,0 +1,385 @@
+// Decode-shaped products (m <= 16): Q4_0 x Q8_0 and BitNet ternary GEMV.
+//
+// Q4_0 x Q8_0 (llama.cpp visual guide, lesson 31 "The CPU backend", section
+// "How the quantized dot product works"): per block, sumi = sum_j
+// (nibble_j - 8) * q_j exactly in int32, then acc += sumi * (dw * da) in f32.
+// On the GPU a warp owns ROWS weight rows; lane l takes blocks l, l+32, ...
+// of every row, so each warp-wide 128-bit load reads 512 contiguous bytes of
+// one row (coalesced streaming, no reuse, L1 bypassed).  The 16 nibble bytes
+// of a block are one uint4; the low nibbles of word i are elements 4i..4i+3
+// and the high nibbles elements 16+4i..16+4i+3, which line up with
+// activation words i and 4+i, so each block is 8 dp4a (unsigned nibble x
+// signed int8) plus the -8 offset applied once per block as -8 * sum(q)
+// (computed with dp4a against 0x01010101 and shared by all ROWS rows).  The
+// per-lane f32 partials are summed by an xor-shuffle tree.  An optional
+// split over k writes f32 partials [S, m, n] to the workspace and a second
+// kernel adds them in slice order (deterministic; the prefill page of the
+// Fucina reference section 9.9.2 does the same for its split-K).
+//
+// BitNet (Loom docs, "Plan 9 SIMD Forward", section "BitNet ternary MAD
+// kernel"): dot = sum(code * q) - sum(q), exact in int32.  Codes are unpacked
+// in registers, four at a time: (word >> 2s) & 0x03030303 holds the codes of
+// elements s, s+4, s+8, s+12, and the matching activation bytes are gathered
+// with byte permutes, so each 16 weights cost four dp4a.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kWarps = 8;        // warps per CTA
+constexpr int kUnroll = 4;       // blocks (per lane, per row) loaded before use
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// unsigned bytes of a times signed bytes of b, summed into c
+__device__ __forceinline__ int dp4a_us(unsigned a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ float h2f(unsigned short h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+// ---------------------------------------------------------------------------
+// Q4_0 x Q8_0
+
+template <int MT, int ROWS, bool EMIT>
+__global__ void __launch_bounds__(kWarps * 32)
+gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__restrict__ wd,
+                      const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
+                      float *__restrict__ out, int32_t *__restrict__ sumi, int m, int64_t n,
+                      int64_t k, int64_t kb_per_split) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t kb = k / kQK;
+    const int64_t row0 = ((int64_t)blockIdx.x * kWarps + warp) * ROWS;
+    if (row0 >= n) return;
+    const int64_t kb0 = (int64_t)blockIdx.y * kb_per_split;
+    const int64_t kb1 = min(kb, kb0 + kb_per_split);
+    const int64_t wrow = k / 2;  // bytes per weight row
+
+    float acc[ROWS][MT];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[r][t] = 0.0f;
+
+    for (int64_t bb = kb0 + lane; bb < kb1; bb += 32 * kUnroll) {
+        uint4 wv[kUnroll][ROWS];
+        unsigned short dwv[kUnroll][ROWS];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t b = bb + 32 * u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const int64_t row = row0 + r;
+                if (b < kb1 && row < n) {
+                    wv[u][r] = ld_stream_v4(wq + row * wrow + b * 16);
+                    dwv[u][r] = EMIT ? (unsigned short)0 : __ldg(wd + row * kb + b);  // no scales when emitting
+                } else {
+                    wv[u][r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                    dwv[u][r] = 0;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t b = bb + 32 * u;
+            if (b >= kb1) break;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t >= m) break;
+                const int4 a0 = __ldg(reinterpret_cast<const int4 *>(aq + t * k + b * kQK));
+                const int4 a1 = __ldg(reinterpret_cast<const int4 *>(aq + t * k + b * kQK + 16));
+                const float da = EMIT ? 0.0f : h2f(__ldg(ad + t * kb + b));
+                int asum = dp4a_us(0x01010101u, a0.x, 0);
+                asum = dp4a_us(0x01010101u, a0.y, asum);
+                asum = dp4a_us(0x01010101u, a0.z, asum);
+                asum = dp4a_us(0x01010101u, a0.w, asum);
+                asum = dp4a_us(0x01010101u, a1.x, asum);
+                asum = dp4a_us(0x01010101u, a1.y, asum);
+                asum = dp4a_us(0x01010101u, a1.z, asum);
+                asum = dp4a_us(0x01010101u, a1.w, asum);
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const uint4 w = wv[u][r];
+                    int s = -8 * asum;
+                    s = dp4a_us(w.x & 0x0F0F0F0Fu, a0.x, s);
+                    s = dp4a_us(w.y & 0x0F0F0F0Fu, a0.y, s);
+                    s = dp4a_us(w.z & 0x0F0F0F0Fu, a0.z, s);
+                    s = dp4a_us(w.w & 0x0F0F0F0Fu, a0.w, s);
+                    s = dp4a_us((w.x >> 4) & 0x0F0F0F0Fu, a1.x, s);
+                    s = dp4a_us((w.y >> 4) & 0x0F0F0F0Fu, a1.y, s);
+                    s = dp4a_us((w.z >> 4) & 0x0F0F0F0Fu, a1.z, s);
+                    s = dp4a_us((w.w >> 4) & 0x0F0F0F0Fu, a1.w, s);
+                    if (EMIT) {
+                        if (row0 + r < n) sumi[((int64_t)t * n + row0 + r) * kb + b] = s;
+                    } else {
+                        const float sc = __fmul_rn(h2f(dwv[u][r]), da);
+                        acc[r][t] = fmaf((float)s, sc, acc[r][t]);
+                    }
+                }
+            }
+        }
+    }
+    if (EMIT) return;
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            float v = acc[r][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r][t] = v;
+        }
+    if (lane == 0) {
+        float *dst = out + (int64_t)blockIdx.y * m * n;  // split slice (0 when unsplit)
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            if (row0 + r >= n) break;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t >= m) break;
+                dst[(int64_t)t * n + row0 + r] = acc[r][t];
+            }
+        }
+    }
+}
+
+// y[i] = sum over slices s = 0..S-1 of partials[s][i], in that order.
+__global__ void splitk_reduce_kernel(const float *__restrict__ partials, float *__restrict__ y,
+                                     int64_t count, int splits) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    float v = partials[i];
+    for (int s = 1; s < splits; ++s) v += partials[(int64_t)s * count + i];
+    y[i] = v;
+}
+
+template <int MT, int ROWS>
+cudaError_t launch_q4(const uint8_t *wq, const uint16_t *wd, const int8_t *aq, const uint16_t *ad,
+                      float *out, int32_t *sumi, int64_t m, int64_t n, int64_t k, int split,
+                      cudaStream_t s) {
+    const int64_t kb = k / kQK;
+    const int64_t per = (kb + split - 1) / split;
+    const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
+    dim3 grid((unsigned)((n + rows_per_cta - 1) / rows_per_cta), (unsigned)split);
+    const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
+    const auto *adp = reinterpret_cast<const unsigned short *>(ad);
+    if (sumi)
+        gemv_q4_0_q8_0_kernel<MT, ROWS, true><<<grid, kWarps * 32, 0, s>>>(
+            wq, wdp, aq, adp, out, sumi, (int)m, n, k, per);
+    else
+        gemv_q4_0_q8_0_kernel<MT, ROWS, false><<<grid, kWarps * 32, 0, s>>>(
+            wq, wdp, aq, adp, out, sumi, (int)m, n, k, per);
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// BitNet ternary
+
+// Gather byte s of each of the four words into one word:
+// out_s = (a.byte s, b.byte s, c.byte s, d.byte s).
+__device__ __forceinline__ void transpose4x4(int a, int b, int c, int d, int out[4]) {
+    const int t0 = __byte_perm(a, b, 0x5140);  // a0 b0 a1 b1
+    const int t1 = __byte_perm(c, d, 0x5140);  // c0 d0 c1 d1
+    const int t2 = __byte_perm(a, b, 0x7362);  // a2 b2 a3 b3
+    const int t3 = __byte_perm(c, d, 0x7362);  // c2 d2 c3 d3
+    out[0] = __byte_perm(t0, t1, 0x5410);      // a0 b0 c0 d0
+    out[1] = __byte_perm(t0, t1, 0x7632);      // a1 b1 c1 d1
+    out[2] = __byte_perm(t2, t3, 0x5410);
+    out[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// 16 codes of `word` against 16 activations (int4 a = elements 0..15).
+__device__ __forceinline__ int ternary_dot16(uint32_t word, const int act_t[4], int acc) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) acc = dp4a_us((word >> (2 * s)) & 0x03030303u, act_t[s], acc);
+    return acc;
+}
+
+template <int MT, int ROWS, bool VEC, bool EMIT>
+__global__ void __launch_bounds__(kWarps * 32)
+bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *__restrict__ aq,
+                   const float *__restrict__ scale, const int32_t *__restrict__ asum,
+                   float *__restrict__ y, int32_t *__restrict__ dot_out, int m, int64_t n,
+                   int64_t k) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t row0 = ((int64_t)blockIdx.x * kWarps + warp) * ROWS;
+    if (row0 >= n) return;
+    const int64_t kw = k / 16;  // words per row
+    int acc[ROWS][MT];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[r][t] = 0;
+
+    if (VEC) {
+        // 4 words (64 weights) per lane per step, 128-bit loads
+        const int64_t kv = kw / 4;
+        for (int64_t jj = lane; jj < kv; jj += 32 * kUnroll) {
+            uint4 wv[kUnroll][ROWS];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t j = jj + 32 * u;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r)
+                    wv[u][r] = (j < kv && row0 + r < n)
+                                   ? ld_stream_v4(w + (row0 + r) * kw + j * 4)
+                                   : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t j = jj + 32 * u;
+                if (j >= kv) break;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t >= m) break;
+                    const int4 *ap = reinterpret_cast<const int4 *>(aq + t * k + j * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int4 a = __ldg(ap + q);
+                        int at[4];
+                        transpose4x4(a.x, a.y, a.z, a.w, at);
+#pragma unroll
+                        for (int r = 0; r < ROWS; ++r) {
+                            const uint32_t word = q == 0 ? wv[u][r].x
+                                                : q == 1 ? wv[u][r].y
+                                                : q == 2 ? wv[u][r].z
+                                                         : wv[u][r].w;
+                            acc[r][t] = ternary_dot16(word, at, acc[r][t]);
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // one word (16 weights) per lane per step
+        for (int64_t j = lane; j < kw; j += 32) {
+            uint32_t wv[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) wv[r] = (row0 + r < n) ? __ldg(w + (row0 + r) * kw + j) : 0x55555555u;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t >= m) break;
+                const int *ap = reinterpret_cast<const int *>(aq + t * k + j * 16);
+                int at[4];
+                transpose4x4(__ldg(ap), __ldg(ap + 1), __ldg(ap + 2), __ldg(ap + 3), at);
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) acc[r][t] = ternary_dot16(wv[r], at, acc[r][t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            int v = acc[r][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r][t] = v;
+        }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            if (row0 + r >= n) break;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                if (t >= m) break;
+                const int d = acc[r][t] - asum[t];
+                if (EMIT) {
+                    dot_out[(int64_t)t * n + row0 + r] = d;
+                } else {
+                    const float st = scale[t];
+                    y[(int64_t)t * n + row0 + r] =
+                        st != 0.0f ? __fdiv_rn(__fmul_rn((float)d, absmean), st) : 0.0f;
+                }
+            }
+        }
+    }
+}
+
+template <int MT, int ROWS>
+cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, const float *scale,
+                          const int32_t *asum, float *y, int32_t *dot, int64_t m, int64_t n,
+                          int64_t k, cudaStream_t s) {
+    const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
+    const unsigned grid = (unsigned)((n + rows_per_cta - 1) / rows_per_cta);
+    const bool vec = (k % 64) == 0;
+#define QMM_BITNET_LAUNCH(V, E)                                                           \
+    bitnet_gemv_kernel<MT, ROWS, V, E><<<grid, kWarps * 32, 0, s>>>(w, absmean, aq, scale, \
+                                                                    asum, y, dot, (int)m, n, k)
+    if (vec) {
+        if (dot) QMM_BITNET_LAUNCH(true, true); else QMM_BITNET_LAUNCH(true, false);
+    } else {
+        if (dot) QMM_BITNET_LAUNCH(false, true); else QMM_BITNET_LAUNCH(false, false);
+    }
+#undef QMM_BITNET_LAUNCH
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+
+int gemv_auto_split(int64_t m, int64_t n, int64_t k) {
+    // Aim for at least two CTAs per SM (152 SMs) without slices shorter than
+    // 32 blocks per lane group.
+    const int64_t kb = k / kQK;
+    const int rows_per_cta = kWarps * (m <= 2 ? 2 : 1);
+    const int64_t ctas = (n + rows_per_cta - 1) / rows_per_cta;
+    const int64_t want = 2 * 152;
+    if (ctas >= want) return 1;
+    int64_t s = (want + ctas - 1) / ctas;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, kb / 64));
+    s = std::min<int64_t>(s, 32);
+    return (int)std::max<int64_t>(1, s);
+}
+
+size_t gemv_workspace_bytes(int64_t m, int64_t n, int64_t /*k*/, int split) {
+    return split > 1 ? (size_t)split * (size_t)m * (size_t)n * sizeof(float) : 0;
+}
+
+cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, int split, float *partials,
+                                  cudaStream_t s) {
+    float *out = split > 1 ? partials : y;
+    cudaError_t e;
+    if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    else if (m == 2) e = launch_q4<2, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    else if (m <= 4) e = launch_q4<4, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    else if (m <= 8) e = launch_q4<8, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    else e = launch_q4<16, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    if (e != cudaSuccess || split <= 1 || sumi) return e;
+    const int64_t count = m * n;
+    const int threads = 256;
+    splitk_reduce_kernel<<<(unsigned)((count + threads - 1) / threads), threads, 0, s>>>(
+        partials, y, count, split);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
+                               const float *scale, const int32_t *sum, float *y, int32_t *dot,
+                               int64_t m, int64_t n, int64_t k, cudaStream_t s) {
+    if (m == 1) return launch_bitnet<1, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    if (m == 2) return launch_bitnet<2, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+}
+
+}  // namespace qmm

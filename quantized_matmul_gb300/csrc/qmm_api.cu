@@ -1,0 +1,252 @@
+// C ABI of libqmm.so (declared in include/qmm.h).
+//
+// Every entry point validates its arguments on the host and launches nothing
+// when a check fails; the kernels behind it check nothing (the split of the
+// Fucina course, chapter 06, section 6.3: validation happens once, above
+// small unchecked kernels, and output buffers come from the caller).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+namespace {
+
+using qmm::kQK;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_ok[kMaxDevices];  // 0 unknown, 1 supported, 2 not supported
+
+qmm_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return QMM_ERR_UNSUPPORTED_DEVICE;
+    int state = g_dev_ok[dev].load(std::memory_order_relaxed);
+    if (state == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return QMM_ERR_CUDA;
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_dev_ok[dev].store(state, std::memory_order_relaxed);
+    }
+    return state == 1 ? QMM_OK : QMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmm_status launch_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// Grid dimension limits of the launchers: counts that end up in a 32-bit
+// grid.x stay well below 2^31.
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+qmm_status check_q4_common(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                           const uint16_t *ad, const void *y, int64_t m, int64_t n, int64_t k) {
+    if (!wq || !wd || !aq || !ad || !y) return QMM_ERR_NULL;
+    if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return QMM_ERR_SHAPE;
+    if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 31))
+        return QMM_ERR_SHAPE;
+    if (m * k > kMaxElems || n * k > kMaxElems || m * n > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(wq, 16) || !aligned(aq, 16) || !aligned(wd, 2) || !aligned(ad, 2) ||
+        !aligned(y, 4))
+        return QMM_ERR_ALIGN;
+    return QMM_OK;
+}
+
+qmm_status gemv_split(int split_k, int64_t m, int64_t n, int64_t k, int *out) {
+    if (split_k < 0) return QMM_ERR_ARG;
+    int s = split_k == 0 ? qmm::gemv_auto_split(m, n, k) : split_k;
+    if (s > k / kQK || s > 65535) return QMM_ERR_ARG;
+    *out = s;
+    return QMM_OK;
+}
+
+qmm_status gemm_shape_ok(int64_t m, int64_t n, int64_t k) {
+    // The tensor maps use 32-bit dimensions and the tile grid uses 16-bit grid.y.
+    if (k / 2 >= (int64_t(1) << 32) || (n + 127) / 128 > 65535) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_quantize_act_q8_0(const float *x, int64_t m, int64_t k, int64_t ldx, int8_t *aq,
+                                 uint16_t *ad, void *stream) {
+    if (!x || !aq || !ad) return QMM_ERR_NULL;
+    if (m <= 0 || k <= 0 || k % kQK != 0 || ldx < k) return QMM_ERR_SHAPE;
+    if (m * k > kMaxElems || m * ldx > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(x, 4) || !aligned(ad, 2)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_quantize_act_q8_0(x, m, k, ldx, aq, ad, as_stream(stream)));
+}
+
+qmm_status qmm_quantize_weight_q4_0(const float *w, int64_t n, int64_t k, uint8_t *wq,
+                                    uint16_t *wd, void *stream) {
+    if (!w || !wq || !wd) return QMM_ERR_NULL;
+    if (n <= 0 || k <= 0 || k % kQK != 0 || n * k > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(w, 4) || !aligned(wd, 2)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_quantize_weight_q4_0(w, n, k, wq, wd, as_stream(stream)));
+}
+
+qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                              const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                              int split_k, void *workspace, size_t workspace_bytes, void *stream) {
+    if (qmm_status st = check_q4_common(wq, wd, aq, ad, y, m, n, k)) return st;
+    if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    int split = 1;
+    if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
+    const size_t need = qmm::gemv_workspace_bytes(m, n, k, split);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return QMM_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 16)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemv_q4_0_q8_0(wq, wd, aq, ad, y, nullptr, m, n, k, split,
+                                                    static_cast<float *>(workspace),
+                                                    as_stream(stream)));
+}
+
+qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                              const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    if (qmm_status st = check_q4_common(wq, wd, aq, ad, y, m, n, k)) return st;
+    if (qmm_status st = gemm_shape_ok(m, n, k)) return st;
+    const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+    if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemm_q4_0_q8_0(wq, wd, aq, ad, y, nullptr, m, n, k, workspace,
+                                                    as_stream(stream)));
+}
+
+qmm_status qmm_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t *aq,
+                                   float *act_scale, int32_t *act_sum, void *stream) {
+    if (!x || !aq || !act_scale || !act_sum) return QMM_ERR_NULL;
+    if (m <= 0 || k <= 0 || k % 16 != 0 || m >= (int64_t(1) << 31) || m * k > kMaxElems ||
+        k > (int64_t(1) << 21))
+        return QMM_ERR_SHAPE;
+    if (!aligned(x, 4) || !aligned(act_scale, 4) || !aligned(act_sum, 4)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(
+        qmm::launch_quantize_act_bitnet(x, m, k, aq, act_scale, act_sum, as_stream(stream)));
+}
+
+qmm_status qmm_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t *w, void *stream) {
+    if (!t || !w) return QMM_ERR_NULL;
+    if (n <= 0 || k <= 0 || k % 16 != 0 || n * k > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(w, 4)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_pack_ternary(t, n, k, w, as_stream(stream)));
+}
+
+static qmm_status check_bitnet(const uint32_t *w, const int8_t *aq, const float *act_scale,
+                               const int32_t *act_sum, const void *out, int64_t m, int64_t n,
+                               int64_t k) {
+    if (!w || !aq || !act_scale || !act_sum || !out) return QMM_ERR_NULL;
+    if (m <= 0 || m > QMM_GEMV_MAX_M || n <= 0 || k <= 0 || k % 16 != 0 ||
+        k > (int64_t(1) << 21) || n >= (int64_t(1) << 31) || n * k > kMaxElems)
+        return QMM_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(aq, 16) || !aligned(act_scale, 4) || !aligned(act_sum, 4) ||
+        !aligned(out, 4))
+        return QMM_ERR_ALIGN;
+    return QMM_OK;
+}
+
+qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean, const int8_t *aq,
+                           const float *act_scale, const int32_t *act_sum, float *y, int64_t m,
+                           int64_t n, int64_t k, void *stream) {
+    if (qmm_status st = check_bitnet(w, aq, act_scale, act_sum, y, m, n, k)) return st;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_bitnet_gemv(w, weight_absmean, aq, act_scale, act_sum, y,
+                                                 nullptr, m, n, k, as_stream(stream)));
+}
+
+size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k) {
+    if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return SIZE_MAX;
+    switch (op) {
+        case QMM_OP_GEMV_Q4_0_Q8_0: {
+            if (m > QMM_GEMV_MAX_M) return SIZE_MAX;
+            int split = 1;
+            if (gemv_split(split_k, m, n, k, &split) != QMM_OK) return SIZE_MAX;
+            return qmm::gemv_workspace_bytes(m, n, k, split);
+        }
+        case QMM_OP_GEMM_Q4_0_Q8_0:
+            return qmm::gemm_workspace_bytes(m, n, k);
+        default:
+            return SIZE_MAX;
+    }
+}
+
+int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k) {
+    if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return 1;
+    return qmm::gemv_auto_split(m, n, k);
+}
+
+qmm_status qmm_check_device_error(void *stream) {
+    unsigned int word = 0;
+    if (qmm::gemm_read_and_clear_error(&word, as_stream(stream)) != cudaSuccess) return QMM_ERR_CUDA;
+    return word ? QMM_ERR_TIMEOUT : QMM_OK;
+}
+
+const char *qmm_status_string(qmm_status status) {
+    switch (status) {
+        case QMM_OK: return "ok";
+        case QMM_ERR_NULL: return "null pointer";
+        case QMM_ERR_SHAPE: return "invalid shape";
+        case QMM_ERR_ALIGN: return "misaligned pointer";
+        case QMM_ERR_WORKSPACE: return "workspace missing or too small";
+        case QMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+        case QMM_ERR_CUDA: return "CUDA error";
+        case QMM_ERR_TIMEOUT: return "device-side wait timed out";
+        case QMM_ERR_ARG: return "invalid argument";
+    }
+    return "unknown status";
+}
+
+int qmm_version(void) { return 100; }
+
+qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int8_t *aq,
+                                          int32_t *sumi, int64_t m, int64_t n, int64_t k,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+    // The scale planes are not read by the block-sum variants; pass aligned
+    // dummies through the shared shape/alignment check.
+    static const uint16_t dummy[8] = {0};
+    if (!sumi) return QMM_ERR_NULL;
+    if (qmm_status st = check_q4_common(wq, dummy, aq, dummy, sumi, m, n, k)) return st;
+    if (path == 0) {
+        if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemv_q4_0_q8_0(wq, nullptr, aq, nullptr, nullptr, sumi, m,
+                                                        n, k, 1, nullptr, as_stream(stream)));
+    }
+    if (path == 1) {
+        if (qmm_status st = gemm_shape_ok(m, n, k)) return st;
+        const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+        if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+        if (qmm_status st = check_device()) return st;
+        // The block-sum variant reads no scale planes (passed as NULL).
+        return launch_status(qmm::launch_gemm_q4_0_q8_0(wq, nullptr, aq, nullptr, nullptr, sumi, m,
+                                                        n, k, workspace, as_stream(stream)));
+    }
+    return QMM_ERR_ARG;
+}
+
+qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32_t *act_sum,
+                                int32_t *dot, int64_t m, int64_t n, int64_t k, void *stream) {
+    static const float dummy_scale[4] = {0};
+    if (qmm_status st = check_bitnet(w, aq, dummy_scale, act_sum, dot, m, n, k)) return st;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_bitnet_gemv(w, 0.0f, aq, nullptr, act_sum, nullptr, dot, m, n,
+                                                 k, as_stream(stream)));
+}
+
+void qmm_debug_set_wait_limit(uint32_t iterations) { qmm::gemm_set_wait_limit(iterations); }
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: the library builds and loads, it exports every
+symbol include/qmm.h declares, and argument checks run on the host before
+anything touches the device (so every call below returns without a launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmm.h")
+
+QMM_OK, QMM_ERR_NULL, QMM_ERR_SHAPE, QMM_ERR_ALIGN, QMM_ERR_WORKSPACE = 0, 1, 2, 3, 4
+QMM_ERR_ARG = 8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_matmul_gb300 import build
+    build.build()
+    import quantized_matmul_gb300 as q
+    return q.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ["qmm_quantize_act_q8_0", "qmm_gemv_q4_0_q8_0", "qmm_gemm_q4_0_q8_0",
+                     "qmm_bitnet_gemv", "qmm_quantize_act_bitnet", "qmm_workspace_bytes",
+                     "qmm_check_device_error", "qmm_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_exports_are_unmangled_c_symbols():
+    from quantized_matmul_gb300 import build
+    build.build()
+    out = os.popen(f"nm -D --defined-only {build.LIB}").read()
+    exported = set(re.findall(r"\bT (qmm_[a-z0-9_]+)\b", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_status_strings_and_version(lib):
+    assert lib.qmm_status_string(0) == b"ok"
+    assert lib.qmm_status_string(7) == b"device-side wait timed out"
+    assert lib.qmm_status_string(99) == b"unknown status"
+    assert lib.qmm_version() >= 100
+
+
+def test_workspace_queries(lib):
+    # no split: no workspace
+    assert lib.qmm_workspace_bytes(1, 1, 4096, 4096, 1) == 0
+    # explicit split of 4 at m=2, n=100: 4 * 2 * 100 floats
+    assert lib.qmm_workspace_bytes(1, 2, 100, 4096, 4) == 4 * 2 * 100 * 4
+    # GEMM: fp16 activations + transposed f32 scales, 256-byte rounded
+    m, k = 512, 4096
+    a16 = m * k * 2
+    da = (k // 32) * m * 4
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == a16 + da
+    bad = ctypes.c_size_t(-1).value
+    assert lib.qmm_workspace_bytes(9, 1, 1, 32, 0) == bad        # unknown op
+    assert lib.qmm_workspace_bytes(1, 1, 1, 33, 0) == bad        # k not a block multiple
+    assert lib.qmm_workspace_bytes(1, 17, 1, 32, 0) == bad       # GEMV m > 16
+    assert lib.qmm_workspace_bytes(1, 1, 1, 64, 3) == bad        # more slices than blocks
+
+
+def test_auto_split_policy(lib):
+    # a narrow output with a long reduction is split, a wide one is not
+    assert lib.qmm_gemv_auto_split(1, 256, 16384) > 1
+    assert lib.qmm_gemv_auto_split(1, 128256, 4096) == 1
+    assert lib.qmm_gemv_auto_split(1, 4096, 4096) >= 1
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    A16 = _p(0x10000)  # never dereferenced: every call below fails its host checks
+    A2 = _p(0x10002)   # 2-byte aligned only
+    # null pointers
+    assert lib.qmm_quantize_act_q8_0(None, 1, 32, 32, A16, A16, None) == QMM_ERR_NULL
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, None, A16, A16, 1, 1, 32, 1, None, 0, None) == QMM_ERR_NULL
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, None, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_NULL
+    assert lib.qmm_bitnet_gemv(None, 1.0, A16, A16, A16, A16, 1, 1, 16, None) == QMM_ERR_NULL
+    # shapes
+    assert lib.qmm_quantize_act_q8_0(A16, 1, 33, 33, A16, A16, None) == QMM_ERR_SHAPE
+    assert lib.qmm_quantize_act_q8_0(A16, 1, 64, 32, A16, A16, None) == QMM_ERR_SHAPE  # ldx < k
+    assert lib.qmm_quantize_act_q8_0(A16, 0, 32, 32, A16, A16, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 17, 1, 32, 1, None, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 0, 32, 1, None, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 1, 48, A16, 1 << 20, None) == QMM_ERR_SHAPE
+    assert lib.qmm_bitnet_gemv(A16, 1.0, A16, A16, A16, A16, 1, 1, 24, None) == QMM_ERR_SHAPE
+    assert lib.qmm_bitnet_gemv(A16, 1.0, A16, A16, A16, A16, 17, 1, 16, None) == QMM_ERR_SHAPE
+    assert lib.qmm_quantize_act_bitnet(A16, 1, 20, A16, A16, A16, None) == QMM_ERR_SHAPE
+    assert lib.qmm_pack_ternary(A16, 1, 8, A16, None) == QMM_ERR_SHAPE
+    # alignment
+    assert lib.qmm_gemv_q4_0_q8_0(A2, A16, A16, A16, A16, 1, 1, 32, 1, None, 0, None) == QMM_ERR_ALIGN
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A2, A16, A16, 1, 1, 32, 1, None, 0, None) == QMM_ERR_ALIGN
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, A2, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_ALIGN
+    assert lib.qmm_bitnet_gemv(A2, 1.0, A16, A16, A16, A16, 1, 1, 16, None) == QMM_ERR_ALIGN
+    # workspace
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, A16, 4, 4, 32, None, 0, None) == QMM_ERR_WORKSPACE
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, A16, 4, 4, 32, A16, 16, None) == QMM_ERR_WORKSPACE
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, 2, None, 0, None) == QMM_ERR_WORKSPACE
+    assert lib.qmm_gemm_q4_0_q8_0(A16, A16, A16, A16, A16, 4, 4, 32, _p(0x10010), 1 << 20, None) == QMM_ERR_ALIGN
+    # split_k out of range
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, 3, A16, 1 << 20, None) == QMM_ERR_ARG
+    assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, -1, A16, 1 << 20, None) == QMM_ERR_ARG
+    # debug entry: unknown path
+    assert lib.qmm_debug_block_sums_q4_0_q8_0(5, A16, A16, A16, 1, 1, 32, None, 0, None) == QMM_ERR_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import quantized_matmul_gb300 as q
+    with pytest.raises(ValueError, match="CUDA"):
+        q.quantize_act_q8_0(torch.zeros(1, 32))

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Integer results (quantized codes, fp16 scale bits, per-block sums, ternary
+words, BitNet dots and BitNet outputs) must match bit for bit.  Q4_0 x Q8_0
+f32 outputs must pass the gate of conftest.rel_gate: each output within
+1e-5 * sum_b |sumi * dw * da| of the oracle, and max|diff| / max|y| <= 1e-5.
+Shapes straddle the kernels' tiles (32-block lanes, 16-row CTAs, 128-row and
+16..128-token tensor-core tiles) with ragged tails, plus the degenerate cases
+(one row, one block, all-zero blocks, large outliers)."""
+import numpy as np
+import pytest
+
+from conftest import rel_gate
+from quantized_matmul_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+QK = 32
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def to_np(t):
+    return t.cpu().numpy()
+
+
+def f16_bits(t):
+    """fp16 device tensor -> uint16 bit patterns on the host."""
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def adversarial_x(seed, m, k):
+    w, x = synthetic.q4_0_case(seed, 1, k, m, outlier_p=0.02)
+    x = x.copy()
+    if m > 1:
+        x[1, :QK] = 0.0                      # an all-zero block
+    if m > 2:
+        x[2, 5] = 1e4                        # an outlier
+    if k > QK:
+        x[0, QK:2 * QK] = np.float32(1e-30)  # scale far below fp16 range
+    return x
+
+
+def q4_case(orc, seed, m, n, k):
+    """Oracle-quantized operands (weights and activations) for a parity case."""
+    w, x = synthetic.q4_0_case(seed, n, k, m)
+    wq, wd = orc.quantize_q4_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    return wq, wd, aq, ad
+
+
+# ---------------------------------------------------------------------------
+# quantizers
+
+@pytest.mark.parametrize("m,k", [(1, 32), (3, 64), (17, 4064), (2, 4096), (1, 11008)])
+def test_quantize_act_q8_0_bit_exact(qmm, orc, m, k):
+    x = adversarial_x(10 + m, m, k)
+    aq_ref, ad_ref = orc.quantize_q8_0(x)
+    aq, ad = qmm.quantize_act_q8_0(to_dev(x))
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(f16_bits(ad), ad_ref)
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (7, 96), (129, 4096)])
+def test_quantize_weight_q4_0_bit_exact(qmm, orc, n, k):
+    w, _ = synthetic.q4_0_case(20 + n, n, k, 1)
+    w = w.copy()
+    w[0, :QK] = 0.0                    # zero block: d = -0, all nibbles 8
+    if n > 1:
+        w[1, 3], w[1, 9] = 0.5, -0.5   # tie on |w|: the first index wins
+    wq_ref, wd_ref = orc.quantize_q4_0(w)
+    wq, wd = qmm.quantize_weight_q4_0(to_dev(w))
+    assert np.array_equal(to_np(wq), wq_ref)
+    assert np.array_equal(f16_bits(wd), wd_ref)
+
+
+# ---------------------------------------------------------------------------
+# GEMV
+
+GEMV_SHAPES = [(1, 1, 32), (1, 31, 64), (1, 33, 4064), (1, 129, 4096), (2, 127, 4096),
+               (3, 32, 96), (4, 128, 4096), (7, 65, 1024), (8, 17, 4096), (15, 33, 512),
+               (16, 129, 4096), (1, 4097, 256)]
+
+
+@pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
+def test_gemv_block_sums_bit_exact(qmm, orc, m, n, k):
+    wq, wd, aq, ad = q4_case(orc, 1000 + m * 7 + n, m, n, k)
+    ref = orc.block_sums(wq, aq)
+    got = qmm.debug_block_sums(0, to_dev(wq), to_dev(aq))
+    assert np.array_equal(to_np(got), ref)
+
+
+@pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
+@pytest.mark.parametrize("split", [1, 0, 3])
+def test_gemv_matches_oracle(qmm, orc, m, n, k, split):
+    if split > k // QK:
+        pytest.skip("more slices than blocks")
+    wq, wd, aq, ad = q4_case(orc, 2000 + m * 7 + n, m, n, k)
+    y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
+    absterms = orc.gemm_q4_0_q8_0_absterms(wq, wd, aq, ad)
+    y = qmm.gemv_q4_0_q8_0(to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq),
+                           to_dev(ad.view(np.float16)), split_k=split)
+    ok, worst, maxrel = rel_gate(to_np(y), y_ref, absterms)
+    assert ok, (worst, maxrel)
+
+
+# ---------------------------------------------------------------------------
+# tensor-core GEMM
+
+GEMM_SHAPES = [(1, 1, 32), (1, 128, 64), (16, 129, 96), (17, 127, 4096), (33, 300, 256),
+               (64, 128, 4064), (128, 256, 4096), (129, 130, 512), (200, 520, 1024),
+               (512, 384, 4096)]
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
+def test_gemm_block_sums_bit_exact(qmm, orc, m, n, k):
+    wq, wd, aq, ad = q4_case(orc, 3000 + m + n, m, n, k)
+    ref = orc.block_sums(wq, aq)
+    got = qmm.debug_block_sums(1, to_dev(wq), to_dev(aq))
+    assert np.array_equal(to_np(got), ref)
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
+def test_gemm_matches_oracle(qmm, orc, m, n, k):
+    wq, wd, aq, ad = q4_case(orc, 4000 + m + n, m, n, k)
+    y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
+    absterms = orc.gemm_q4_0_q8_0_absterms(wq, wd, aq, ad)
+    y = to_np(qmm.gemm_q4_0_q8_0(to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq),
+                                 to_dev(ad.view(np.float16))))
+    ok, worst, maxrel = rel_gate(y, y_ref, absterms)
+    assert ok, (worst, maxrel)
+
+
+@pytest.mark.parametrize("m,n,k", [(5, 130, 4096), (129, 257, 1024)])
+def test_gemm_is_bit_identical_to_serial_order(qmm, orc, m, n, k):
+    """Each GEMM output accumulates fma(sumi, dw*da, acc) over blocks in
+    ascending order, the oracle's order, so the f32 bits agree exactly."""
+    wq, wd, aq, ad = q4_case(orc, 5000 + m, m, n, k)
+    y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
+    y = to_np(qmm.gemm_q4_0_q8_0(to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq),
+                                 to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
+def test_gemm_and_gemv_agree_with_adversarial_activations(qmm, orc):
+    m, n, k = 9, 200, 4096
+    w, _ = synthetic.q4_0_case(61, n, k, 1)
+    x = adversarial_x(62, m, k)
+    wq, wd = orc.quantize_q4_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
+    absterms = orc.gemm_q4_0_q8_0_absterms(wq, wd, aq, ad)
+    args = (to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    for y in (qmm.gemv_q4_0_q8_0(*args), qmm.gemm_q4_0_q8_0(*args)):
+        ok, worst, maxrel = rel_gate(to_np(y), y_ref, absterms)
+        assert ok, (worst, maxrel)
+
+
+# ---------------------------------------------------------------------------
+# BitNet ternary
+
+BITNET_SHAPES = [(1, 1, 16), (1, 33, 48), (1, 6912, 2560), (2, 129, 2560), (3, 65, 160),
+                 (5, 100, 4096), (16, 31, 1024), (1, 40, 2576)]
+
+
+@pytest.mark.parametrize("m,n,k", BITNET_SHAPES)
+def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
+    t, x, absmean = synthetic.bitnet_case(70 + m + n, n, k, m)
+    x = x.copy()
+    if m > 1:
+        x[1] = 0.0  # zero row: scale 0, y 0
+    tw_ref = orc.pack_ternary(t)
+    aq_ref, s_ref, asum_ref = orc.quantize_act_bitnet(x)
+    tw = qmm.pack_ternary(to_dev(t))
+    assert np.array_equal(to_np(tw).view(np.uint32), tw_ref)
+    aq, s, asum = qmm.quantize_act_bitnet(to_dev(x))
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(to_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(to_np(asum), asum_ref)
+    dot = qmm.debug_bitnet_dot(tw, aq, asum)
+    assert np.array_equal(to_np(dot), orc.bitnet_dot(tw_ref, aq_ref, asum_ref))
+    y = qmm.bitnet_gemv(tw, absmean, aq, s, asum)
+    y_ref = orc.bitnet_gemv(tw_ref, absmean, aq_ref, s_ref, asum_ref)
+    assert np.array_equal(to_np(y).view(np.uint32), y_ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# bounded waits
+
+def test_gemm_wait_timeout_reports_and_device_stays_usable(qmm, orc):
+    """A wait limit of one poll makes the GEMM's barrier waits give up; the
+    kernel must report QMM_ERR_TIMEOUT through the device error word, release
+    its resources and return, after which a normal call works."""
+    import torch
+    wq, wd, aq, ad = q4_case(orc, 77, 40, 256, 2048)
+    args = (to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    assert qmm.check_device_error() == 0
+    try:
+        qmm.set_wait_limit(1)
+        qmm.gemm_q4_0_q8_0(*args)
+        torch.cuda.synchronize()
+        status = qmm.check_device_error()
+    finally:
+        qmm.set_wait_limit(0)
+    assert status == 7
+    y = to_np(qmm.gemm_q4_0_q8_0(*args))
+    torch.cuda.synchronize()
+    assert qmm.check_device_error() == 0
+    y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
