@@ -195,10 +195,17 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
                                 int32_t *dot, int64_t m, int64_t n, int64_t k, void *stream);
 
 /* Upper bound on the polling iterations of every bounded wait inside the
- * GEMM kernel (default 1 << 26; 0 restores the default).  Tests lower it to
- * make a wait give up on purpose and check that QMM_ERR_TIMEOUT comes back
- * while the device stays usable.  Affects kernels launched after the call. */
+ * GEMM kernel (default 1 << 24; 0 restores the default).  Each poll may
+ * suspend the waiting warp for a short hardware-defined time.  Affects
+ * kernels launched after the call. */
 void qmm_debug_set_wait_limit(uint32_t iterations);
+
+/* Test hook: while enabled, the GEMM kernel's load stage issues no copies,
+ * so its pipeline waits can only run out their poll limit.  Tests use it
+ * with a small limit to check that the kernel then records QMM_ERR_TIMEOUT
+ * (read by qmm_check_device_error), releases its resources and returns, and
+ * that the device stays usable.  Outputs of such a call are unspecified. */
+void qmm_debug_withhold_gemm_loads(int enable);
 
 #ifdef __cplusplus
 }

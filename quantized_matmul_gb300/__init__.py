@@ -69,6 +69,7 @@ def load() -> ctypes.CDLL:
             "qmm_debug_block_sums_q4_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_debug_bitnet_dot": (I, [P, P, P, P, I64, I64, I64, P]),
             "qmm_debug_set_wait_limit": (None, [U32]),
+            "qmm_debug_withhold_gemm_loads": (None, [I]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -296,3 +297,7 @@ def debug_bitnet_dot(tw, aq, act_sum):
 
 def set_wait_limit(iterations: int) -> None:
     load().qmm_debug_set_wait_limit(int(iterations))
+
+
+def withhold_gemm_loads(enable: bool) -> None:
+    load().qmm_debug_withhold_gemm_loads(1 if enable else 0)

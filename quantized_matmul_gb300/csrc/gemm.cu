@@ -15,20 +15,26 @@
 // by CUDA cores while the tensor core already computes the next block.
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M, TMEM lanes) by BN
-// tokens (the MMA's N, TMEM columns).  Roles (384 threads):
+// tokens (the MMA's N, TMEM columns).  Roles (320 threads, 10 warps):
 //   warp 0      TMA producer: per stage of 2 blocks (64 k-elements) it loads
 //               the 128 x 32 B nibble tile, the BN x 64 fp16 activation tile
 //               (128-byte swizzle) and the 2 x BN f32 activation scales.
-//   warp 1      allocates TMEM; one thread issues the MMAs (2 x K=16 per
+//   warp 1      allocates TMEM; its lane 0 issues the MMAs (2 x K=16 per
 //               block into accumulator buffer b % NACC) and commits.
-//   warps 2-3   convert nibbles to fp16 (value - 8) into the 128-byte-swizzled
-//               K-major A tile the MMA reads.
-//   warps 4-11  epilogue: thread (warp % 4, lane) owns weight row n; each of
-//               the two warp groups owns half of the BN columns.  For every
-//               block it loads the accumulator from TMEM and applies
-//               acc = fma(sumi, dw * da, acc), blocks in ascending order -- the
-//               same order and operations as the serial definition, so the
-//               result is reproducible bit for bit.
+//   warps 2-9   (a) convert the nibbles of a stage to fp16 (value - 8) in the
+//               128-byte-swizzled K-major A tile the MMA reads, one block per
+//               lane, two stages ahead of (b); (b) drain: thread
+//               (warp % 4, lane) owns weight row n and half of the BN
+//               columns; for every block it loads the accumulator from TMEM
+//               and applies acc = fma(sumi, dw * da, acc), blocks in
+//               ascending order -- the same order and operations as the
+//               serial definition, so the result is reproducible bit for bit.
+// A TMEM lane quarter can only be read by the warps of the SM sub-partition
+// with the same index (warp % 4), so giving both jobs to these eight warps
+// spreads the conversion work evenly over the four sub-partitions instead
+// of starving the drains of two of them.  The producer and MMA loops run on
+// whole warps (lane 0 issues) so they never sit next to lanes parked at a
+// CTA barrier.
 // An activation prepass (same stream) writes the fp16 copy of the int8
 // activations and the transposed f32 activation scales into the workspace.
 //
@@ -49,12 +55,16 @@ namespace {
 
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 64;                // k-elements per pipeline stage (two blocks)
-constexpr int kStages = 4;
 constexpr int kNacc = 4;               // TMEM accumulator buffers
-constexpr int kThreads = 384;
-constexpr int kConvWarps = 2;
-constexpr int kEpiWarps = 8;
-constexpr int kEpiWarp0 = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;           // convert + drain warps
+constexpr int kEpiWarp0 = 2;
+constexpr int kLookahead = 2;          // stages converted ahead of the drain
+
+// pipeline depth: 5 stages for the wide tiles (one CTA per SM), 4 for the
+// narrow ones so two CTAs fit on an SM
+template <int BN>
+constexpr int stages_for() { return BN >= 64 ? 5 : 4; }
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kDrainLimit = 1u << 22;
 
@@ -223,6 +233,36 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 
 __device__ __forceinline__ float h2f(unsigned short h) { return __half2float(__ushort_as_half(h)); }
 
+// Pairs of f32 in one 64-bit register: the paired FP32 instructions give two
+// independent IEEE round-to-nearest results per instruction.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
     __half2 h;
     memcpy(&h, &u, 4);
@@ -268,6 +308,7 @@ __device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
 
 template <int BN>
 struct Smem {
+    static constexpr int kStages = stages_for<BN>();
     static constexpr int kA = kBM * kBK * 2;        // fp16 weights, 16 KB
     static constexpr int kB = BN * kBK * 2;         // fp16 activations
     static constexpr int kNib = kBM * (kBK / 2);    // nibble bytes, 4 KB
@@ -285,21 +326,22 @@ struct Smem {
 };
 
 template <int BN, bool EMIT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, BN <= 32 ? 2 : 1)
 gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       const __grid_constant__ CUtensorMap tm_act,
                       const __grid_constant__ CUtensorMap tm_da,
                       const unsigned short *__restrict__ wd, float *__restrict__ y,
                       int32_t *__restrict__ sumi, int m, int n, int kb_total,
-                      uint32_t wait_limit) {
+                      uint32_t wait_limit, int withhold_loads) {
     using S = Smem<BN>;
+    constexpr int kStages = S::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *bar_load = bar;                  // TMA landed (tx) + producer arrive
-    uint64_t *bar_conv = bar + kStages;        // A tile converted (conv warps)
-    uint64_t *bar_empty = bar + 2 * kStages;   // MMA done + epilogue read scales
+    uint64_t *bar_conv = bar + kStages;        // A tile converted (8 warps)
+    uint64_t *bar_empty = bar + 2 * kStages;   // MMA done + drains read the scales
     uint64_t *bar_accf = bar + 3 * kStages;    // accumulator buffer full
     uint64_t *bar_acce = bar_accf + kNacc;     // accumulator buffer drained
     uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion
@@ -316,7 +358,7 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
-            mbar_init(&bar_conv[s], kConvWarps);
+            mbar_init(&bar_conv[s], kEpiWarps);
             mbar_init(&bar_empty[s], 1 + kEpiWarps);
         }
         for (int b = 0; b < kNacc; ++b) {
@@ -339,116 +381,130 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         int issued = 0;
-        if (lane == 0) {
-            for (int it = 0; it < num_stages; ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!wait_bounded(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
+        // withhold_loads (test hook): issue nothing, so every consumer wait
+        // can only run out its poll limit
+        for (int it = 0; it < (withhold_loads ? 0 : num_stages); ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            if (!wait_bounded_warp(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&bar_load[s], S::kTx);
                 tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * (kBK / 2), n0);
                 tma_load_2d(smem + S::kOffB + s * S::kB, &tm_act, &bar_load[s], it * kBK, t0);
                 tma_load_2d(smem + S::kOffDa + s * S::kDa, &tm_da, &bar_load[s], t0, 2 * it);
-                issued = it + 1;
             }
-            // Never leave a copy in flight: wait for every stage still pending.
-            for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it) {
-                volatile int no_abort = 0;
-                wait_bounded(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
-                             &no_abort);
-            }
+            __syncwarp();
+            issued = it + 1;
+        }
+        // Never leave a copy in flight: wait for every stage still pending.
+        for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it) {
+            volatile int no_abort = 0;
+            wait_bounded_warp(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
+                              &no_abort);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBM, BN);
-            bool ok = true;
-            int issued_any = 0;
-            for (int it = 0; it < num_stages && ok; ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag)) break;
+        constexpr uint32_t idesc = idesc_f16(kBM, BN);
+        bool ok = true;
+        int issued_any = 0;
+        for (int it = 0; it < num_stages && ok; ++it) {
+            const int s = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            if (!wait_bounded_warp(&bar_conv[s], ph, wait_limit, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + S::kOffA + s * S::kA);
+            const uint32_t b_base = smem_u32(smem + S::kOffB + s * S::kB);
+            for (int h = 0; h < 2; ++h) {
+                const int kbi = 2 * it + h;
+                if (kbi >= kb_total) break;
+                const int buf = kbi % kNacc;
+                const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
+                if (!wait_bounded_warp(&bar_acce[buf], aph ^ 1u, wait_limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(smem + S::kOffA + s * S::kA);
-                const uint32_t b_base = smem_u32(smem + S::kOffB + s * S::kB);
-                for (int h = 0; h < 2; ++h) {
-                    const int kbi = 2 * it + h;
-                    if (kbi >= kb_total) break;
-                    const int buf = kbi % kNacc;
-                    const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
-                    if (!wait_bounded(&bar_acce[buf], aph ^ 1u, wait_limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                if (lane == 0) {
                     const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const uint32_t koff = (uint32_t)(h * 64 + u * 32);  // bytes along k
-                        mma_f16(d_tmem, smem_desc_sw128(a_base + koff), smem_desc_sw128(b_base + koff),
-                                idesc, (uint32_t)u);
+                        mma_f16(d_tmem, smem_desc_sw128(a_base + koff),
+                                smem_desc_sw128(b_base + koff), idesc, (uint32_t)u);
                     }
                     mma_commit(&bar_accf[buf]);
-                    issued_any = 1;
                 }
-                if (ok) mma_commit(&bar_empty[s]);
+                __syncwarp();
+                issued_any = 1;
             }
-            // Wait until every MMA issued by this thread has finished.
-            if (issued_any) {
-                mma_commit(bar_drain);
-                volatile int no_abort = 0;
-                wait_bounded(bar_drain, 0, kDrainLimit, &no_abort);
-            }
+            if (ok && lane == 0) mma_commit(&bar_empty[s]);
+            __syncwarp();
         }
-    } else if (warp < kEpiWarp0) {
-        // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - 64;  // 0..63
-        for (int it = 0; it < num_stages; ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
-            const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
+        // Wait until every MMA issued by lane 0 has finished.
+        if (issued_any) {
+            if (lane == 0) mma_commit(bar_drain);
+            __syncwarp();
+            volatile int no_abort = 0;
+            wait_bounded_warp(bar_drain, 0, kDrainLimit, &no_abort);
+        }
+    } else {
+        // ------------------------------------------------- convert + drain
+        constexpr int kCols = BN / 2;            // columns per thread
+        const int ew = warp - kEpiWarp0;         // 0..7
+        const int q = warp & 3;                  // TMEM lane quarter = sub-partition
+        const int half = ew >> 2;
+        const int row = n0 + 32 * q + lane;      // weight row owned by this thread
+        const int c0 = half * kCols;             // first column (token) in the tile
+        const bool row_ok = row < n;
+        const unsigned short *wrow = wd + (int64_t)(row_ok ? row : 0) * kb_total;
+        const int unit = ew * 32 + lane;         // (row, block) pair converted by this lane
+        const int urow = unit >> 1, ublk = unit & 1;
+
+        // Converts this lane's block of stage j into the A tile.
+        auto convert = [&](int j) -> bool {
+            const int s = j % kStages;
+            const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) return false;
+            const uint4 v = *reinterpret_cast<const uint4 *>(smem + S::kOffNib + s * S::kNib + unit * 16);
+            uint4 out[4];
+            unpack_block_f16(v, out);
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int unit = ct + 64 * j;  // (row, block) pair, contiguous in the nibble tile
-                const int row = unit >> 1, blk = unit & 1;
-                const uint4 v = *reinterpret_cast<const uint4 *>(nib + unit * 16);
-                uint4 out[4];
-                unpack_block_f16(v, out);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = (blk * 4 + c) ^ (row & 7);
-                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + chunk * 16) = out[c];
-                }
+            for (int c = 0; c < 4; ++c) {
+                const int chunk = (ublk * 4 + c) ^ (urow & 7);
+                *reinterpret_cast<uint4 *>(a_tile + urow * 128 + chunk * 16) = out[c];
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_conv[s]);
-        }
-    } else {
-        // ------------------------------------------------------------ epilogue
-        constexpr int kCols = BN / 2;            // columns per thread
-        const int q = warp & 3;                  // TMEM lane quarter
-        const int half = (warp - kEpiWarp0) >> 2;
-        const int row = n0 + 32 * q + lane;      // weight row owned by this thread
-        const int c0 = half * kCols;             // first column (token) in the tile
-        const bool row_ok = row < n;
-        float acc[kCols];
+            return true;
+        };
+
+        uint64_t acc[kCols / 2];                 // f32 pairs
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) acc[c] = 0.0f;
+        for (int c = 0; c < kCols / 2; ++c) acc[c] = 0ull;
         bool ok = true;
+        for (int j = 0; j < kLookahead && j < num_stages && ok; ++j) ok = convert(j);
         for (int it = 0; it < num_stages && ok; ++it) {
             const int s = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
+            // both block scales of this stage, loaded before the conversion
+            // of a later stage hides their latency
+            float dws[2] = {0.0f, 0.0f};
+            if (!EMIT && row_ok) {
+                dws[0] = h2f(__ldg(wrow + 2 * it));
+                if (2 * it + 1 < kb_total) dws[1] = h2f(__ldg(wrow + 2 * it + 1));
+            }
+            if (it + kLookahead < num_stages && !convert(it + kLookahead)) {
+                ok = false;
+                break;
+            }
+            // this warp waited for stage it's copies when it converted it
             const float *da_tile = reinterpret_cast<const float *>(smem + S::kOffDa + s * S::kDa);
             for (int h = 0; h < 2; ++h) {
                 const int kbi = 2 * it + h;
                 if (kbi >= kb_total) break;
                 const int buf = kbi % kNacc;
                 const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
-                const float dw =
-                    (!EMIT && row_ok) ? h2f(__ldg(wd + (int64_t)row * kb_total + kbi)) : 0.0f;
                 if (!wait_bounded_warp(&bar_accf[buf], aph, wait_limit, abort_flag)) {
                     ok = false;
                     break;
@@ -485,11 +541,18 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
                         }
                     }
                 } else {
-                    const float *dar = da_tile + h * BN + c0;
+                    // acc += sumi * (dw * da), two columns per instruction;
+                    // dw * da is exact in f32 (two 11-bit significands)
+                    const uint64_t dw2 = pack_f32x2(dws[h], dws[h]);
+                    const float4 *dap = reinterpret_cast<const float4 *>(da_tile + h * BN + c0);
 #pragma unroll
-                    for (int c = 0; c < kCols; ++c) {
-                        const float sc = __fmul_rn(dw, dar[c]);
-                        acc[c] = fmaf(__uint_as_float(v[c]), sc, acc[c]);
+                    for (int c4 = 0; c4 < kCols / 4; ++c4) {
+                        const float4 d = dap[c4];
+                        const uint64_t s01 = mul_f32x2(dw2, pack_f32x2(d.x, d.y));
+                        const uint64_t s23 = mul_f32x2(dw2, pack_f32x2(d.z, d.w));
+                        acc[2 * c4] = fma_f32x2(pack_u32x2(v[4 * c4], v[4 * c4 + 1]), s01, acc[2 * c4]);
+                        acc[2 * c4 + 1] =
+                            fma_f32x2(pack_u32x2(v[4 * c4 + 2], v[4 * c4 + 3]), s23, acc[2 * c4 + 1]);
                     }
                 }
             }
@@ -498,9 +561,12 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         }
         if (!EMIT && ok && !*abort_flag && row_ok) {
 #pragma unroll
-            for (int c = 0; c < kCols; ++c) {
-                const int t = t0 + c0 + c;
-                if (t < m) y[(int64_t)t * n + row] = acc[c];
+            for (int c = 0; c < kCols / 2; ++c) {
+                float lo, hi;
+                unpack_f32x2(acc[c], lo, hi);
+                const int t = t0 + c0 + 2 * c;
+                if (t < m) y[(int64_t)t * n + row] = lo;
+                if (t + 1 < m) y[(int64_t)(t + 1) * n + row] = hi;
             }
         }
     }
@@ -600,6 +666,7 @@ WsPlan plan_ws(int64_t m, int64_t k) {
 }
 
 uint32_t g_wait_limit = 1u << 24;
+int g_withhold_loads = 0;
 
 template <int BN>
 cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &da,
@@ -613,12 +680,12 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
         auto kern = gemm_q4_0_q8_0_kernel<BN, true>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
         kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
-                                               g_wait_limit);
+                                               g_wait_limit, g_withhold_loads);
     } else {
         auto kern = gemm_q4_0_q8_0_kernel<BN, false>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
         kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
-                                               g_wait_limit);
+                                               g_wait_limit, g_withhold_loads);
     }
     return cudaPeekAtLastError();
 }
@@ -628,6 +695,8 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
 size_t gemm_workspace_bytes(int64_t m, int64_t /*n*/, int64_t k) { return plan_ws(m, k).total; }
 
 void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : (1u << 24); }
+
+void gemm_set_withhold_loads(int enable) { g_withhold_loads = enable ? 1 : 0; }
 
 cudaError_t gemm_read_and_clear_error(unsigned int *word, cudaStream_t s) {
     unsigned int zero = 0;

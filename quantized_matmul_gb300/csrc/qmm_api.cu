@@ -249,4 +249,6 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
 
 void qmm_debug_set_wait_limit(uint32_t iterations) { qmm::gemm_set_wait_limit(iterations); }
 
+void qmm_debug_withhold_gemm_loads(int enable) { qmm::gemm_set_withhold_loads(enable); }
+
 }  // extern "C"

@@ -43,5 +43,6 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
 // synchronized).  Returns the raw word: 0 = no error.
 cudaError_t gemm_read_and_clear_error(unsigned int *word, cudaStream_t s);
 void gemm_set_wait_limit(uint32_t iterations);
+void gemm_set_withhold_loads(int enable);
 
 }  // namespace qmm

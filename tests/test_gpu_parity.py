@@ -192,19 +192,22 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
 # bounded waits
 
 def test_gemm_wait_timeout_reports_and_device_stays_usable(qmm, orc):
-    """A wait limit of one poll makes the GEMM's barrier waits give up; the
-    kernel must report QMM_ERR_TIMEOUT through the device error word, release
-    its resources and return, after which a normal call works."""
+    """With the GEMM's loads withheld no pipeline barrier can complete: every
+    bounded wait must run out, the kernel must record QMM_ERR_TIMEOUT in the
+    device error word, release TMEM and return; afterwards a normal call on
+    the same context gives the exact result."""
     import torch
     wq, wd, aq, ad = q4_case(orc, 77, 40, 256, 2048)
     args = (to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
     assert qmm.check_device_error() == 0
     try:
-        qmm.set_wait_limit(1)
+        qmm.set_wait_limit(2000)
+        qmm.withhold_gemm_loads(True)
         qmm.gemm_q4_0_q8_0(*args)
         torch.cuda.synchronize()
         status = qmm.check_device_error()
     finally:
+        qmm.withhold_gemm_loads(False)
         qmm.set_wait_limit(0)
     assert status == 7
     y = to_np(qmm.gemm_q4_0_q8_0(*args))
