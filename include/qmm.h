@@ -110,6 +110,31 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
                               int64_t m, int64_t n, int64_t k, int split_k,
                               void *workspace, size_t workspace_bytes, void *stream);
 
+/* The GEMV above for callers that cannot allocate device memory where they
+ * run it -- for instance a latency-critical decode loop that must not enter
+ * the CUDA allocator (its locks and possible implicit synchronization), or a
+ * component that only receives device pointers and owns no allocator.  The
+ * pages this library follows have no counterpart: this is a deployment
+ * convenience.  Same arguments, result and rules as qmm_gemv_q4_0_q8_0
+ * except that there is no workspace: the split-K partials go to a device
+ * array owned by the library, QMM_NOALLOC_SCRATCH_FLOATS floats (4 MiB)
+ * reserved on every GPU that loads the library and held until the process
+ * exits.  The call itself allocates nothing.
+ *   - An explicit split_k > 1 with split_k * m * n > QMM_NOALLOC_SCRATCH_FLOATS
+ *     returns QMM_ERR_WORKSPACE and launches nothing; split_k = 0 picks the
+ *     automatic split, lowered until the partials fit.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array (it keeps the last call's
+ *     partials; each call overwrites all it reads, so nothing needs
+ *     clearing): calls whose executions overlap on the GPU, e.g. on two
+ *     streams, race and give wrong results.  Order them on one stream. */
+#define QMM_NOALLOC_SCRATCH_FLOATS (1 << 20)
+qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
+                                      const int8_t *aq, const uint16_t *ad, float *y,
+                                      int64_t m, int64_t n, int64_t k, int split_k,
+                                      void *stream);
+
 /* Q4_0 x Q8_0 matrix product for prefill (m >= 1, any n, k % 32 == 0), same
  * result definition as the GEMV.  The block sums run on the tensor cores
  * (tcgen05.mma kind::f16 with f32 accumulators in TMEM): the int4 and int8

@@ -58,6 +58,7 @@ def load() -> ctypes.CDLL:
             "qmm_quantize_weight_q4_0": (I, [P, I64, I64, P, P, P]),
             "qmm_gemv_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
             "qmm_gemm_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
+            "qmm_gemv_q4_0_q8_0_noalloc": (I, [P, P, P, P, P, I64, I64, I64, I, P]),
             "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
             "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
             "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
@@ -188,6 +189,21 @@ def gemv_q4_0_q8_0(wq, wd, aq, ad, y=None, split_k: int = 0, workspace=None):
                                    _dev(y, torch.float32, "y", (m, n)), m, n, k, split_k,
                                    ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
     _check(st, "qmm_gemv_q4_0_q8_0")
+    return y
+
+
+def gemv_q4_0_q8_0_noalloc(wq, wd, aq, ad, y=None, split_k: int = 0):
+    """The decode GEMV for callers that cannot allocate device memory where
+    they run it: the split-K partials use a 4 MiB array the library reserves
+    on each GPU, so no workspace is passed.  Calls that overlap on the GPU
+    share that array and race; order them on one stream."""
+    torch = _torch()
+    m, n, k = _q4_shapes(wq, wd, aq, ad)
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    st = load().qmm_gemv_q4_0_q8_0_noalloc(wq.data_ptr(), wd.data_ptr(), aq.data_ptr(),
+                                           ad.data_ptr(), _dev(y, torch.float32, "y", (m, n)),
+                                           m, n, k, split_k, _stream())
+    _check(st, "qmm_gemv_q4_0_q8_0_noalloc")
     return y
 
 

@@ -24,6 +24,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "qmm_internal.h"
 
@@ -380,6 +381,48 @@ cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *a
     if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+}
+
+// ---------------------------------------------------------------------------
+// Split-K GEMV without caller-provided memory.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// product: code running where cudaMalloc is off limits (a real-time or
+// latency-critical loop that must not take the allocator's locks or risk
+// an implicit synchronization, or a host process that was handed device
+// pointers by another component and owns no allocator at all).  For them the
+// split-K partials live in this library-owned array, reserved once per GPU
+// when the library is loaded on it and held until the process exits.
+
+static __device__ __align__(256) float g_gemv_scratch[kGemvNoAllocScratchFloats];
+
+namespace {
+std::mutex g_scratch_mu;
+float *g_scratch_ptr[64] = {};  // device address of g_gemv_scratch, per device
+}  // namespace
+
+cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                          const uint16_t *ad, float *y, int64_t m, int64_t n,
+                                          int64_t k, int split, cudaStream_t s) {
+    float *scratch = nullptr;
+    if (split > 1) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_ptr[dev]) {
+            // host code only knows a stand-in for the array: ask the runtime
+            // for its address on the current device (first call per device)
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_gemv_scratch);
+            if (e != cudaSuccess) return e;
+            g_scratch_ptr[dev] = static_cast<float *>(p);
+        }
+        scratch = g_scratch_ptr[dev];
+    }
+    // every slice writes all of its m * n partials, so nothing needs clearing
+    return launch_gemv_q4_0_q8_0(wq, wd, aq, ad, y, nullptr, m, n, k, split, scratch, s);
 }
 
 }  // namespace qmm

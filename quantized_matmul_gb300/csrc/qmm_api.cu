@@ -16,6 +16,8 @@
 namespace {
 
 using qmm::kQK;
+static_assert(qmm::kGemvNoAllocScratchFloats == QMM_NOALLOC_SCRATCH_FLOATS,
+              "the header and the library must agree on the built-in scratch size");
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ok[kMaxDevices];  // 0 unknown, 1 supported, 2 not supported
@@ -110,6 +112,24 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_
     return launch_status(qmm::launch_gemv_q4_0_q8_0(wq, wd, aq, ad, y, nullptr, m, n, k, split,
                                                     static_cast<float *>(workspace),
                                                     as_stream(stream)));
+}
+
+qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                      const uint16_t *ad, float *y, int64_t m, int64_t n,
+                                      int64_t k, int split_k, void *stream) {
+    if (qmm_status st = check_q4_common(wq, wd, aq, ad, y, m, n, k)) return st;
+    if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    int split = 1;
+    if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
+    const int64_t cap = qmm::kGemvNoAllocScratchFloats;
+    if (split > 1 && (int64_t)split * m * n > cap) {
+        if (split_k != 0) return QMM_ERR_WORKSPACE;  // the built-in scratch is too small
+        split = (int)(cap / (m * n));                // automatic choice: largest that fits
+        if (split < 2) split = 1;
+    }
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemv_q4_0_q8_0_noalloc(wq, wd, aq, ad, y, m, n, k, split,
+                                                            as_stream(stream)));
 }
 
 qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,

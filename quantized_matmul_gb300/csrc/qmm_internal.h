@@ -29,6 +29,12 @@ cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, int split, float *partials,
                                   cudaStream_t s);
+// Split-K GEMV whose partials live in a library-owned device array of
+// kGemvNoAllocScratchFloats floats (split * m * n must fit).
+constexpr int64_t kGemvNoAllocScratchFloats = int64_t(1) << 20;
+cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                          const uint16_t *ad, float *y, int64_t m, int64_t n,
+                                          int64_t k, int split, cudaStream_t s);
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s);
