@@ -220,9 +220,10 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
                                 int32_t *dot, int64_t m, int64_t n, int64_t k, void *stream);
 
 /* Upper bound on the polling iterations of every bounded wait inside the
- * GEMM kernel (default 1 << 24; 0 restores the default).  Each poll may
- * suspend the waiting warp for a short hardware-defined time.  Affects
- * kernels launched after the call. */
+ * GEMM kernel (default 1 << 17; 0 restores the default).  Each poll
+ * suspends the waiting warp for at most 20 microseconds (it resumes as soon
+ * as the awaited phase completes).  Affects kernels launched after the
+ * call. */
 void qmm_debug_set_wait_limit(uint32_t iterations);
 
 /* Test hook: while enabled, the GEMM kernel's load stage issues no copies,

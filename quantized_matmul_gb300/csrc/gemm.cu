@@ -15,26 +15,28 @@
 // by CUDA cores while the tensor core already computes the next block.
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M, TMEM lanes) by BN
-// tokens (the MMA's N, TMEM columns).  Roles (320 threads, 10 warps):
+// tokens (the MMA's N, TMEM columns).  Roles (704 threads, 22 warps):
 //   warp 0      TMA producer: per stage of 2 blocks (64 k-elements) it loads
 //               the 128 x 32 B nibble tile, the BN x 64 fp16 activation tile
 //               (128-byte swizzle) and the 2 x BN f32 activation scales.
 //   warp 1      allocates TMEM; its lane 0 issues the MMAs (2 x K=16 per
 //               block into accumulator buffer b % NACC) and commits.
-//   warps 2-9   (a) convert the nibbles of a stage to fp16 (value - 8) in the
-//               128-byte-swizzled K-major A tile the MMA reads, one block per
-//               lane, two stages ahead of (b); (b) drain: thread
-//               (warp % 4, lane) owns weight row n and half of the BN
-//               columns; for every block it loads the accumulator from TMEM
-//               and applies acc = fma(sumi, dw * da, acc), blocks in
-//               ascending order -- the same order and operations as the
-//               serial definition, so the result is reproducible bit for bit.
-// A TMEM lane quarter can only be read by the warps of the SM sub-partition
-// with the same index (warp % 4), so giving both jobs to these eight warps
-// spreads the conversion work evenly over the four sub-partitions instead
-// of starving the drains of two of them.  The producer and MMA loops run on
-// whole warps (lane 0 issues) so they never sit next to lanes parked at a
-// CTA barrier.
+//   warps 2-5   convert the nibbles of a stage to fp16 (value - 8) in the
+//               128-byte-swizzled K-major A tile the MMA reads, as far ahead
+//               of the MMA as the shared-memory stages allow (one converter
+//               warp per SM sub-partition, so the work is spread evenly).
+//   warps 6-21  drain: thread (warp % 4, lane) owns weight row n and a
+//               quarter of the BN columns; for every block it loads the
+//               accumulator from TMEM and applies acc = fma(sumi, dw * da,
+//               acc), blocks in ascending order -- the same order and
+//               operations as the serial definition, so the result is
+//               reproducible bit for bit.  (A TMEM lane quarter is readable
+//               only from the sub-partition with the same index, warp % 4.)
+// The roles meet only at mbarriers: converters run ahead of the MMA by up to
+// the number of stages, the MMA runs ahead of the drains by up to the number
+// of TMEM accumulator slots, so no role waits on another role's latency
+// chain.  The producer and MMA loops run on whole warps with lane 0
+// issuing.
 // An activation prepass (same stream) writes the fp16 copy of the int8
 // activations and the transposed f32 activation scales into the workspace.
 //
@@ -55,18 +57,39 @@ namespace {
 
 constexpr int kBM = 128;               // weight rows per tile (MMA M)
 constexpr int kBK = 64;                // k-elements per pipeline stage (two blocks)
-constexpr int kNacc = 4;               // TMEM accumulator buffers
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;           // convert + drain warps
-constexpr int kEpiWarp0 = 2;
-constexpr int kLookahead = 2;          // stages converted ahead of the drain
-
-// pipeline depth: 5 stages for the wide tiles (one CTA per SM), 4 for the
-// narrow ones so two CTAs fit on an SM
+constexpr int kConvWarps = 4;          // warps 2-5: one converter per sub-partition
+constexpr int kConvWarp0 = 2;
+constexpr int kEpiWarp0 = 6;           // warps 6-21 may drain
+// drain warps per TMEM lane quarter: enough for 32 columns each at most
 template <int BN>
-constexpr int stages_for() { return BN >= 64 ? 5 : 4; }
+__host__ __device__ constexpr int drain_groups() { return BN <= 32 ? 1 : 2; }
+// producer, MMA and four converter warps, then the drain warps
+template <int BN>
+__host__ __device__ constexpr int threads_for() { return 32 * (kEpiWarp0 + 4 * drain_groups<BN>()); }
+constexpr int kSmemBudget = 200 * 1024;  // per SM
+
+// bytes of one pipeline stage and the number of stages that fit the budget
+template <int BN>
+constexpr int stage_bytes() { return kBM * kBK * 2 + BN * kBK * 2 + kBM * (kBK / 2) + 2 * BN * 4; }
+template <int BN>
+constexpr int ctas_per_sm() { return BN <= 32 ? 2 : 1; }
+template <int BN>
+constexpr int stages_for() {
+    return (kSmemBudget / ctas_per_sm<BN>()) / stage_bytes<BN>() < 9
+               ? (kSmemBudget / ctas_per_sm<BN>()) / stage_bytes<BN>() : 9;
+}
+// TMEM accumulator slots, one per stage in flight (each holds the stage's two
+// block accumulators, 2 * BN columns): as many as 512 columns hold, at most 8
+template <int BN>
+constexpr int nacc_for() { return 256 / BN < 8 ? 256 / BN : 8; }
 constexpr uint32_t kErrTimeout = 1u;
-constexpr uint32_t kDrainLimit = 1u << 22;
+// A waiting warp asks to be suspended for up to this long per poll; it
+// resumes as soon as the phase completes, so a wait does not spin and take
+// issue slots from the warps sharing its SM sub-partition.
+constexpr uint32_t kSuspendHintNs = 20000;
+// Default poll limit: 2^17 polls of at most kSuspendHintNs each (~2.6 s).
+constexpr uint32_t kDefaultWaitLimit = 1u << 17;
+constexpr uint32_t kDrainLimit = 1u << 17;
 
 __device__ unsigned int g_gemm_error = 0;
 
@@ -96,11 +119,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     asm volatile(
         "{\n"
         ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         "selp.u32 %0, 1, 0, p;\n"
         "}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -201,6 +224,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -309,6 +352,8 @@ __device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
 template <int BN>
 struct Smem {
     static constexpr int kStages = stages_for<BN>();
+    static constexpr int kNacc = nacc_for<BN>();
+    static constexpr int kEpiWarps = 4 * drain_groups<BN>();
     static constexpr int kA = kBM * kBK * 2;        // fp16 weights, 16 KB
     static constexpr int kB = BN * kBK * 2;         // fp16 activations
     static constexpr int kNib = kBM * (kBK / 2);    // nibble bytes, 4 KB
@@ -326,7 +371,7 @@ struct Smem {
 };
 
 template <int BN, bool EMIT>
-__global__ void __launch_bounds__(kThreads, BN <= 32 ? 2 : 1)
+__global__ void __launch_bounds__(threads_for<BN>(), ctas_per_sm<BN>())
 gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       const __grid_constant__ CUtensorMap tm_act,
                       const __grid_constant__ CUtensorMap tm_da,
@@ -335,15 +380,17 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       uint32_t wait_limit, int withhold_loads) {
     using S = Smem<BN>;
     constexpr int kStages = S::kStages;
+    constexpr int kNacc = S::kNacc;
+    constexpr int kEpiWarps = S::kEpiWarps;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *bar_load = bar;                  // TMA landed (tx) + producer arrive
-    uint64_t *bar_conv = bar + kStages;        // A tile converted (8 warps)
-    uint64_t *bar_empty = bar + 2 * kStages;   // MMA done + drains read the scales
-    uint64_t *bar_accf = bar + 3 * kStages;    // accumulator buffer full
-    uint64_t *bar_acce = bar_accf + kNacc;     // accumulator buffer drained
+    uint64_t *bar_conv = bar + kStages;        // A tile converted (4 warps)
+    uint64_t *bar_empty = bar + 2 * kStages;   // drains done with the stage (implies its MMAs are)
+    uint64_t *bar_accf = bar + 3 * kStages;    // accumulator slot full (both blocks of a stage)
+    uint64_t *bar_acce = bar_accf + kNacc;     // accumulator slot drained
     uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
@@ -353,13 +400,13 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     const int t0 = blockIdx.x * BN;   // first token of the tile
     const int n0 = blockIdx.y * kBM;  // first weight row of the tile
     const int num_stages = (kb_total + 1) / 2;
-    constexpr uint32_t kTmemCols = (uint32_t)(kNacc * BN) < 32 ? 32 : (uint32_t)(kNacc * BN);
+    constexpr uint32_t kTmemCols = (uint32_t)(2 * kNacc * BN) < 32 ? 32 : (uint32_t)(2 * kNacc * BN);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
-            mbar_init(&bar_conv[s], kEpiWarps);
-            mbar_init(&bar_empty[s], 1 + kEpiWarps);
+            mbar_init(&bar_conv[s], kConvWarps);
+            mbar_init(&bar_empty[s], kEpiWarps);
         }
         for (int b = 0; b < kNacc; ++b) {
             mbar_init(&bar_accf[b], 1);
@@ -404,160 +451,180 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16(kBM, BN);
-        bool ok = true;
-        int issued_any = 0;
-        for (int it = 0; it < num_stages && ok; ++it) {
-            const int s = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            if (!wait_bounded_warp(&bar_conv[s], ph, wait_limit, abort_flag)) break;
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + S::kOffA + s * S::kA);
-            const uint32_t b_base = smem_u32(smem + S::kOffB + s * S::kB);
-            for (int h = 0; h < 2; ++h) {
-                const int kbi = 2 * it + h;
-                if (kbi >= kb_total) break;
-                const int buf = kbi % kNacc;
-                const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
-                if (!wait_bounded_warp(&bar_acce[buf], aph ^ 1u, wait_limit, abort_flag)) {
-                    ok = false;
+        // The serial critical path at narrow tiles: lane 0 alone waits and
+        // issues, with the descriptors of stage s one constant step apart, one
+        // commit per stage (the drains free the stage's buffers only after
+        // that commit fired, so it also covers the shared-memory tiles).
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kBM, BN);
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffA));
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffB));
+            int issued_any = 0;
+            for (int it = 0; it < num_stages; ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                const int slot = it % kNacc;
+                const uint32_t sph = (uint32_t)(it / kNacc) & 1u;
+                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag) ||
+                    !wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag))
                     break;
-                }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t koff = (uint32_t)(h * 64 + u * 32);  // bytes along k
-                        mma_f16(d_tmem, smem_desc_sw128(a_base + koff),
-                                smem_desc_sw128(b_base + koff), idesc, (uint32_t)u);
-                    }
-                    mma_commit(&bar_accf[buf]);
+                // descriptor start address advances 32 bytes (2 in units of
+                // 16 bytes) per K=16 step inside the 128-byte swizzle row
+                const uint64_t a_desc = a_desc0 + (uint64_t)(s * (S::kA >> 4));
+                const uint64_t b_desc = b_desc0 + (uint64_t)(s * (S::kB >> 4));
+                const uint32_t d0 = tmem_base + (uint32_t)(slot * 2 * BN);
+                mma_f16(d0, a_desc + 0, b_desc + 0, idesc, 0u);
+                mma_f16(d0, a_desc + 2, b_desc + 2, idesc, 1u);
+                if (2 * it + 1 < kb_total) {
+                    mma_f16(d0 + BN, a_desc + 4, b_desc + 4, idesc, 0u);
+                    mma_f16(d0 + BN, a_desc + 6, b_desc + 6, idesc, 1u);
                 }
-                __syncwarp();
+                mma_commit(&bar_accf[slot]);
                 issued_any = 1;
             }
-            if (ok && lane == 0) mma_commit(&bar_empty[s]);
-            __syncwarp();
+            // Wait until every MMA issued here has finished.
+            if (issued_any) {
+                mma_commit(bar_drain);
+                volatile int no_abort = 0;
+                wait_bounded(bar_drain, 0, kDrainLimit, &no_abort);
+            }
         }
-        // Wait until every MMA issued by lane 0 has finished.
-        if (issued_any) {
-            if (lane == 0) mma_commit(bar_drain);
-            __syncwarp();
-            volatile int no_abort = 0;
-            wait_bounded_warp(bar_drain, 0, kDrainLimit, &no_abort);
-        }
-    } else {
-        // ------------------------------------------------- convert + drain
-        constexpr int kCols = BN / 2;            // columns per thread
-        const int ew = warp - kEpiWarp0;         // 0..7
-        const int q = warp & 3;                  // TMEM lane quarter = sub-partition
-        const int half = ew >> 2;
-        const int row = n0 + 32 * q + lane;      // weight row owned by this thread
-        const int c0 = half * kCols;             // first column (token) in the tile
-        const bool row_ok = row < n;
-        const unsigned short *wrow = wd + (int64_t)(row_ok ? row : 0) * kb_total;
-        const int unit = ew * 32 + lane;         // (row, block) pair converted by this lane
-        const int urow = unit >> 1, ublk = unit & 1;
-
-        // Converts this lane's block of stage j into the A tile.
-        auto convert = [&](int j) -> bool {
+        __syncwarp();
+    } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
+        // ------------------------------------------------------------ converters
+        // 128 rows x 2 blocks per stage; converter cw takes blocks
+        // cw * 64 + lane and cw * 64 + 32 + lane (contiguous 16-byte reads;
+        // the swizzled 16-byte stores of 8 consecutive lanes hit 8 different
+        // bank groups)
+        const int cw = warp - kConvWarp0;
+        for (int j = 0; j < num_stages; ++j) {
             const int s = j % kStages;
             const uint32_t ph = (uint32_t)(j / kStages) & 1u;
-            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) return false;
-            const uint4 v = *reinterpret_cast<const uint4 *>(smem + S::kOffNib + s * S::kNib + unit * 16);
-            uint4 out[4];
-            unpack_block_f16(v, out);
+            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
+            const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
+            uint4 v[2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int chunk = (ublk * 4 + c) ^ (urow & 7);
-                *reinterpret_cast<uint4 *>(a_tile + urow * 128 + chunk * 16) = out[c];
+            for (int i = 0; i < 2; ++i)
+                v[i] = *reinterpret_cast<const uint4 *>(nib + (cw * 64 + 32 * i + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int unit = cw * 64 + 32 * i + lane;
+                const int row = unit >> 1, blk = unit & 1;
+                uint4 out[4];
+                unpack_block_f16(v[i], out);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((blk * 4 + c) ^ (row & 7)) * 16)) =
+                        out[c];
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_conv[s]);
-            return true;
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+        // ------------------------------------------------------------ drains
+        constexpr int kCols = BN / drain_groups<BN>();  // columns per thread (16 or 32)
+        const int ew = warp - kEpiWarp0;         // 0..15
+        const int q = warp & 3;                  // TMEM lane quarter = sub-partition
+        const int grp = ew >> 2;                 // column group 0..3
+        const int row = n0 + 32 * q + lane;      // weight row owned by this thread
+        const int c0 = grp * kCols;              // first column (token) in the tile
+        const bool row_ok = row < n;
+        const unsigned short *wrow = wd + (int64_t)(row_ok ? row : 0) * kb_total;
+        // The raw fp16 weight scales of a stage are loaded one stage ahead and
+        // converted only where they are used: a warp issues in order, so a
+        // conversion right after the load would stall it for the whole
+        // global-load latency every stage.
+        auto load_scales = [&](int j, unsigned short (&raw)[2]) {
+            raw[0] = raw[1] = 0;
+            if (!EMIT && row_ok && j < num_stages) {
+                raw[0] = __ldg(wrow + 2 * j);
+                if (2 * j + 1 < kb_total) raw[1] = __ldg(wrow + 2 * j + 1);
+            }
         };
-
-        uint64_t acc[kCols / 2];                 // f32 pairs
+        uint64_t acc[kCols / 2 > 0 ? kCols / 2 : 1];  // f32 pairs
 #pragma unroll
         for (int c = 0; c < kCols / 2; ++c) acc[c] = 0ull;
+        unsigned short dw_next[2];
+        load_scales(0, dw_next);
         bool ok = true;
-        for (int j = 0; j < kLookahead && j < num_stages && ok; ++j) ok = convert(j);
         for (int it = 0; it < num_stages && ok; ++it) {
             const int s = it % kStages;
-            // both block scales of this stage, loaded before the conversion
-            // of a later stage hides their latency
-            float dws[2] = {0.0f, 0.0f};
-            if (!EMIT && row_ok) {
-                dws[0] = h2f(__ldg(wrow + 2 * it));
-                if (2 * it + 1 < kb_total) dws[1] = h2f(__ldg(wrow + 2 * it + 1));
-            }
-            if (it + kLookahead < num_stages && !convert(it + kLookahead)) {
+            const unsigned short dw_cur[2] = {dw_next[0], dw_next[1]};
+            load_scales(it + 1, dw_next);
+            const int slot = it % kNacc;
+            // the accumulators of a stage are committed after its copies
+            // landed, so this wait also covers the activation-scale tile
+            if (!wait_bounded_warp(&bar_accf[slot], (uint32_t)(it / kNacc) & 1u, wait_limit,
+                                   abort_flag)) {
                 ok = false;
                 break;
             }
-            // this warp waited for stage it's copies when it converted it
+            tc_fence_after();
             const float *da_tile = reinterpret_cast<const float *>(smem + S::kOffDa + s * S::kDa);
+            // BN == 16: both blocks' 16 columns are adjacent in the slot, so one
+            // 32-column TMEM load fetches the whole stage; otherwise each block
+            // is loaded (32 columns) right before it is consumed.
+            uint32_t both[BN == 16 ? 32 : 1];
+            if constexpr (BN == 16) {
+                tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * 2 * BN), both);
+                tmem_wait_ld();
+            }
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int kbi = 2 * it + h;
                 if (kbi >= kb_total) break;
-                const int buf = kbi % kNacc;
-                const uint32_t aph = (uint32_t)(kbi / kNacc) & 1u;
-                if (!wait_bounded_warp(&bar_accf[buf], aph, wait_limit, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + c0);
-                uint32_t v[kCols];
-                if constexpr (kCols >= 16) {
+                // consume the block in chunks of at most 32 columns: one TMEM
+                // load, then its multiply-adds (keeps the live registers low)
+                constexpr int kChunk = BN == 16 ? 16 : 32;
 #pragma unroll
-                    for (int g = 0; g < kCols / 16; ++g) {
-                        uint32_t r[16];
-                        tmem_ld16(taddr + 16 * g, r);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) v[16 * g + i] = r[i];
+                for (int g = 0; g < kCols / kChunk; ++g) {
+                    uint32_t vblk[BN == 16 ? 1 : 32];
+                    if constexpr (BN != 16) {
+                        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) +
+                                      (uint32_t)(slot * 2 * BN + h * BN + c0 + 32 * g),
+                                  vblk);
+                        tmem_wait_ld();
                     }
-                } else {
-                    uint32_t r[8];
-                    tmem_ld8(taddr, r);
+                    const uint32_t *v = BN == 16 ? both + 16 * h : vblk;
+                    const int cg = c0 + kChunk * g;  // first column of the chunk
+                    if constexpr (EMIT) {
+                        if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = r[i];
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_acce[buf]);
-                if constexpr (EMIT) {
-                    if (row_ok) {
-#pragma unroll
-                        for (int c = 0; c < kCols; ++c) {
-                            const int t = t0 + c0 + c;
-                            if (t < m)
-                                sumi[((int64_t)t * n + row) * kb_total + kbi] =
-                                    __float2int_rn(__uint_as_float(v[c]));
+                            for (int c = 0; c < kChunk; ++c) {
+                                const int t = t0 + cg + c;
+                                if (t < m)
+                                    sumi[((int64_t)t * n + row) * kb_total + kbi] =
+                                        __float2int_rn(__uint_as_float(v[c]));
+                            }
                         }
-                    }
-                } else {
-                    // acc += sumi * (dw * da), two columns per instruction;
-                    // dw * da is exact in f32 (two 11-bit significands)
-                    const uint64_t dw2 = pack_f32x2(dws[h], dws[h]);
-                    const float4 *dap = reinterpret_cast<const float4 *>(da_tile + h * BN + c0);
+                    } else {
+                        // acc += sumi * (dw * da), two columns per instruction;
+                        // dw * da is exact in f32 (two 11-bit significands)
+                        const float dw = h2f(dw_cur[h]);
+                        const uint64_t dw2 = pack_f32x2(dw, dw);
+                        const float4 *dap = reinterpret_cast<const float4 *>(da_tile + h * BN + cg);
+                        uint64_t *accg = acc + (kChunk / 2) * g;
 #pragma unroll
-                    for (int c4 = 0; c4 < kCols / 4; ++c4) {
-                        const float4 d = dap[c4];
-                        const uint64_t s01 = mul_f32x2(dw2, pack_f32x2(d.x, d.y));
-                        const uint64_t s23 = mul_f32x2(dw2, pack_f32x2(d.z, d.w));
-                        acc[2 * c4] = fma_f32x2(pack_u32x2(v[4 * c4], v[4 * c4 + 1]), s01, acc[2 * c4]);
-                        acc[2 * c4 + 1] =
-                            fma_f32x2(pack_u32x2(v[4 * c4 + 2], v[4 * c4 + 3]), s23, acc[2 * c4 + 1]);
+                        for (int c4 = 0; c4 < kChunk / 4; ++c4) {
+                            const float4 d = dap[c4];
+                            const uint64_t s01 = mul_f32x2(dw2, pack_f32x2(d.x, d.y));
+                            const uint64_t s23 = mul_f32x2(dw2, pack_f32x2(d.z, d.w));
+                            accg[2 * c4] = fma_f32x2(pack_u32x2(v[4 * c4], v[4 * c4 + 1]), s01, accg[2 * c4]);
+                            accg[2 * c4 + 1] =
+                                fma_f32x2(pack_u32x2(v[4 * c4 + 2], v[4 * c4 + 3]), s23, accg[2 * c4 + 1]);
+                        }
                     }
                 }
             }
+            tc_fence_before();
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(&bar_empty[s]);
+            if (lane == 0) {
+                mbar_arrive(&bar_acce[slot]);
+                mbar_arrive(&bar_empty[s]);
+            }
         }
         if (!EMIT && ok && !*abort_flag && row_ok) {
 #pragma unroll
@@ -665,7 +732,7 @@ WsPlan plan_ws(int64_t m, int64_t k) {
     return p;
 }
 
-uint32_t g_wait_limit = 1u << 24;
+uint32_t g_wait_limit = kDefaultWaitLimit;
 int g_withhold_loads = 0;
 
 template <int BN>
@@ -679,12 +746,12 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
     if (sumi) {
         auto kern = gemm_q4_0_q8_0_kernel<BN, true>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
+        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
                                                g_wait_limit, g_withhold_loads);
     } else {
         auto kern = gemm_q4_0_q8_0_kernel<BN, false>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, kThreads, S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
+        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
                                                g_wait_limit, g_withhold_loads);
     }
     return cudaPeekAtLastError();
@@ -694,7 +761,7 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
 
 size_t gemm_workspace_bytes(int64_t m, int64_t /*n*/, int64_t k) { return plan_ws(m, k).total; }
 
-void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : (1u << 24); }
+void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : kDefaultWaitLimit; }
 
 void gemm_set_withhold_loads(int enable) { g_withhold_loads = enable ? 1 : 0; }
 
