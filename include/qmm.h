@@ -135,6 +135,55 @@ qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
                                       int64_t m, int64_t n, int64_t k, int split_k,
                                       void *stream);
 
+/* Decode linear layer y = x W^T with Q8_0 activations (1 <= m <=
+ * QMM_GEMV_MAX_M): qmm_quantize_act_q8_0 of x into aq/ad, then
+ * qmm_gemv_q4_0_q8_0 with split_k = 1, enqueued as one call; y, aq and ad
+ * are bit for bit those of the two calls.
+ *   x f32 [m, ldx] (first k columns), 4-byte aligned; aq int8 [m, k] 16-byte
+ *   aligned; ad fp16 bits [m, k/32] 2-byte aligned; wq, wd, y as for
+ *   qmm_gemv_q4_0_q8_0.
+ *   flags: 0, or QMM_LINEAR_PDL: launch both kernels with programmatic
+ *   dependent launch.  Each may then start while its predecessor on the
+ *   stream is still running: the quantizer reads x, and the GEMV reads aq/ad
+ *   and writes y, only after the predecessor completed, while the GEMV loads
+ *   its first weight blocks (wq, wd) before that.  So layer i+1's first
+ *   weight traffic overlaps layer i's tail and the launch gaps close.  Only
+ *   valid when wq and wd are not written by work still running on the
+ *   stream when the call is enqueued (true for model weights).  A chain of
+ *   such calls on one stream stays ordered: every kernel reads its inputs
+ *   after the kernel before it completed, which completed after the one
+ *   before that, and so on. */
+#define QMM_LINEAR_PDL 1
+qmm_status qmm_linear_q4_0(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
+                           int8_t *aq, uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                           int flags, void *stream);
+
+/* One problem of qmm_linear_q4_0_grouped: the arguments of qmm_linear_q4_0
+ * for one weight matrix (same meaning, layout and alignment rules). */
+typedef struct qmm_linear_problem {
+    const uint8_t *wq;   /* Q4_0 nibbles [n, k/2] */
+    const uint16_t *wd;  /* Q4_0 scales, fp16 bits [n, k/32] */
+    const float *x;      /* activations f32 [m, ldx] */
+    int64_t ldx;
+    int8_t *aq;          /* receives the Q8_0 codes [m, k] */
+    uint16_t *ad;        /* receives the Q8_0 scales, fp16 bits [m, k/32] */
+    float *y;            /* receives y f32 [m, n] */
+    int64_t n;
+    int64_t k;
+} qmm_linear_problem;
+
+/* Up to QMM_GROUP_MAX independent decode linear layers with the same m in
+ * two launches in all: one quantizer launch over every problem's x, then
+ * one GEMV launch whose CTAs cover every problem's rows (the way a model's
+ * Q/K/V or gate/up projections, or the experts of a mixture, are batched).
+ * Each problem's y, aq and ad are bit for bit those of qmm_linear_q4_0 on
+ * it alone.  `problems` is a host array read during the call.  The problems
+ * must be independent: no problem's aq, ad or y may overlap any buffer of
+ * another problem.  flags as for qmm_linear_q4_0. */
+#define QMM_GROUP_MAX 16
+qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count, int64_t m,
+                                   int flags, void *stream);
+
 /* Q4_0 x Q8_0 matrix product for prefill (m >= 1, any n, k % 32 == 0), same
  * result definition as the GEMV.  The block sums run on the tensor cores
  * (tcgen05.mma kind::f16 with f32 accumulators in TMEM): the int4 and int8

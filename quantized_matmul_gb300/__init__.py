@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
             "qmm_gemv_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
             "qmm_gemm_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_gemv_q4_0_q8_0_noalloc": (I, [P, P, P, P, P, I64, I64, I64, I, P]),
+            "qmm_linear_q4_0": (I, [P, P, P, I64, P, P, P, I64, I64, I64, I, P]),
+            "qmm_linear_q4_0_grouped": (I, [P, I, I64, I, P]),
             "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
             "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
             "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
@@ -220,13 +222,88 @@ def gemm_q4_0_q8_0(wq, wd, aq, ad, y=None, workspace=None):
     return y
 
 
-def linear_q4_0(x, wq, wd, y=None, gemv_max_m: int = GEMV_MAX_M):
-    """y = x @ dequant(W)^T: quantize x to Q8_0, then the GEMV for m <=
-    gemv_max_m and the tensor-core GEMM above it."""
-    aq, ad = quantize_act_q8_0(x)
-    if aq.shape[0] <= gemv_max_m:
-        return gemv_q4_0_q8_0(wq, wd, aq, ad, y=y)
-    return gemm_q4_0_q8_0(wq, wd, aq, ad, y=y)
+LINEAR_PDL = 1
+GROUP_MAX = 16
+
+
+class LinearProblem(ctypes.Structure):
+    """qmm_linear_problem: one weight matrix of qmm_linear_q4_0_grouped."""
+    _fields_ = [("wq", ctypes.c_void_p), ("wd", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("ldx", ctypes.c_int64), ("aq", ctypes.c_void_p), ("ad", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+def linear_q4_0(x, wq, wd, y=None, pdl: bool = False, aq=None, ad=None, workspace=None,
+                codes: bool = False):
+    """y = x @ dequant(W)^T with Q8_0 activations, one library call.
+
+    m <= 16: qmm_linear_q4_0, the quantizer then the decode GEMV; pdl=True
+    launches both with programmatic dependent launch,
+    so in a chain of layers on one stream each layer's weights stream while
+    the previous layer finishes (the weights must not be written by work
+    still running on the stream).  m > 16: quantizer + tensor-core GEMM
+    (workspace used there).  aq/ad are optional preallocated code and scale
+    buffers; codes=True also returns (aq, ad)."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    m, k = x.shape
+    n = wq.shape[0]
+    if m <= GEMV_MAX_M:
+        _dev(wq, torch.uint8, "wq", (n, k // 2))
+        _dev(wd, torch.float16, "wd", (n, k // QK))
+        aq = _empty((m, k), torch.int8, x) if aq is None else aq
+        ad = _empty((m, k // QK), torch.float16, x) if ad is None else ad
+        y = _empty((m, n), torch.float32, x) if y is None else y
+        st = load().qmm_linear_q4_0(wq.data_ptr(), wd.data_ptr(), _dev(x, torch.float32, "x"), k,
+                                    _dev(aq, torch.int8, "aq", (m, k)),
+                                    _dev(ad, torch.float16, "ad", (m, k // QK)),
+                                    _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                    LINEAR_PDL if pdl else 0, _stream())
+        _check(st, "qmm_linear_q4_0")
+        return (y, aq, ad) if codes else y
+    aq, ad = quantize_act_q8_0(x, aq=aq, ad=ad)
+    y = gemm_q4_0_q8_0(wq, wd, aq, ad, y=y, workspace=workspace)
+    return (y, aq, ad) if codes else y
+
+
+def linear_q4_0_grouped(problems, pdl: bool = False):
+    """Independent decode linear layers with the same m in two launches.
+
+    problems: a list of (x, wq, wd) or (x, wq, wd, y, aq, ad) tuples (missing
+    outputs are allocated).  Returns the list of (y, aq, ad).  Each result is
+    bit for bit that of linear_q4_0 on the problem alone."""
+    torch = _torch()
+    if not 1 <= len(problems) <= GROUP_MAX:
+        raise ValueError(f"1..{GROUP_MAX} problems, got {len(problems)}")
+    table = (LinearProblem * len(problems))()
+    outs = []
+    m = None
+    for p, prob in enumerate(problems):
+        x, wq, wd = prob[:3]
+        if x.dim() == 1:
+            x = x.unsqueeze(0)
+        mp, k = x.shape
+        if m is None:
+            m = mp
+        if mp != m:
+            raise ValueError("every problem of a group has the same m")
+        n = wq.shape[0]
+        y, aq, ad = (tuple(prob[3:6]) + (None, None, None))[:3]
+        y = _empty((m, n), torch.float32, x) if y is None else y
+        aq = _empty((m, k), torch.int8, x) if aq is None else aq
+        ad = _empty((m, k // QK), torch.float16, x) if ad is None else ad
+        table[p] = LinearProblem(_dev(wq, torch.uint8, "wq", (n, k // 2)),
+                                 _dev(wd, torch.float16, "wd", (n, k // QK)),
+                                 _dev(x, torch.float32, "x"), k,
+                                 _dev(aq, torch.int8, "aq", (m, k)),
+                                 _dev(ad, torch.float16, "ad", (m, k // QK)),
+                                 _dev(y, torch.float32, "y", (m, n)), n, k)
+        outs.append((y, aq, ad))
+    st = load().qmm_linear_q4_0_grouped(ctypes.addressof(table), len(problems), m,
+                                        LINEAR_PDL if pdl else 0, _stream())
+    _check(st, "qmm_linear_q4_0_grouped")
+    return outs
 
 
 # ---------------------------------------------------------------------------

@@ -56,18 +56,25 @@ __device__ __forceinline__ float h2f(unsigned short h) {
 // ---------------------------------------------------------------------------
 // Q4_0 x Q8_0
 
-template <int MT, int ROWS, bool EMIT>
-__global__ void __launch_bounds__(kWarps * 32)
-gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__restrict__ wd,
-                      const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
-                      float *__restrict__ out, int32_t *__restrict__ sumi, int m, int64_t n,
-                      int64_t k, int64_t kb_per_split) {
+// One CTA's share of the GEMV: row group `group` (kWarps * ROWS rows), k
+// slice `slice`.  PDL: the warp loads its first batch of weight blocks and
+// scales (model parameters, never written by the preceding kernels), then
+// waits for the predecessor (the activation quantizer) before it reads aq/ad
+// or writes out.
+template <int MT, int ROWS, bool EMIT, bool PDL>
+__device__ __forceinline__ void gemv_cta(const uint8_t *__restrict__ wq,
+                                         const unsigned short *__restrict__ wd,
+                                         const int8_t *__restrict__ aq,
+                                         const unsigned short *__restrict__ ad,
+                                         float *__restrict__ out, int32_t *__restrict__ sumi,
+                                         int m, int64_t n, int64_t k, int64_t kb_per_split,
+                                         int64_t group, int64_t slice) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t kb = k / kQK;
-    const int64_t row0 = ((int64_t)blockIdx.x * kWarps + warp) * ROWS;
+    const int64_t row0 = (group * kWarps + warp) * ROWS;
     if (row0 >= n) return;
-    const int64_t kb0 = (int64_t)blockIdx.y * kb_per_split;
+    const int64_t kb0 = slice * kb_per_split;
     const int64_t kb1 = min(kb, kb0 + kb_per_split);
     const int64_t wrow = k / 2;  // bytes per weight row
 
@@ -77,9 +84,9 @@ gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__re
 #pragma unroll
         for (int t = 0; t < MT; ++t) acc[r][t] = 0.0f;
 
-    for (int64_t bb = kb0 + lane; bb < kb1; bb += 32 * kUnroll) {
-        uint4 wv[kUnroll][ROWS];
-        unsigned short dwv[kUnroll][ROWS];
+    uint4 wv[kUnroll][ROWS];
+    unsigned short dwv[kUnroll][ROWS];
+    auto load_batch = [&](int64_t bb) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t b = bb + 32 * u;
@@ -95,6 +102,15 @@ gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__re
                 }
             }
         }
+    };
+    const int64_t first = kb0 + lane;
+    if (PDL) {
+        load_batch(first);
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    for (int64_t bb = first; bb < kb1; bb += 32 * kUnroll) {
+        if (!PDL || bb != first) load_batch(bb);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t b = bb + 32 * u;
@@ -135,33 +151,63 @@ gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__re
             }
         }
     }
-    if (EMIT) return;
+    if constexpr (!EMIT) {  // the emitting variant stores block sums only
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-            float v = acc[r][t];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            acc[r][t] = v;
-        }
-    if (lane == 0) {
-        float *dst = out + (int64_t)blockIdx.y * m * n;  // split slice (0 when unsplit)
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r) {
-            if (row0 + r >= n) break;
+        for (int r = 0; r < ROWS; ++r)
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-                if (t >= m) break;
-                dst[(int64_t)t * n + row0 + r] = acc[r][t];
+                float v = acc[r][t];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                acc[r][t] = v;
+            }
+        if (lane == 0) {
+            float *dst = out + slice * m * n;  // split slice (0 when unsplit)
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                if (row0 + r >= n) break;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t >= m) break;
+                    dst[(int64_t)t * n + row0 + r] = acc[r][t];
+                }
             }
         }
     }
 }
 
+template <int MT, int ROWS, bool EMIT, bool PDL>
+__global__ void __launch_bounds__(kWarps * 32)
+gemv_q4_0_q8_0_kernel(const uint8_t *__restrict__ wq, const unsigned short *__restrict__ wd,
+                      const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
+                      float *__restrict__ out, int32_t *__restrict__ sumi, int m, int64_t n,
+                      int64_t k, int64_t kb_per_split) {
+    gemv_cta<MT, ROWS, EMIT, PDL>(wq, wd, aq, ad, out, sumi, m, n, k, kb_per_split, blockIdx.x,
+                                  blockIdx.y);
+}
+
+// Several independent GEMVs in one launch: CTA c serves the problem whose
+// range of CTAs holds c (the table is a kernel parameter, read in place).
+template <int MT, int ROWS, bool PDL>
+__global__ void __launch_bounds__(kWarps * 32)
+gemv_grouped_kernel(const __grid_constant__ LinearGroup tab) {
+    int p = 0;
+    while (p + 1 < tab.count && (int64_t)blockIdx.x >= tab.cta_end[p]) ++p;
+    const int64_t group = (int64_t)blockIdx.x - (p ? tab.cta_end[p - 1] : 0);
+    const LinearProblem &P = tab.p[p];
+    gemv_cta<MT, ROWS, false, PDL>(P.wq, reinterpret_cast<const unsigned short *>(P.wd), P.aq,
+                                   reinterpret_cast<const unsigned short *>(P.ad), P.y, nullptr,
+                                   tab.m, P.n, P.k, P.k / kQK, group, 0);
+}
+
 // y[i] = sum over slices s = 0..S-1 of partials[s][i], in that order.
+template <bool PDL>
 __global__ void splitk_reduce_kernel(const float *__restrict__ partials, float *__restrict__ y,
                                      int64_t count, int splits) {
+    if (PDL) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= count) return;
     float v = partials[i];
@@ -172,18 +218,21 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ partials, float *
 template <int MT, int ROWS>
 cudaError_t launch_q4(const uint8_t *wq, const uint16_t *wd, const int8_t *aq, const uint16_t *ad,
                       float *out, int32_t *sumi, int64_t m, int64_t n, int64_t k, int split,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool pdl) {
     const int64_t kb = k / kQK;
     const int64_t per = (kb + split - 1) / split;
     const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
     dim3 grid((unsigned)((n + rows_per_cta - 1) / rows_per_cta), (unsigned)split);
     const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
     const auto *adp = reinterpret_cast<const unsigned short *>(ad);
+    if (pdl)
+        return launch_kernel(gemv_q4_0_q8_0_kernel<MT, ROWS, false, true>, grid, dim3(kWarps * 32),
+                             0, s, true, wq, wdp, aq, adp, out, sumi, (int)m, n, k, per);
     if (sumi)
-        gemv_q4_0_q8_0_kernel<MT, ROWS, true><<<grid, kWarps * 32, 0, s>>>(
+        gemv_q4_0_q8_0_kernel<MT, ROWS, true, false><<<grid, kWarps * 32, 0, s>>>(
             wq, wdp, aq, adp, out, sumi, (int)m, n, k, per);
     else
-        gemv_q4_0_q8_0_kernel<MT, ROWS, false><<<grid, kWarps * 32, 0, s>>>(
+        gemv_q4_0_q8_0_kernel<MT, ROWS, false, false><<<grid, kWarps * 32, 0, s>>>(
             wq, wdp, aq, adp, out, sumi, (int)m, n, k, per);
     return cudaPeekAtLastError();
 }
@@ -332,6 +381,21 @@ cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, co
     return cudaPeekAtLastError();
 }
 
+template <int MT, int ROWS>
+cudaError_t launch_grouped(LinearGroup tab, bool pdl, cudaStream_t s) {
+    const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
+    int64_t total = 0;
+    for (int p = 0; p < tab.count; ++p) {
+        total += (tab.p[p].n + rows_per_cta - 1) / rows_per_cta;
+        tab.cta_end[p] = total;
+    }
+    if (pdl)
+        return launch_kernel(gemv_grouped_kernel<MT, ROWS, true>, dim3((unsigned)total),
+                             dim3(kWarps * 32), 0, s, true, tab);
+    gemv_grouped_kernel<MT, ROWS, false><<<(unsigned)total, kWarps * 32, 0, s>>>(tab);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -357,19 +421,23 @@ size_t gemv_workspace_bytes(int64_t m, int64_t n, int64_t /*k*/, int split) {
 cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, int split, float *partials,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, bool pdl) {
+    if (sumi) pdl = false;
     float *out = split > 1 ? partials : y;
     cudaError_t e;
-    if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
-    else if (m == 2) e = launch_q4<2, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
-    else if (m <= 4) e = launch_q4<4, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
-    else if (m <= 8) e = launch_q4<8, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
-    else e = launch_q4<16, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s);
+    if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
+    else if (m == 2) e = launch_q4<2, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
+    else if (m <= 4) e = launch_q4<4, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
+    else if (m <= 8) e = launch_q4<8, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
+    else e = launch_q4<16, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
     if (e != cudaSuccess || split <= 1 || sumi) return e;
     const int64_t count = m * n;
     const int threads = 256;
-    splitk_reduce_kernel<<<(unsigned)((count + threads - 1) / threads), threads, 0, s>>>(
-        partials, y, count, split);
+    const dim3 grid((unsigned)((count + threads - 1) / threads));
+    if (pdl)
+        return launch_kernel(splitk_reduce_kernel<true>, grid, dim3(threads), 0, s, true,
+                             (const float *)partials, y, count, split);
+    splitk_reduce_kernel<false><<<grid, threads, 0, s>>>(partials, y, count, split);
     return cudaPeekAtLastError();
 }
 
@@ -381,6 +449,17 @@ cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *a
     if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+}
+
+cudaError_t launch_linear_grouped(const LinearGroup &tab, bool pdl, cudaStream_t s) {
+    cudaError_t e = launch_quantize_grouped(tab, s, pdl);
+    if (e != cudaSuccess) return e;
+    const int m = tab.m;
+    if (m == 1) return launch_grouped<1, 2>(tab, pdl, s);
+    if (m == 2) return launch_grouped<2, 2>(tab, pdl, s);
+    if (m <= 4) return launch_grouped<4, 1>(tab, pdl, s);
+    if (m <= 8) return launch_grouped<8, 1>(tab, pdl, s);
+    return launch_grouped<16, 1>(tab, pdl, s);
 }
 
 // ---------------------------------------------------------------------------

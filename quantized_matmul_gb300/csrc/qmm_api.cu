@@ -18,6 +18,7 @@ namespace {
 using qmm::kQK;
 static_assert(qmm::kGemvNoAllocScratchFloats == QMM_NOALLOC_SCRATCH_FLOATS,
               "the header and the library must agree on the built-in scratch size");
+static_assert(qmm::kGroupMax == QMM_GROUP_MAX, "the header and the library must agree");
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_ok[kMaxDevices];  // 0 unknown, 1 supported, 2 not supported
@@ -66,6 +67,16 @@ qmm_status gemv_split(int split_k, int64_t m, int64_t n, int64_t k, int *out) {
     int s = split_k == 0 ? qmm::gemv_auto_split(m, n, k) : split_k;
     if (s > k / kQK || s > 65535) return QMM_ERR_ARG;
     *out = s;
+    return QMM_OK;
+}
+
+qmm_status check_linear(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
+                        const int8_t *aq, const uint16_t *ad, const float *y, int64_t m,
+                        int64_t n, int64_t k) {
+    if (!x) return QMM_ERR_NULL;
+    if (qmm_status st = check_q4_common(wq, wd, aq, ad, y, m, n, k)) return st;
+    if (m > QMM_GEMV_MAX_M || ldx < k || m * ldx > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(x, 4)) return QMM_ERR_ALIGN;
     return QMM_OK;
 }
 
@@ -130,6 +141,43 @@ qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, con
     if (qmm_status st = check_device()) return st;
     return launch_status(qmm::launch_gemv_q4_0_q8_0_noalloc(wq, wd, aq, ad, y, m, n, k, split,
                                                             as_stream(stream)));
+}
+
+qmm_status qmm_linear_q4_0(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
+                           int8_t *aq, uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                           int flags, void *stream) {
+    if (qmm_status st = check_linear(wq, wd, x, ldx, aq, ad, y, m, n, k)) return st;
+    if (flags & ~QMM_LINEAR_PDL) return QMM_ERR_ARG;
+    if (qmm_status st = check_device()) return st;
+    const bool pdl = (flags & QMM_LINEAR_PDL) != 0;
+    const cudaStream_t s = as_stream(stream);
+    cudaError_t e = qmm::launch_quantize_act_q8_0(x, m, k, ldx, aq, ad, s, pdl);
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    return launch_status(qmm::launch_gemv_q4_0_q8_0(wq, wd, aq, ad, y, nullptr, m, n, k, 1,
+                                                    nullptr, s, pdl));
+}
+
+qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count, int64_t m,
+                                   int flags, void *stream) {
+    if (!problems) return QMM_ERR_NULL;
+    if (count < 1 || count > QMM_GROUP_MAX) return QMM_ERR_ARG;
+    if (flags & ~QMM_LINEAR_PDL) return QMM_ERR_ARG;
+    qmm::LinearGroup tab = {};
+    int64_t ctas = 0, blocks = 0;
+    for (int p = 0; p < count; ++p) {
+        const qmm_linear_problem &P = problems[p];
+        if (qmm_status st = check_linear(P.wq, P.wd, P.x, P.ldx, P.aq, P.ad, P.y, m, P.n, P.k))
+            return st;
+        ctas += (P.n + 15) / 16;
+        blocks += m * (P.k / kQK);
+        tab.p[p] = {P.wq, P.wd, P.x, P.ldx, P.aq, P.ad, P.y, P.n, P.k};
+    }
+    if (ctas >= (int64_t(1) << 31) || blocks >= (int64_t(1) << 33)) return QMM_ERR_SHAPE;
+    tab.count = count;
+    tab.m = (int)m;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(
+        qmm::launch_linear_grouped(tab, (flags & QMM_LINEAR_PDL) != 0, as_stream(stream)));
 }
 
 qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,

@@ -11,9 +11,61 @@ namespace qmm {
 
 constexpr int kQK = 32;  // elements per quantization block
 
+// Programmatic dependent launch.  A kernel launched with `pdl` set may start
+// while the previous kernel on its stream is still running.  pdl_wait()
+// returns once that kernel has completed and its writes are visible (at once
+// when the launch had no such predecessor), so everything a kernel reads
+// from its predecessor comes after it; pdl_launch_dependents() lets the next
+// PDL launch on the stream begin once every CTA of this grid has called it
+// or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+// A group of independent decode linear layers sharing m: layer p computes
+// y_p = x_p W_p^T (Q8_0 quantization of x_p into aq_p/ad_p, then the GEMV).
+// Passed by value as a kernel parameter, so no device copy of the table.
+constexpr int kGroupMax = 16;
+struct LinearProblem {
+    const uint8_t *wq;
+    const uint16_t *wd;
+    const float *x;
+    int64_t ldx;
+    int8_t *aq;
+    uint16_t *ad;
+    float *y;
+    int64_t n, k;
+};
+struct LinearGroup {
+    LinearProblem p[kGroupMax];
+    int64_t cta_end[kGroupMax];  // cumulative CTA counts (filled by the launchers)
+    int count;
+    int m;
+};
+
 // quant.cu
+// The quantizer over every problem of a group in one launch.
+cudaError_t launch_quantize_grouped(const LinearGroup &g, cudaStream_t s, bool pdl);
+// pdl: launch with programmatic dependent launch (x is read after pdl_wait)
 cudaError_t launch_quantize_act_q8_0(const float *x, int64_t m, int64_t k, int64_t ldx,
-                                     int8_t *aq, uint16_t *ad, cudaStream_t s);
+                                     int8_t *aq, uint16_t *ad, cudaStream_t s, bool pdl = false);
 cudaError_t launch_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
                                         uint8_t *wq, uint16_t *wd, cudaStream_t s);
 cudaError_t launch_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t *aq,
@@ -25,10 +77,13 @@ cudaError_t launch_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t 
 int gemv_auto_split(int64_t m, int64_t n, int64_t k);
 size_t gemv_workspace_bytes(int64_t m, int64_t n, int64_t k, int split);
 // sumi != nullptr selects the block-sum emitting variant (split must be 1).
+// pdl: launch with programmatic dependent launch; the GEMV then loads its
+// first weight blocks before pdl_wait and everything else after it (sumi
+// must be null).
 cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, int split, float *partials,
-                                  cudaStream_t s);
+                                  cudaStream_t s, bool pdl = false);
 // Split-K GEMV whose partials live in a library-owned device array of
 // kGemvNoAllocScratchFloats floats (split * m * n must fit).
 constexpr int64_t kGemvNoAllocScratchFloats = int64_t(1) << 20;
@@ -38,6 +93,8 @@ cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s);
+// Quantizer then GEMV (unsplit) for every problem of the group: two launches.
+cudaError_t launch_linear_grouped(const LinearGroup &g, bool pdl, cudaStream_t s);
 
 // gemm.cu
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);

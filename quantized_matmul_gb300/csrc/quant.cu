@@ -31,15 +31,12 @@ __device__ __forceinline__ unsigned short f32_to_f16_bits(float v) {
     return __half_as_ushort(__float2half_rn(v));
 }
 
-// Q8_0: grid covers m * (k/32) blocks, one warp each.
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-quantize_act_q8_0_kernel(const float *__restrict__ x, int64_t m, int64_t k, int64_t ldx,
-                         int8_t *__restrict__ aq, unsigned short *__restrict__ ad) {
-    const int lane = threadIdx.x & 31;
+// One Q8_0 block (row i, block b) per warp, lane j holding element j.
+__device__ __forceinline__ void quantize_q8_0_block(const float *__restrict__ x, int64_t ldx,
+                                                    int64_t k, int64_t i, int64_t b, int lane,
+                                                    int8_t *__restrict__ aq,
+                                                    unsigned short *__restrict__ ad) {
     const int64_t kb = k / kQK;
-    const int64_t blk = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (blk >= m * kb) return;
-    const int64_t i = blk / kb, b = blk - i * kb;
     const float v = x[i * ldx + b * kQK + lane];
     const float amax = warp_max(fabsf(v));
     const float d = __fdiv_rn(amax, 127.0f);
@@ -47,6 +44,45 @@ quantize_act_q8_0_kernel(const float *__restrict__ x, int64_t m, int64_t k, int6
     if (d != 0.0f) q = fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
     aq[i * k + b * kQK + lane] = (int8_t)(int)q;
     if (lane == 0) ad[i * kb + b] = f32_to_f16_bits(d);
+}
+
+// Q8_0: grid covers m * (k/32) blocks, one warp each.  With PDL the next
+// kernel (the GEMV) may launch at once and stream its weights while this
+// grid waits for x from its own predecessor.
+template <bool PDL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+quantize_act_q8_0_kernel(const float *__restrict__ x, int64_t m, int64_t k, int64_t ldx,
+                         int8_t *__restrict__ aq, unsigned short *__restrict__ ad) {
+    if (PDL) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+    const int64_t kb = k / kQK;
+    const int64_t blk = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (blk >= m * kb) return;
+    const int64_t i = blk / kb;
+    quantize_q8_0_block(x, ldx, k, i, blk - i * kb, threadIdx.x & 31, aq, ad);
+}
+
+// The same over a group of problems: warp w serves the problem whose range
+// of blocks holds w (cta_end here counts blocks, filled by the launcher).
+template <bool PDL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+quantize_grouped_kernel(const __grid_constant__ LinearGroup tab) {
+    if (PDL) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
+    const int64_t blk = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (blk >= tab.cta_end[tab.count - 1]) return;
+    int p = 0;
+    while (p + 1 < tab.count && blk >= tab.cta_end[p]) ++p;
+    const LinearProblem &P = tab.p[p];
+    const int64_t local = blk - (p ? tab.cta_end[p - 1] : 0);
+    const int64_t kb = P.k / kQK;
+    const int64_t i = local / kb;
+    quantize_q8_0_block(P.x, P.ldx, P.k, i, local - i * kb, threadIdx.x & 31, P.aq,
+                        reinterpret_cast<unsigned short *>(P.ad));
 }
 
 // Q4_0: one warp per block; the signed absmax is the element of largest |w|
@@ -137,11 +173,30 @@ __global__ void pack_ternary_kernel(const int8_t *__restrict__ t, int64_t words,
 }  // namespace
 
 cudaError_t launch_quantize_act_q8_0(const float *x, int64_t m, int64_t k, int64_t ldx,
-                                     int8_t *aq, uint16_t *ad, cudaStream_t s) {
+                                     int8_t *aq, uint16_t *ad, cudaStream_t s, bool pdl) {
     const int64_t blocks = m * (k / kQK);
     const int64_t grid = (blocks + kWarpsPerCta - 1) / kWarpsPerCta;
-    quantize_act_q8_0_kernel<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(
-        x, m, k, ldx, aq, reinterpret_cast<unsigned short *>(ad));
+    auto *adp = reinterpret_cast<unsigned short *>(ad);
+    if (pdl)
+        return launch_kernel(quantize_act_q8_0_kernel<true>, dim3((unsigned)grid),
+                             dim3(kWarpsPerCta * 32), 0, s, true, x, m, k, ldx, aq, adp);
+    quantize_act_q8_0_kernel<false><<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(
+        x, m, k, ldx, aq, adp);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_quantize_grouped(const LinearGroup &g, cudaStream_t s, bool pdl) {
+    LinearGroup tab = g;
+    int64_t total = 0;
+    for (int p = 0; p < tab.count; ++p) {
+        total += (int64_t)tab.m * (tab.p[p].k / kQK);
+        tab.cta_end[p] = total;
+    }
+    const dim3 grid((unsigned)((total + kWarpsPerCta - 1) / kWarpsPerCta));
+    if (pdl)
+        return launch_kernel(quantize_grouped_kernel<true>, grid, dim3(kWarpsPerCta * 32), 0, s,
+                             true, tab);
+    quantize_grouped_kernel<false><<<grid, kWarpsPerCta * 32, 0, s>>>(tab);
     return cudaPeekAtLastError();
 }
 

@@ -32,6 +32,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ["qmm_quantize_act_q8_0", "qmm_gemv_q4_0_q8_0", "qmm_gemm_q4_0_q8_0",
                      "qmm_bitnet_gemv", "qmm_quantize_act_bitnet", "qmm_workspace_bytes",
+                     "qmm_linear_q4_0", "qmm_linear_q4_0_grouped",
                      "qmm_check_device_error", "qmm_status_string"]:
         assert required in names
 
@@ -116,6 +117,25 @@ def test_argument_errors_return_before_any_launch(lib):
     # split_k out of range
     assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, 3, A16, 1 << 20, None) == QMM_ERR_ARG
     assert lib.qmm_gemv_q4_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, -1, A16, 1 << 20, None) == QMM_ERR_ARG
+    # decode linear: m above the GEMV limit, ldx below k, bad flags
+    assert lib.qmm_linear_q4_0(A16, A16, A16, 32, A16, A16, A16, 17, 1, 32, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_linear_q4_0(A16, A16, A16, 16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_linear_q4_0(A16, A16, A16, 32, A16, A16, A16, 1, 1, 32, 2, None) == QMM_ERR_ARG
+    assert lib.qmm_linear_q4_0(A16, A16, None, 32, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_NULL
+    assert lib.qmm_linear_q4_0(A16, A16, A2, 32, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_ALIGN
+    # grouped: table checks
+    import quantized_matmul_gb300 as q
+    tab = (q.LinearProblem * 17)()
+    for i in range(17):
+        tab[i] = q.LinearProblem(0x10000, 0x10000, 0x10000, 32, 0x10000, 0x10000, 0x10000, 1, 32)
+    assert lib.qmm_linear_q4_0_grouped(None, 1, 1, 0, None) == QMM_ERR_NULL
+    assert lib.qmm_linear_q4_0_grouped(ctypes.addressof(tab), 0, 1, 0, None) == QMM_ERR_ARG
+    assert lib.qmm_linear_q4_0_grouped(ctypes.addressof(tab), 17, 1, 0, None) == QMM_ERR_ARG
+    tab[3].k = 48
+    assert lib.qmm_linear_q4_0_grouped(ctypes.addressof(tab), 5, 1, 0, None) == QMM_ERR_SHAPE
+    tab[3].k = 32
+    tab[2].aq = 0x10004
+    assert lib.qmm_linear_q4_0_grouped(ctypes.addressof(tab), 5, 1, 0, None) == QMM_ERR_ALIGN
     # debug entry: unknown path
     assert lib.qmm_debug_block_sums_q4_0_q8_0(5, A16, A16, A16, 1, 1, 32, None, 0, None) == QMM_ERR_ARG
 

@@ -215,3 +215,143 @@ def test_gemm_wait_timeout_reports_and_device_stays_usable(qmm, orc):
     assert qmm.check_device_error() == 0
     y_ref = orc.gemm_q4_0_q8_0(wq, wd, aq, ad)
     assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# decode linear layer: quantizer + GEMV in one call, optionally chained with
+# programmatic dependent launch
+
+LINEAR_SHAPES = [(1, 1, 32), (1, 129, 4096), (2, 300, 11008), (3, 65, 4064), (4, 33, 1024),
+                 (5, 33, 1024), (8, 257, 4096), (16, 70, 2048), (1, 4096, 11008),
+                 (1, 11008, 4096), (2, 17, 96), (4, 40, 16384), (3, 9, 19680)]
+
+
+@pytest.mark.parametrize("m,n,k", LINEAR_SHAPES)
+@pytest.mark.parametrize("pdl", [False, True])
+def test_linear_matches_separate_calls_and_oracle(qmm, orc, m, n, k, pdl):
+    """qmm_linear_q4_0 gives the oracle's codes bit for bit and the separate
+    calls' y."""
+    w, _ = synthetic.q4_0_case(6000 + m + n, n, k, 1)
+    x = adversarial_x(6100 + m, m, k)
+    wq, wd = orc.quantize_q4_0(w)
+    aq_ref, ad_ref = orc.quantize_q8_0(x)
+    wq_d, wd_d = to_dev(wq), to_dev(wd.view(np.float16))
+    y, aq, ad = qmm.linear_q4_0(to_dev(x), wq_d, wd_d, pdl=pdl, codes=True)
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(f16_bits(ad), ad_ref)
+    aq2, ad2 = qmm.quantize_act_q8_0(to_dev(x))
+    y2 = qmm.gemv_q4_0_q8_0(wq_d, wd_d, aq2, ad2, split_k=1)
+    assert np.array_equal(to_np(y).view(np.uint32), to_np(y2).view(np.uint32))
+    ok, worst, maxrel = rel_gate(to_np(y), orc.gemm_q4_0_q8_0(wq, wd, aq_ref, ad_ref),
+                                 orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_ref, ad_ref))
+    assert ok, (worst, maxrel)
+
+
+GROUP_SHAPES = [(129, 4096), (300, 11008), (65, 4064), (1, 32), (4096, 4096), (40, 96),
+                (11008, 4096)]
+
+
+@pytest.mark.parametrize("m", [1, 3, 16])
+@pytest.mark.parametrize("pdl", [False, True])
+def test_linear_grouped_matches_single_calls_and_oracle(qmm, orc, m, pdl):
+    """Every problem of a group gets the bits qmm_linear_q4_0 gives it alone,
+    and the oracle's codes."""
+    probs, refs = [], []
+    for j, (n, k) in enumerate(GROUP_SHAPES):
+        w, _ = synthetic.q4_0_case(6500 + j, n, k, 1)
+        x = adversarial_x(6600 + j + m, m, k)
+        wq, wd = orc.quantize_q4_0(w)
+        wq_d, wd_d = to_dev(wq), to_dev(wd.view(np.float16))
+        probs.append((to_dev(x), wq_d, wd_d))
+        refs.append((x, wq, wd))
+    outs = qmm.linear_q4_0_grouped(probs, pdl=pdl)
+    for (x_d, wq_d, wd_d), (x, wq, wd), (y, aq, ad) in zip(probs, refs, outs):
+        y1, aq1, ad1 = qmm.linear_q4_0(x_d, wq_d, wd_d, codes=True)
+        assert np.array_equal(to_np(aq), to_np(aq1))
+        assert np.array_equal(f16_bits(ad), f16_bits(ad1))
+        assert np.array_equal(to_np(y).view(np.uint32), to_np(y1).view(np.uint32))
+        aq_ref, ad_ref = orc.quantize_q8_0(x)
+        assert np.array_equal(to_np(aq), aq_ref)
+        assert np.array_equal(f16_bits(ad), ad_ref)
+        ok, worst, maxrel = rel_gate(to_np(y), orc.gemm_q4_0_q8_0(wq, wd, aq_ref, ad_ref),
+                                     orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_ref, ad_ref))
+        assert ok, (worst, maxrel)
+
+
+def test_linear_grouped_full_table(qmm, orc):
+    """A table of QMM_GROUP_MAX problems, all of one tiny shape."""
+    probs, refs = [], []
+    for j in range(qmm.GROUP_MAX):
+        w, x = synthetic.q4_0_case(6700 + j, 24 + j, 64, 2)
+        wq, wd = orc.quantize_q4_0(w)
+        probs.append((to_dev(x), to_dev(wq), to_dev(wd.view(np.float16))))
+        refs.append((x, wq, wd))
+    outs = qmm.linear_q4_0_grouped(probs)
+    for (x, wq, wd), (y, aq, ad) in zip(refs, outs):
+        aq_ref, ad_ref = orc.quantize_q8_0(x)
+        assert np.array_equal(to_np(aq), aq_ref)
+        ok, worst, maxrel = rel_gate(to_np(y), orc.gemm_q4_0_q8_0(wq, wd, aq_ref, ad_ref),
+                                     orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_ref, ad_ref))
+        assert ok, (worst, maxrel)
+
+
+def test_linear_reads_strided_rows(qmm, orc):
+    """x rows with a leading dimension above k (a column slice of a wider
+    buffer) quantize exactly like a packed copy."""
+    import torch
+    m, n, k = 3, 50, 2048
+    w, _ = synthetic.q4_0_case(6400, n, k, 1)
+    x = adversarial_x(6401, m, k + 96)
+    wq, wd = orc.quantize_q4_0(w)
+    xd = to_dev(x)[:, :k]
+    aq_ref, ad_ref = orc.quantize_q8_0(np.ascontiguousarray(x[:, :k]))
+    wq_d, wd_d = to_dev(wq), to_dev(wd.view(np.float16))
+    aq = torch.empty(m, k, dtype=torch.int8, device="cuda")
+    ad = torch.empty(m, k // 32, dtype=torch.float16, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    lib = qmm.load()
+    st = lib.qmm_linear_q4_0(wq_d.data_ptr(), wd_d.data_ptr(), xd.data_ptr(), k + 96,
+                             aq.data_ptr(), ad.data_ptr(), y.data_ptr(), m, n, k, 0,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(f16_bits(ad), ad_ref)
+    ok, worst, maxrel = rel_gate(to_np(y), orc.gemm_q4_0_q8_0(wq, wd, aq_ref, ad_ref),
+                                 orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_ref, ad_ref))
+    assert ok, (worst, maxrel)
+
+
+@pytest.mark.parametrize("m", [1, 4])
+def test_linear_pdl_chain_reads_the_previous_layer_output(qmm, orc, m):
+    """Layer i+1 consumes layer i's output and shares its aq buffer; with
+    programmatic dependent launch every kernel must still wait for its
+    predecessor before it reads them, so the chain gives the same bits with
+    and without PDL, and each layer's output matches the oracle applied to
+    that layer's actual input.  The 11008 -> 4096 layer is split over k
+    (three kernels in that layer)."""
+    import torch
+    dims = [4096, 11008, 4096, 4096]
+    layers = []
+    for j in range(len(dims) - 1):
+        w, _ = synthetic.q4_0_case(6200 + j, dims[j + 1], dims[j], 1)
+        wq, wd = orc.quantize_q4_0(w)
+        layers.append((wq, wd, to_dev(wq), to_dev(wd.view(np.float16))))
+    _, x0 = synthetic.q4_0_case(6299, 1, dims[0], m)
+    aq_flat = torch.empty(m * max(dims), dtype=torch.int8, device="cuda")
+    outs = {}
+    for pdl in (False, True):
+        hs = [to_dev(x0)]
+        for j, (_, _, wq_d, wd_d) in enumerate(layers):
+            aq_j = aq_flat[: m * dims[j]].view(m, dims[j])
+            hs.append(qmm.linear_q4_0(hs[-1], wq_d, wd_d, pdl=pdl, aq=aq_j))
+        torch.cuda.synchronize()
+        outs[pdl] = [to_np(h) for h in hs]
+    for a, b in zip(outs[False], outs[True]):
+        assert np.isfinite(a).all()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    for j, (wq, wd, _, _) in enumerate(layers):
+        aq_r, ad_r = orc.quantize_q8_0(outs[True][j])
+        ok, worst, maxrel = rel_gate(outs[True][j + 1], orc.gemm_q4_0_q8_0(wq, wd, aq_r, ad_r),
+                                     orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_r, ad_r))
+        assert ok, (j, worst, maxrel)
