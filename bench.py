@@ -560,7 +560,10 @@ def main():
     ap.add_argument("--configs", choices=["all", "main"], default="all",
                     help="'main' measures only the layer-set headline")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of oracle time for the cpu_baseline leg")
+                    help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
+    ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab"], default=None,
+                    help="profiling aid: run only this workload (steps as given) and print "
+                         "its result; the headline contract line is not produced")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -574,6 +577,15 @@ def main():
         import quantized_matmul_gb300 as q
         q.load()  # the CUDA library; raises if it is missing
         peaks = load_peaks()
+        if args.only:
+            run = {"gemv": lambda: run_single_gemv(q, args.steps, args.warmup, dist, peaks),
+                   "bitnet": lambda: run_bitnet(q, args.steps, args.warmup, dist, peaks),
+                   "prefill": lambda: run_prefill(q, args.steps, args.warmup, dist, peaks),
+                   "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks)}
+            res = run[args.only]()
+            if dist.rank == 0:
+                print(json.dumps({"only": args.only, "result": res}), flush=True)
+            return
         main_res = run_layer_set(q, args, dist, peaks)
         configs = {"layer_set_variants": main_res["variants"]}
         if args.configs == "all":
@@ -582,7 +594,7 @@ def main():
             configs["bitnet_2560x6912"] = run_bitnet(q, short * 5, args.warmup, dist, peaks)
             configs["prefill_512x14336x4096"] = run_prefill(q, max(50, short // 20), 10, dist, peaks)
             configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks)
-        cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 else None
+        cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
         if dist.rank == 0:
             line = {
                 "metric": METRIC, "value": round(main_res["value"], 1), "unit": "GB/s",

@@ -104,7 +104,12 @@ qmm_status qmm_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
  *   kernel on the same stream (deterministic); 0 = the library picks S from
  *   the shape.  S may not exceed k/32.  workspace: device memory of at least
  *   qmm_workspace_bytes(QMM_OP_GEMV_Q4_0_Q8_0, m, n, k, split_k) bytes,
- *   16-byte aligned (NULL allowed when that size is 0). */
+ *   16-byte aligned (NULL allowed when that size is 0).
+ * With one slice and 8 <= m, when k/32 is a multiple of 8, wq, wd, aq and
+ * ad are 16-byte aligned and the quantized activations fit in shared memory,
+ * a persistent kernel streams the weights through shared memory with tensor
+ * copies; otherwise each warp streams them through registers.  Both give
+ * the same bits. */
 qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
                               const int8_t *aq, const uint16_t *ad, float *y,
                               int64_t m, int64_t n, int64_t k, int split_k,
@@ -269,7 +274,8 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
                                 int32_t *dot, int64_t m, int64_t n, int64_t k, void *stream);
 
 /* Upper bound on the polling iterations of every bounded wait inside the
- * GEMM kernel (default 1 << 17; 0 restores the default).  Each poll
+ * GEMM and the streaming GEMV kernels (default 1 << 17; 0 restores the
+ * default).  Each poll
  * suspends the waiting warp for at most 20 microseconds (it resumes as soon
  * as the awaited phase completes).  Affects kernels launched after the
  * call. */
@@ -281,6 +287,11 @@ void qmm_debug_set_wait_limit(uint32_t iterations);
  * (read by qmm_check_device_error), releases its resources and returns, and
  * that the device stays usable.  Outputs of such a call are unspecified. */
 void qmm_debug_withhold_gemm_loads(int enable);
+
+/* The same hook for the shared-memory streaming decode GEMV (see
+ * qmm_gemv_q4_0_q8_0): while enabled its producer arms no stage, so the
+ * consumers' waits run out their limit. */
+void qmm_debug_withhold_gemv_loads(int enable);
 
 #ifdef __cplusplus
 }

@@ -73,6 +73,7 @@ def load() -> ctypes.CDLL:
             "qmm_debug_bitnet_dot": (I, [P, P, P, P, I64, I64, I64, P]),
             "qmm_debug_set_wait_limit": (None, [U32]),
             "qmm_debug_withhold_gemm_loads": (None, [I]),
+            "qmm_debug_withhold_gemv_loads": (None, [I]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -394,3 +395,8 @@ def set_wait_limit(iterations: int) -> None:
 
 def withhold_gemm_loads(enable: bool) -> None:
     load().qmm_debug_withhold_gemm_loads(1 if enable else 0)
+
+
+def withhold_gemv_loads(enable: bool) -> None:
+    """Test hook: the streaming GEMV arms no stage while enabled."""
+    load().qmm_debug_withhold_gemv_loads(1 if enable else 0)

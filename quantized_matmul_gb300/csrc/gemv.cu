@@ -423,6 +423,14 @@ cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
                                   int64_t n, int64_t k, int split, float *partials,
                                   cudaStream_t s, bool pdl) {
     if (sumi) pdl = false;
+    if (!sumi && split <= 1) {
+        LinearGroup tab = {};
+        tab.p[0] = {wq, wd, nullptr, 0, const_cast<int8_t *>(aq), const_cast<uint16_t *>(ad),
+                    y, n, k};
+        tab.count = 1;
+        tab.m = (int)m;
+        if (stream_gemv_supported(tab)) return launch_stream_gemv(tab, pdl, s);
+    }
     float *out = split > 1 ? partials : y;
     cudaError_t e;
     if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
@@ -454,6 +462,7 @@ cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *a
 cudaError_t launch_linear_grouped(const LinearGroup &tab, bool pdl, cudaStream_t s) {
     cudaError_t e = launch_quantize_grouped(tab, s, pdl);
     if (e != cudaSuccess) return e;
+    if (stream_gemv_supported(tab)) return launch_stream_gemv(tab, pdl, s);
     const int m = tab.m;
     if (m == 1) return launch_grouped<1, 2>(tab, pdl, s);
     if (m == 2) return launch_grouped<2, 2>(tab, pdl, s);

@@ -257,9 +257,11 @@ int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k) {
 }
 
 qmm_status qmm_check_device_error(void *stream) {
-    unsigned int word = 0;
+    unsigned int word = 0, word2 = 0;
     if (qmm::gemm_read_and_clear_error(&word, as_stream(stream)) != cudaSuccess) return QMM_ERR_CUDA;
-    return word ? QMM_ERR_TIMEOUT : QMM_OK;
+    if (qmm::stream_read_and_clear_error(&word2, as_stream(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return (word | word2) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 const char *qmm_status_string(qmm_status status) {
@@ -315,8 +317,13 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
                                                  k, as_stream(stream)));
 }
 
-void qmm_debug_set_wait_limit(uint32_t iterations) { qmm::gemm_set_wait_limit(iterations); }
+void qmm_debug_set_wait_limit(uint32_t iterations) {
+    qmm::gemm_set_wait_limit(iterations);
+    qmm::stream_set_wait_limit(iterations);
+}
 
 void qmm_debug_withhold_gemm_loads(int enable) { qmm::gemm_set_withhold_loads(enable); }
+
+void qmm_debug_withhold_gemv_loads(int enable) { qmm::stream_set_withhold_loads(enable); }
 
 }  // extern "C"

@@ -96,6 +96,16 @@ cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *a
 // Quantizer then GEMV (unsplit) for every problem of the group: two launches.
 cudaError_t launch_linear_grouped(const LinearGroup &g, bool pdl, cudaStream_t s);
 
+// gemv_stream.cu: the decode GEMV (unsplit) with the weights staged through
+// shared memory by tensor copies; identical results to the register GEMV.
+// Used when 8 <= m <= 16, every problem has k/32 % 8 == 0 and 16-byte
+// aligned wq, wd, aq, ad, and the activations fit in shared memory.
+bool stream_gemv_supported(const LinearGroup &g);
+cudaError_t launch_stream_gemv(const LinearGroup &g, bool pdl, cudaStream_t s);
+cudaError_t stream_read_and_clear_error(unsigned int *word, cudaStream_t s);
+void stream_set_wait_limit(uint32_t iterations);
+void stream_set_withhold_loads(int enable);
+
 // gemm.cu
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 // sumi != nullptr selects the block-sum emitting variant.

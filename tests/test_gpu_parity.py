@@ -189,6 +189,61 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
 
 
 # ---------------------------------------------------------------------------
+# the two decode GEMV kernels (shared-memory streaming and register streaming)
+
+def _misaligned_copy(t):
+    """The same values at a 2-byte offset from a 16-byte boundary: the library
+    then takes the register-streaming kernel."""
+    import torch
+    flat = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    v = flat[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 == 2
+    return v
+
+
+@pytest.mark.parametrize("m,n,k", [(8, 300, 4096), (16, 129, 11008), (12, 77, 8192),
+                                   (16, 40, 2048), (9, 16, 256), (8, 1, 4096),
+                                   (10, 4099, 4096)])
+def test_streaming_and_register_gemv_agree_bitwise(qmm, orc, m, n, k):
+    wq, wd, aq, ad = q4_case(orc, 7000 + m + n, m, n, k)
+    wq_d, wd_d = to_dev(wq), to_dev(wd.view(np.float16))
+    aq_d, ad_d = to_dev(aq), to_dev(ad.view(np.float16))
+    y_stream = to_np(qmm.gemv_q4_0_q8_0(wq_d, wd_d, aq_d, ad_d, split_k=1))
+    y_reg = to_np(qmm.gemv_q4_0_q8_0(wq_d, _misaligned_copy(wd_d), aq_d, ad_d, split_k=1))
+    assert np.array_equal(y_stream.view(np.uint32), y_reg.view(np.uint32))
+    ok, worst, maxrel = rel_gate(y_stream, orc.gemm_q4_0_q8_0(wq, wd, aq, ad),
+                                 orc.gemm_q4_0_q8_0_absterms(wq, wd, aq, ad))
+    assert ok, (worst, maxrel)
+
+
+def test_streaming_gemv_wait_timeout_reports_and_device_stays_usable(qmm, orc):
+    """With the streaming GEMV's stages never armed, the consumers' bounded
+    waits must run out, the kernel must record QMM_ERR_TIMEOUT and return;
+    afterwards a normal call on the same context gives the usual result."""
+    import torch
+    wq, wd, aq, ad = q4_case(orc, 7100, 8, 256, 4096)
+    args = (to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    assert qmm.check_device_error() == 0
+    try:
+        qmm.set_wait_limit(200)
+        qmm.withhold_gemv_loads(True)
+        qmm.gemv_q4_0_q8_0(*args, split_k=1)
+        torch.cuda.synchronize()
+        status = qmm.check_device_error()
+    finally:
+        qmm.withhold_gemv_loads(False)
+        qmm.set_wait_limit(0)
+    assert status == 7
+    y = to_np(qmm.gemv_q4_0_q8_0(*args, split_k=1))
+    torch.cuda.synchronize()
+    assert qmm.check_device_error() == 0
+    ok, worst, maxrel = rel_gate(y, orc.gemm_q4_0_q8_0(wq, wd, aq, ad),
+                                 orc.gemm_q4_0_q8_0_absterms(wq, wd, aq, ad))
+    assert ok, (worst, maxrel)
+
+
+# ---------------------------------------------------------------------------
 # bounded waits
 
 def test_gemm_wait_timeout_reports_and_device_stays_usable(qmm, orc):
@@ -247,17 +302,24 @@ def test_linear_matches_separate_calls_and_oracle(qmm, orc, m, n, k, pdl):
     assert ok, (worst, maxrel)
 
 
-GROUP_SHAPES = [(129, 4096), (300, 11008), (65, 4064), (1, 32), (4096, 4096), (40, 96),
-                (11008, 4096)]
+# at m >= 8 the first set streams through shared memory; the second (k/32
+# not a multiple of 8 in some problems) always streams through registers
+GROUP_SHAPE_SETS = {
+    "streaming": [(129, 1024), (300, 2048), (1, 256), (4096, 1024), (40, 2048),
+                  (1100, 512), (17, 512)],
+    "register": [(129, 4096), (300, 11008), (65, 4064), (1, 32), (4096, 4096), (40, 96),
+                 (11008, 4096)],
+}
 
 
-@pytest.mark.parametrize("m", [1, 3, 16])
+@pytest.mark.parametrize("shapes", sorted(GROUP_SHAPE_SETS))
+@pytest.mark.parametrize("m", [1, 3, 8, 16])
 @pytest.mark.parametrize("pdl", [False, True])
-def test_linear_grouped_matches_single_calls_and_oracle(qmm, orc, m, pdl):
+def test_linear_grouped_matches_single_calls_and_oracle(qmm, orc, m, pdl, shapes):
     """Every problem of a group gets the bits qmm_linear_q4_0 gives it alone,
     and the oracle's codes."""
     probs, refs = [], []
-    for j, (n, k) in enumerate(GROUP_SHAPES):
+    for j, (n, k) in enumerate(GROUP_SHAPE_SETS[shapes]):
         w, _ = synthetic.q4_0_case(6500 + j, n, k, 1)
         x = adversarial_x(6600 + j + m, m, k)
         wq, wd = orc.quantize_q4_0(w)
