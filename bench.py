@@ -99,6 +99,28 @@ def load_peaks():
             "source": "fallback"}
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the last ncu capture, as recorded
+    in profiles/traffic.txt (kernel, bytes, sha256 of the kernel's source
+    file, that file), or None when there is no record or the source changed
+    since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel:
+                src = os.path.join(ROOT, parts[3])
+                if not os.path.exists(src):
+                    return None
+                with open(src, "rb") as g:
+                    digest = hashlib.sha256(g.read()).hexdigest()
+                return int(parts[1]) if digest == parts[2] else None
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken during a timed region."""
 
@@ -335,7 +357,11 @@ def run_layer_set(q, args, dist, peaks):
     roofline = {"bound": "hbm", "kernel": "gemv_grouped_kernel<1,2,true>",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": peaks["source"], "traffic": None,
+                "peak_source": peaks["source"],
+                "traffic": recorded_traffic("gemv_grouped_kernel<1,2,1>"),
+                "traffic_source": "profiles/traffic.txt (ncu dram__bytes_read.sum + "
+                                  "dram__bytes_write.sum of one launch; null once the kernel's "
+                                  "source changed since that capture)",
                 "algorithmic_bytes_per_launch": step_bytes,
                 "avg_launch_us": round(ms * 1e3 / args.steps, 3),
                 "measured": "the timed step (one grouped quantizer launch + one grouped GEMV "
@@ -497,7 +523,7 @@ def _oracle_step(mats):
     for n, k, rows, wq, wd, x in mats:
         aq, ad = oracle.quantize_q8_0(x)
         oracle.gemm_q4_0_q8_0(wq, wd, aq, ad)
-        moved += quant_bytes(1, k) + gemv_bytes(1, rows, k)
+        moved += linear_bytes(1, rows, k)  # the GPU arm's accounting, on the sampled rows
     return moved
 
 
@@ -519,15 +545,16 @@ def cpu_baseline(budget_s: float, frac: float = 0.25):
 def run_reference(args, dist):
     if dist.rank != 0:
         return
-    # one full step calibrates the cost; each timed step then takes a row
-    # sample sized so warm-up + steps finish in about a minute
-    full = _oracle_layer_set(1.0)
+    # a 1% row sample calibrates the cost of a full step; each timed step then
+    # takes a row sample sized so warm-up + steps finish within the budget
+    probe_frac = 0.01
+    probe = _oracle_layer_set(probe_frac)
     t0 = time.perf_counter()
-    _oracle_step(full)
-    full_s = time.perf_counter() - t0
-    del full
-    frac = min(1.0, 60.0 / max(1, args.steps + args.warmup) / max(full_s, 1e-6))
-    frac = max(frac, 1e-3)
+    _oracle_step(probe)
+    full_s = (time.perf_counter() - t0) / probe_frac
+    del probe
+    frac = min(1.0, args.ref_budget / max(1, args.steps + args.warmup) / max(full_s, 1e-6))
+    frac = max(frac, 1e-4)
     mats = _oracle_layer_set(frac)
     for _ in range(args.warmup):
         _oracle_step(mats)
@@ -559,6 +586,8 @@ def main():
     ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
     ap.add_argument("--configs", choices=["all", "main"], default="all",
                     help="'main' measures only the layer-set headline")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds of oracle work for --impl reference (warm-up + steps)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
     ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab"], default=None,
