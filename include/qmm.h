@@ -194,8 +194,9 @@ qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count
  * (tcgen05.mma kind::f16 with f32 accumulators in TMEM): the int4 and int8
  * values are exact in fp16 and every partial sum is an integer below 2^24,
  * so each block sum is exact; each f32 output then accumulates
- * fma(sumi, dw*da, acc) over blocks in ascending order.  The workspace holds
- * an fp16 copy of the activations and the transposed activation scales.
+ * fma(sumi, dw*da, acc) over blocks in ascending order; the exact products
+ * dw*da come from the tensor core too.  The workspace holds an fp16 copy of
+ * the activations and one 16-byte activation-scale row per (block, token).
  *   wq 16-byte aligned; aq 16-byte aligned; wd, ad 2-byte aligned; y 4-byte;
  *   workspace 256-byte aligned, at least
  *   qmm_workspace_bytes(QMM_OP_GEMM_Q4_0_Q8_0, m, n, k, 0) bytes.

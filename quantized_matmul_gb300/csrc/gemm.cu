@@ -4,41 +4,47 @@
 // section "How the quantized dot product works"): for every output
 // y[t, n] = sum over blocks b of sumi[t, n, b] * (dw[n, b] * da[t, b]) where
 // sumi is the exact integer dot of the 32 nibbles (minus 8) with the 32 int8
-// activations of the block.
+// activations of the block, accumulated block by block in ascending order.
 //
 // How (GB300, sm_103a).  There is no int8 MMA on sm_103a, but every operand
 // value is a small integer that fp16 holds exactly (weights -8..7,
 // activations -127..127) and every partial sum of one block is an integer of
 // magnitude <= 32 * 8 * 127 < 2^24, so tcgen05.mma kind::f16 with an f32
-// accumulator produces each block sum exactly.  The scales differ per block,
-// so each block gets its own accumulator in TMEM and is drained and scaled
-// by CUDA cores while the tensor core already computes the next block.
+// accumulator produces each block sum exactly.  The scale product dw * da of
+// two fp16 values is exact in f32 too, so the tensor core computes it as
+// well: one more MMA per block whose A tile holds dw[n, b] in column 0 and
+// zeros elsewhere and whose B tile holds da[t, b] in column 0 writes the
+// matrix S[n, t] = dw * da, exactly, next to the block sums.  The CUDA cores
+// then do one fused multiply-add per output and block,
+// acc = fma(sumi, S, acc): the same operations, in the same order, as the
+// serial definition, so y is reproducible bit for bit.
 //
 // One CTA computes a tile of 128 weight rows (the MMA's M, TMEM lanes) by BN
-// tokens (the MMA's N, TMEM columns).  Roles (704 threads, 22 warps):
-//   warp 0      TMA producer: per stage of 2 blocks (64 k-elements) it loads
-//               the 128 x 32 B nibble tile, the BN x 64 fp16 activation tile
-//               (128-byte swizzle) and the 2 x BN f32 activation scales.
-//   warp 1      allocates TMEM; its lane 0 issues the MMAs (2 x K=16 per
-//               block into accumulator buffer b % NACC) and commits.
-//   warps 2-5   convert the nibbles of a stage to fp16 (value - 8) in the
-//               128-byte-swizzled K-major A tile the MMA reads, as far ahead
-//               of the MMA as the shared-memory stages allow (one converter
-//               warp per SM sub-partition, so the work is spread evenly).
-//   warps 6-21  drain: thread (warp % 4, lane) owns weight row n and a
-//               quarter of the BN columns; for every block it loads the
-//               accumulator from TMEM and applies acc = fma(sumi, dw * da,
-//               acc), blocks in ascending order -- the same order and
-//               operations as the serial definition, so the result is
-//               reproducible bit for bit.  (A TMEM lane quarter is readable
-//               only from the sub-partition with the same index, warp % 4.)
-// The roles meet only at mbarriers: converters run ahead of the MMA by up to
-// the number of stages, the MMA runs ahead of the drains by up to the number
-// of TMEM accumulator slots, so no role waits on another role's latency
-// chain.  The producer and MMA loops run on whole warps with lane 0
-// issuing.
+// tokens (the MMA's N, TMEM columns).  Roles:
+//   warp 0      TMA producer: per stage of two blocks (64 k-elements) the
+//               128 x 32 B nibble tile, the BN x 64 fp16 activation tile
+//               (128-byte swizzle) and the two BN x 16 B scale rows (da in
+//               the first fp16 of each row, written by the prepass).
+//   warp 1      allocates TMEM; its lane 0 issues, per block, the two K=16
+//               block-sum MMAs and the scale MMA into accumulator slot
+//               b % NACC (2 * BN columns: sums, then S) and commits.
+//   warps 2..   converters (up to four; the stage count is a multiple of
+//               their number C): converter c owns the ring slots c, c+C, ...
+//               and converts every stage that lands in them, in order, so C
+//               stages convert at once; it turns the nibbles into the
+//               128-byte-swizzled K-major fp16 A tile and writes the 128 rows
+//               x 16 B dw tile of each block.
+//   then        drains: thread (warp % 4, lane) owns weight row n (a TMEM
+//               lane quarter is readable only from the sub-partition with the
+//               same index) and BN / groups columns; per block it loads the
+//               sums and S from TMEM and applies the multiply-adds.
+// The roles meet only at mbarriers; each slot's S and sums are drained while
+// the tensor core fills the next slot.  The scale tiles use the no-swizzle
+// K-major layout: 16-byte rows (8 fp16, the value and seven zeros), 8-row
+// groups 128 bytes apart, and the second K core matrix of every group read
+// from one shared block of zeros through the descriptor's leading offset.
 // An activation prepass (same stream) writes the fp16 copy of the int8
-// activations and the transposed f32 activation scales into the workspace.
+// activations and the scale rows into the workspace.
 //
 // Every mbarrier wait is bounded.  On expiry a kernel raises a CTA-wide abort
 // flag, records QMM_ERR_TIMEOUT in a device error word, waits (bounded) for
@@ -55,33 +61,47 @@
 namespace qmm {
 namespace {
 
-constexpr int kBM = 128;               // weight rows per tile (MMA M)
-constexpr int kBK = 64;                // k-elements per pipeline stage (two blocks)
-constexpr int kConvWarps = 4;          // warps 2-5: one converter per sub-partition
-constexpr int kConvWarp0 = 2;
-constexpr int kEpiWarp0 = 6;           // warps 6-21 may drain
-// drain warps per TMEM lane quarter: enough for 32 columns each at most
-template <int BN>
-__host__ __device__ constexpr int drain_groups() { return BN <= 32 ? 1 : 2; }
-// producer, MMA and four converter warps, then the drain warps
-template <int BN>
-__host__ __device__ constexpr int threads_for() { return 32 * (kEpiWarp0 + 4 * drain_groups<BN>()); }
+constexpr int kBM = 128;       // weight rows per tile (MMA M)
+constexpr int kBK = 64;        // k-elements per pipeline stage (two blocks)
+constexpr int kConvWarp0 = 2;  // converters follow the producer and MMA warps
 constexpr int kSmemBudget = 200 * 1024;  // per SM
+constexpr int kZeroBytes = 2048;         // zeros behind every scale tile's second K half
 
-// bytes of one pipeline stage and the number of stages that fit the budget
+// drain warps per TMEM lane quarter, each taking BN / groups columns
 template <int BN>
-constexpr int stage_bytes() { return kBM * kBK * 2 + BN * kBK * 2 + kBM * (kBK / 2) + 2 * BN * 4; }
+__host__ __device__ constexpr int drain_groups() { return BN >= 64 ? BN / 32 : 1; }
 template <int BN>
-constexpr int ctas_per_sm() { return BN <= 32 ? 2 : 1; }
+__host__ __device__ constexpr int ctas_per_sm() { return BN <= 32 ? 2 : 1; }
+// bytes of one pipeline stage: A tile, B tile, nibbles, dw tile, da tile
 template <int BN>
-constexpr int stages_for() {
-    return (kSmemBudget / ctas_per_sm<BN>()) / stage_bytes<BN>() < 9
-               ? (kSmemBudget / ctas_per_sm<BN>()) / stage_bytes<BN>() : 9;
+constexpr int stage_bytes() {
+    return kBM * kBK * 2 + BN * kBK * 2 + kBM * (kBK / 2) + 2 * kBM * 16 + 2 * BN * 16;
 }
-// TMEM accumulator slots, one per stage in flight (each holds the stage's two
-// block accumulators, 2 * BN columns): as many as 512 columns hold, at most 8
 template <int BN>
-constexpr int nacc_for() { return 256 / BN < 8 ? 256 / BN : 8; }
+__host__ __device__ constexpr int stages_fit() {
+    return ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN>() < 8
+               ? ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN>()
+               : 8;
+}
+// Converter warps: up to four, and the stage count a multiple of them, so
+// converter c owns the ring slots s = c (mod converters) and handles every
+// use of them in order.  (A warp that took stages round robin could reach a
+// slot's barrier two phases early, which a parity wait cannot tell apart.)
+template <int BN>
+__host__ __device__ constexpr int conv_warps() { return stages_fit<BN>() < 4 ? stages_fit<BN>() : 4; }
+template <int BN>
+__host__ __device__ constexpr int stages_for() {
+    return stages_fit<BN>() / conv_warps<BN>() * conv_warps<BN>();
+}
+template <int BN>
+__host__ __device__ constexpr int epi_warp0() { return kConvWarp0 + conv_warps<BN>(); }
+template <int BN>
+__host__ __device__ constexpr int threads_for() { return 32 * (epi_warp0<BN>() + 4 * drain_groups<BN>()); }
+// TMEM accumulator slots, one per block in flight (2 * BN columns each)
+template <int BN>
+constexpr int nacc_for() {
+    return (512 / ctas_per_sm<BN>()) / (2 * BN) < 8 ? (512 / ctas_per_sm<BN>()) / (2 * BN) : 8;
+}
 constexpr uint32_t kErrTimeout = 1u;
 // A waiting warp asks to be suspended for up to this long per poll; it
 // resumes as soon as the phase completes, so a wait does not spin and take
@@ -128,10 +148,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking check of a phase (no suspend): a completed phase is seen
+// without the cost of entering the suspending wait.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: true when the phase completed; false after `limit` polls or
 // when another role raised the abort flag (the error word is then set).
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit,
                                              volatile int *abort_flag) {
+    if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag || it >= limit) {
@@ -346,6 +383,19 @@ __device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
     out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // elements 24..31
 }
 
+
+// Shared-memory descriptor for the scale tiles: K-major, no swizzle, 16-byte
+// rows, 8-row groups 128 bytes apart (stride offset), the second K core
+// matrix `lead` bytes after the first (the block of zeros).
+__device__ __forceinline__ uint64_t smem_desc_scale(uint32_t saddr, uint32_t lead) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lead >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= 1ull << 46;  // swizzle mode 0 (none) at bits 61-63
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // Shared memory plan (dynamic; the base is rounded up to 1024 bytes)
 
@@ -354,42 +404,49 @@ struct Smem {
     static constexpr int kStages = stages_for<BN>();
     static constexpr int kNacc = nacc_for<BN>();
     static constexpr int kEpiWarps = 4 * drain_groups<BN>();
-    static constexpr int kA = kBM * kBK * 2;        // fp16 weights, 16 KB
-    static constexpr int kB = BN * kBK * 2;         // fp16 activations
-    static constexpr int kNib = kBM * (kBK / 2);    // nibble bytes, 4 KB
-    static constexpr int kDa = 2 * BN * 4;          // f32 activation scales
+    static constexpr int kA = kBM * kBK * 2;   // fp16 weights, 16 KB
+    static constexpr int kB = BN * kBK * 2;    // fp16 activations
+    static constexpr int kNib = kBM * (kBK / 2);  // nibble bytes, 4 KB
+    static constexpr int kAs = 2 * kBM * 16;   // dw tiles of the two blocks
+    static constexpr int kBs = 2 * BN * 16;    // da tiles of the two blocks
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kA;
     static constexpr int kOffNib = kOffB + kStages * kB;
-    static constexpr int kOffDa = kOffNib + kStages * kNib;
-    static constexpr int kOffBar = kOffDa + kStages * kDa;
+    static constexpr int kOffAs = kOffNib + kStages * kNib;
+    static constexpr int kOffBs = kOffAs + kStages * kAs;
+    static constexpr int kOffZ = kOffBs + kStages * kBs;
+    static constexpr int kOffBar = kOffZ + kZeroBytes;
     static constexpr int kNumBars = 3 * kStages + 2 * kNacc + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte round-up
-    static constexpr uint32_t kTx = kNib + kB + kDa;
+    static constexpr uint32_t kTx = kNib + kB + kBs;
+    static_assert(kOffB % 1024 == 0 && kB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 };
 
 template <int BN, bool EMIT>
 __global__ void __launch_bounds__(threads_for<BN>(), ctas_per_sm<BN>())
 gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       const __grid_constant__ CUtensorMap tm_act,
-                      const __grid_constant__ CUtensorMap tm_da,
+                      const __grid_constant__ CUtensorMap tm_bs,
                       const unsigned short *__restrict__ wd, float *__restrict__ y,
-                      int32_t *__restrict__ sumi, int m, int n, int kb_total,
+                      int32_t *__restrict__ sumi, int m, int n, int kb_total, int m4,
                       uint32_t wait_limit, int withhold_loads) {
     using S = Smem<BN>;
     constexpr int kStages = S::kStages;
     constexpr int kNacc = S::kNacc;
     constexpr int kEpiWarps = S::kEpiWarps;
+    constexpr int kConvWarps = conv_warps<BN>();
+    constexpr int kEpiWarp0 = epi_warp0<BN>();
+    static_assert(kStages % kConvWarps == 0, "converter c owns the slots c (mod converters)");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *bar_load = bar;                  // TMA landed (tx) + producer arrive
-    uint64_t *bar_conv = bar + kStages;        // A tile converted (4 warps)
-    uint64_t *bar_empty = bar + 2 * kStages;   // drains done with the stage (implies its MMAs are)
-    uint64_t *bar_accf = bar + 3 * kStages;    // accumulator slot full (both blocks of a stage)
+    uint64_t *bar_conv = bar + kStages;        // A and dw tiles written (one converter)
+    uint64_t *bar_empty = bar + 2 * kStages;   // the stage's MMAs completed
+    uint64_t *bar_accf = bar + 3 * kStages;    // accumulator slot full (one block)
     uint64_t *bar_acce = bar_accf + kNacc;     // accumulator slot drained
     uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
@@ -402,11 +459,14 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     const int num_stages = (kb_total + 1) / 2;
     constexpr uint32_t kTmemCols = (uint32_t)(2 * kNacc * BN) < 32 ? 32 : (uint32_t)(2 * kNacc * BN);
 
+    // the block of zeros the scale tiles' second K halves read
+    for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(smem + S::kOffZ)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
-            mbar_init(&bar_conv[s], kConvWarps);
-            mbar_init(&bar_empty[s], kEpiWarps);
+            mbar_init(&bar_conv[s], 1);
+            mbar_init(&bar_empty[s], 1);
         }
         for (int b = 0; b < kNacc; ++b) {
             mbar_init(&bar_accf[b], 1);
@@ -417,8 +477,9 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         fence_mbar_init();
         tmap_prefetch(&tm_nib);
         tmap_prefetch(&tm_act);
-        tmap_prefetch(&tm_da);
+        tmap_prefetch(&tm_bs);
     }
+    fence_proxy_async_smem();  // the zeros are read by the tensor core
     if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -435,10 +496,13 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
             const uint32_t ph = (uint32_t)(it / kStages) & 1u;
             if (!wait_bounded_warp(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar_load[s], S::kTx);
+                const bool two = 2 * it + 1 < kb_total;
+                mbar_arrive_expect_tx(&bar_load[s], S::kTx - (two ? 0u : (uint32_t)(BN * 16)));
                 tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * (kBK / 2), n0);
                 tma_load_2d(smem + S::kOffB + s * S::kB, &tm_act, &bar_load[s], it * kBK, t0);
-                tma_load_2d(smem + S::kOffDa + s * S::kDa, &tm_da, &bar_load[s], t0, 2 * it);
+                uint8_t *bs = smem + S::kOffBs + s * S::kBs;
+                tma_load_2d(bs, &tm_bs, &bar_load[s], 0, (2 * it) * m4 + t0);
+                if (two) tma_load_2d(bs + BN * 16, &tm_bs, &bar_load[s], 0, (2 * it + 1) * m4 + t0);
             }
             __syncwarp();
             issued = it + 1;
@@ -451,37 +515,49 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        // The serial critical path at narrow tiles: lane 0 alone waits and
-        // issues, with the descriptors of stage s one constant step apart, one
-        // commit per stage (the drains free the stage's buffers only after
-        // that commit fired, so it also covers the shared-memory tiles).
+        // Lane 0 alone waits and issues.  Per block: two K=16 block-sum MMAs
+        // and the scale MMA into the block's slot, then one commit for the
+        // slot; per stage one more commit frees the stage's tiles.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kBM, BN);
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffA));
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffB));
+            const uint32_t zaddr = smem_u32(smem + S::kOffZ);
             int issued_any = 0;
-            for (int it = 0; it < num_stages; ++it) {
+            bool ok = true;
+            for (int it = 0; it < num_stages && ok; ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                const int slot = it % kNacc;
-                const uint32_t sph = (uint32_t)(it / kNacc) & 1u;
-                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag) ||
-                    !wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag))
-                    break;
+                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag)) break;
                 tc_fence_after();
                 // descriptor start address advances 32 bytes (2 in units of
                 // 16 bytes) per K=16 step inside the 128-byte swizzle row
                 const uint64_t a_desc = a_desc0 + (uint64_t)(s * (S::kA >> 4));
                 const uint64_t b_desc = b_desc0 + (uint64_t)(s * (S::kB >> 4));
-                const uint32_t d0 = tmem_base + (uint32_t)(slot * 2 * BN);
-                mma_f16(d0, a_desc + 0, b_desc + 0, idesc, 0u);
-                mma_f16(d0, a_desc + 2, b_desc + 2, idesc, 1u);
-                if (2 * it + 1 < kb_total) {
-                    mma_f16(d0 + BN, a_desc + 4, b_desc + 4, idesc, 0u);
-                    mma_f16(d0 + BN, a_desc + 6, b_desc + 6, idesc, 1u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int kbi = 2 * it + h;
+                    if (kbi >= kb_total) break;
+                    const int slot = kbi % kNacc;
+                    const uint32_t sph = (uint32_t)(kbi / kNacc) & 1u;
+                    // operands first, so the MMAs issue back to back after the wait
+                    const uint32_t d = tmem_base + (uint32_t)(slot * 2 * BN);
+                    const uint32_t as = smem_u32(smem + S::kOffAs + s * S::kAs + h * kBM * 16);
+                    const uint32_t bs = smem_u32(smem + S::kOffBs + s * S::kBs + h * BN * 16);
+                    const uint64_t as_desc = smem_desc_scale(as, zaddr - as);
+                    const uint64_t bs_desc = smem_desc_scale(bs, zaddr - bs);
+                    if (!wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_f16(d, a_desc + 4 * h, b_desc + 4 * h, idesc, 0u);
+                    mma_f16(d, a_desc + 4 * h + 2, b_desc + 4 * h + 2, idesc, 1u);
+                    if (!EMIT) mma_f16(d + BN, as_desc, bs_desc, idesc, 0u);
+                    mma_commit(&bar_accf[slot]);
+                    issued_any = 1;
                 }
-                mma_commit(&bar_accf[slot]);
-                issued_any = 1;
+                mma_commit(&bar_empty[s]);
             }
             // Wait until every MMA issued here has finished.
             if (issued_any) {
@@ -493,31 +569,50 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         __syncwarp();
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        // 128 rows x 2 blocks per stage; converter cw takes blocks
-        // cw * 64 + lane and cw * 64 + 32 + lane (contiguous 16-byte reads;
-        // the swizzled 16-byte stores of 8 consecutive lanes hit 8 different
-        // bank groups)
+        // Converter c owns the ring slots c (mod kConvWarps), i.e. the stages
+        // c, c + kConvWarps, ... in order: all 256 (row, block) units of a
+        // stage, eight per lane (unit u = 32 i + lane: row u / 2, block u % 2),
+        // so the conversions of kConvWarps stages overlap.  Contiguous
+        // 16-byte nibble reads; the swizzled 16-byte stores of 8 consecutive
+        // lanes hit 8 different bank groups.
         const int cw = warp - kConvWarp0;
-        for (int j = 0; j < num_stages; ++j) {
+        for (int j = cw; j < num_stages; j += kConvWarps) {
             const int s = j % kStages;
             const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+            // the stage's weight scales (global, L2) are requested before the
+            // wait so their latency overlaps it
+            unsigned short dwv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int u = 32 * i + lane;
+                const int row = n0 + (u >> 1), kbi = 2 * j + (u & 1);
+                dwv[i] = (!EMIT && row < n && kbi < kb_total) ? __ldg(wd + (int64_t)row * kb_total + kbi)
+                                                               : (unsigned short)0;
+            }
             if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
             const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
-            uint4 v[2];
+            uint8_t *as_tile = smem + S::kOffAs + s * S::kAs;
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
-                v[i] = *reinterpret_cast<const uint4 *>(nib + (cw * 64 + 32 * i + lane) * 16);
+            for (int half = 0; half < 2; ++half) {  // four units at a time
+                uint4 v[4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int unit = cw * 64 + 32 * i + lane;
-                const int row = unit >> 1, blk = unit & 1;
-                uint4 out[4];
-                unpack_block_f16(v[i], out);
+                for (int i = 0; i < 4; ++i)
+                    v[i] = *reinterpret_cast<const uint4 *>(nib + (32 * (4 * half + i) + lane) * 16);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((blk * 4 + c) ^ (row & 7)) * 16)) =
-                        out[c];
+                for (int i = 0; i < 4; ++i) {
+                    const int u = 32 * (4 * half + i) + lane;
+                    const int row = u >> 1, blk = u & 1;
+                    uint4 out[4];
+                    unpack_block_f16(v[i], out);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(a_tile + row * 128 +
+                                                   (((blk * 4 + c) ^ (row & 7)) * 16)) = out[c];
+                    if (!EMIT)
+                        *reinterpret_cast<uint4 *>(as_tile + blk * kBM * 16 + row * 16) =
+                            make_uint4((uint32_t)dwv[4 * half + i], 0u, 0u, 0u);
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -526,105 +621,54 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
         // ------------------------------------------------------------ drains
         constexpr int kCols = BN / drain_groups<BN>();  // columns per thread (16 or 32)
-        const int ew = warp - kEpiWarp0;         // 0..15
+        const int ew = warp - kEpiWarp0;
         const int q = warp & 3;                  // TMEM lane quarter = sub-partition
-        const int grp = ew >> 2;                 // column group 0..3
+        const int grp = ew >> 2;                 // column group
         const int row = n0 + 32 * q + lane;      // weight row owned by this thread
         const int c0 = grp * kCols;              // first column (token) in the tile
         const bool row_ok = row < n;
-        const unsigned short *wrow = wd + (int64_t)(row_ok ? row : 0) * kb_total;
-        // The raw fp16 weight scales of a stage are loaded one stage ahead and
-        // converted only where they are used: a warp issues in order, so a
-        // conversion right after the load would stall it for the whole
-        // global-load latency every stage.
-        auto load_scales = [&](int j, unsigned short (&raw)[2]) {
-            raw[0] = raw[1] = 0;
-            if (!EMIT && row_ok && j < num_stages) {
-                raw[0] = __ldg(wrow + 2 * j);
-                if (2 * j + 1 < kb_total) raw[1] = __ldg(wrow + 2 * j + 1);
-            }
-        };
-        uint64_t acc[kCols / 2 > 0 ? kCols / 2 : 1];  // f32 pairs
+        const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16);
+        uint64_t acc[kCols / 2];  // f32 pairs
 #pragma unroll
         for (int c = 0; c < kCols / 2; ++c) acc[c] = 0ull;
-        unsigned short dw_next[2];
-        load_scales(0, dw_next);
         bool ok = true;
-        for (int it = 0; it < num_stages && ok; ++it) {
-            const int s = it % kStages;
-            const unsigned short dw_cur[2] = {dw_next[0], dw_next[1]};
-            load_scales(it + 1, dw_next);
-            const int slot = it % kNacc;
-            // the accumulators of a stage are committed after its copies
-            // landed, so this wait also covers the activation-scale tile
-            if (!wait_bounded_warp(&bar_accf[slot], (uint32_t)(it / kNacc) & 1u, wait_limit,
+        for (int kbi = 0; kbi < kb_total; ++kbi) {
+            const int slot = kbi % kNacc;
+            if (!wait_bounded_warp(&bar_accf[slot], (uint32_t)(kbi / kNacc) & 1u, wait_limit,
                                    abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float *da_tile = reinterpret_cast<const float *>(smem + S::kOffDa + s * S::kDa);
-            // BN == 16: both blocks' 16 columns are adjacent in the slot, so one
-            // 32-column TMEM load fetches the whole stage; otherwise each block
-            // is loaded (32 columns) right before it is consumed.
-            uint32_t both[BN == 16 ? 32 : 1];
-            if constexpr (BN == 16) {
-                tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * 2 * BN), both);
+            const uint32_t col = lane_base + (uint32_t)(slot * 2 * BN + c0);
+#pragma unroll
+            for (int g = 0; g < kCols / 16; ++g) {
+                uint32_t sv[16], scv[16];
+                tmem_ld16(col + 16 * g, sv);
+                if constexpr (!EMIT) tmem_ld16(col + BN + 16 * g, scv);
                 tmem_wait_ld();
-            }
+                if constexpr (EMIT) {
+                    if (row_ok) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int kbi = 2 * it + h;
-                if (kbi >= kb_total) break;
-                // consume the block in chunks of at most 32 columns: one TMEM
-                // load, then its multiply-adds (keeps the live registers low)
-                constexpr int kChunk = BN == 16 ? 16 : 32;
-#pragma unroll
-                for (int g = 0; g < kCols / kChunk; ++g) {
-                    uint32_t vblk[BN == 16 ? 1 : 32];
-                    if constexpr (BN != 16) {
-                        tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) +
-                                      (uint32_t)(slot * 2 * BN + h * BN + c0 + 32 * g),
-                                  vblk);
-                        tmem_wait_ld();
-                    }
-                    const uint32_t *v = BN == 16 ? both + 16 * h : vblk;
-                    const int cg = c0 + kChunk * g;  // first column of the chunk
-                    if constexpr (EMIT) {
-                        if (row_ok) {
-#pragma unroll
-                            for (int c = 0; c < kChunk; ++c) {
-                                const int t = t0 + cg + c;
-                                if (t < m)
-                                    sumi[((int64_t)t * n + row) * kb_total + kbi] =
-                                        __float2int_rn(__uint_as_float(v[c]));
-                            }
-                        }
-                    } else {
-                        // acc += sumi * (dw * da), two columns per instruction;
-                        // dw * da is exact in f32 (two 11-bit significands)
-                        const float dw = h2f(dw_cur[h]);
-                        const uint64_t dw2 = pack_f32x2(dw, dw);
-                        const float4 *dap = reinterpret_cast<const float4 *>(da_tile + h * BN + cg);
-                        uint64_t *accg = acc + (kChunk / 2) * g;
-#pragma unroll
-                        for (int c4 = 0; c4 < kChunk / 4; ++c4) {
-                            const float4 d = dap[c4];
-                            const uint64_t s01 = mul_f32x2(dw2, pack_f32x2(d.x, d.y));
-                            const uint64_t s23 = mul_f32x2(dw2, pack_f32x2(d.z, d.w));
-                            accg[2 * c4] = fma_f32x2(pack_u32x2(v[4 * c4], v[4 * c4 + 1]), s01, accg[2 * c4]);
-                            accg[2 * c4 + 1] =
-                                fma_f32x2(pack_u32x2(v[4 * c4 + 2], v[4 * c4 + 3]), s23, accg[2 * c4 + 1]);
+                        for (int c = 0; c < 16; ++c) {
+                            const int t = t0 + c0 + 16 * g + c;
+                            if (t < m)
+                                sumi[((int64_t)t * n + row) * kb_total + kbi] =
+                                    __float2int_rn(__uint_as_float(sv[c]));
                         }
                     }
+                } else {
+                    // acc += sumi * S, two columns per instruction
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        acc[8 * g + c] = fma_f32x2(pack_u32x2(sv[2 * c], sv[2 * c + 1]),
+                                                   pack_u32x2(scv[2 * c], scv[2 * c + 1]),
+                                                   acc[8 * g + c]);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar_acce[slot]);
-                mbar_arrive(&bar_empty[s]);
-            }
+            if (lane == 0) mbar_arrive(&bar_acce[slot]);
         }
         if (!EMIT && ok && !*abort_flag && row_ok) {
 #pragma unroll
@@ -646,9 +690,11 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     }
 }
 
-// Activation prepass: int8 -> fp16 (exact) and fp16 scales -> transposed f32.
+// Activation prepass: int8 -> fp16 (exact), and per block b and token t one
+// 16-byte scale row {da[t, b], 0 x 7} (fp16) at row b * m4 + t (zero rows for
+// t >= m, and all zeros when no scales are given: the block-sum variant).
 __global__ void gemm_prep_kernel(const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
-                                 __half *__restrict__ a16, float *__restrict__ daT, int64_t m,
+                                 __half *__restrict__ a16, uint4 *__restrict__ bs, int64_t m,
                                  int64_t k, int64_t m4) {
     const int64_t kb = k / kQK;
     const int64_t n16 = m * k / 16;  // 16-element groups
@@ -671,10 +717,11 @@ __global__ void gemm_prep_kernel(const int8_t *__restrict__ aq, const unsigned s
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
-    const int64_t nda = kb * m4;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < nda; g += stride) {
+    const int64_t nrows = kb * m4;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < nrows; g += stride) {
         const int64_t b = g / m4, t = g - b * m4;
-        daT[g] = (t < m && ad != nullptr) ? h2f(ad[t * kb + b]) : 0.0f;  // no scales: block-sum variant
+        const uint32_t d = (t < m && ad != nullptr) ? (uint32_t)ad[t * kb + b] : 0u;
+        bs[g] = make_uint4(d, 0u, 0u, 0u);
     }
 }
 
@@ -717,7 +764,7 @@ int choose_bn(int64_t m) {
 }
 
 struct WsPlan {
-    size_t a16_off, a16_bytes, da_off, da_bytes, total;
+    size_t a16_off, a16_bytes, bs_off, bs_bytes, total;
     int64_t m4;
 };
 
@@ -726,9 +773,9 @@ WsPlan plan_ws(int64_t m, int64_t k) {
     p.m4 = (m + 3) / 4 * 4;
     p.a16_off = 0;
     p.a16_bytes = (size_t)m * (size_t)k * 2;
-    p.da_off = (p.a16_bytes + 255) / 256 * 256;
-    p.da_bytes = (size_t)(k / kQK) * (size_t)p.m4 * 4;
-    p.total = p.da_off + (p.da_bytes + 255) / 256 * 256;
+    p.bs_off = (p.a16_bytes + 255) / 256 * 256;
+    p.bs_bytes = (size_t)(k / kQK) * (size_t)p.m4 * 16;
+    p.total = p.bs_off + (p.bs_bytes + 255) / 256 * 256;
     return p;
 }
 
@@ -736,9 +783,9 @@ uint32_t g_wait_limit = kDefaultWaitLimit;
 int g_withhold_loads = 0;
 
 template <int BN>
-cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &da,
+cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &bs,
                         const uint16_t *wd, float *y, int32_t *sumi, int64_t m, int64_t n,
-                        int64_t k, cudaStream_t s) {
+                        int64_t k, int64_t m4, cudaStream_t s) {
     using S = Smem<BN>;
     const int kb = (int)(k / kQK);
     dim3 grid((unsigned)((m + BN - 1) / BN), (unsigned)((n + kBM - 1) / kBM));
@@ -746,13 +793,13 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
     if (sumi) {
         auto kern = gemm_q4_0_q8_0_kernel<BN, true>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
-                                               g_wait_limit, g_withhold_loads);
+        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
+                                                        (int)m4, g_wait_limit, g_withhold_loads);
     } else {
         auto kern = gemm_q4_0_q8_0_kernel<BN, false>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, da, wdp, y, sumi, (int)m, (int)n, kb,
-                                               g_wait_limit, g_withhold_loads);
+        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
+                                                        (int)m4, g_wait_limit, g_withhold_loads);
     }
     return cudaPeekAtLastError();
 }
@@ -786,18 +833,18 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
     const WsPlan p = plan_ws(m, k);
     auto *ws = static_cast<uint8_t *>(workspace);
     __half *a16 = reinterpret_cast<__half *>(ws + p.a16_off);
-    float *daT = reinterpret_cast<float *>(ws + p.da_off);
+    uint4 *bs = reinterpret_cast<uint4 *>(ws + p.bs_off);
     {
         const int threads = 256;
-        const int64_t work = std::max<int64_t>(m * k / 16, (k / kQK) * p.m4);
+        const int64_t work = std::max<int64_t>(m * k / 16, (k / kQK) * p.m4);  // groups, scale rows
         const int64_t blocks = std::min<int64_t>((work + threads - 1) / threads, 152 * 8);
         gemm_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(
-            aq, reinterpret_cast<const unsigned short *>(ad), a16, daT, m, k, p.m4);
+            aq, reinterpret_cast<const unsigned short *>(ad), a16, bs, m, k, p.m4);
         cudaError_t e = cudaPeekAtLastError();
         if (e != cudaSuccess) return e;
     }
     const int bn = choose_bn(m);
-    CUtensorMap tm_nib, tm_act, tm_da;
+    CUtensorMap tm_nib, tm_act, tm_bs;
     // nibbles: u8 [n rows, k/2 bytes], box 32 bytes x 128 rows
     if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)(k / 2), (uint64_t)n,
                      (uint64_t)(k / 2), kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -806,15 +853,15 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
     if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, (uint64_t)k, (uint64_t)m,
                      (uint64_t)k * 2, kBK, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    // activation scales: f32 [k/32 rows, m4], box BN x 2
-    if (!make_map_2d(&tm_da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, daT, (uint64_t)m, (uint64_t)(k / kQK),
-                     (uint64_t)p.m4 * 4, (uint32_t)bn, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+    // activation scale rows: fp16 [k/32 * m4 rows, 8], box 8 x BN
+    if (!make_map_2d(&tm_bs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bs, 8, (uint64_t)(k / kQK) * p.m4, 16,
+                     8, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     switch (bn) {
-        case 16: return launch_tile<16>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
-        case 32: return launch_tile<32>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
-        case 64: return launch_tile<64>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
-        default: return launch_tile<128>(tm_nib, tm_act, tm_da, wd, y, sumi, m, n, k, s);
+        case 16: return launch_tile<16>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 32: return launch_tile<32>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 64: return launch_tile<64>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        default: return launch_tile<128>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
     }
 }
 

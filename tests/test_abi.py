@@ -62,11 +62,16 @@ def test_workspace_queries(lib):
     assert lib.qmm_workspace_bytes(1, 1, 4096, 4096, 1) == 0
     # explicit split of 4 at m=2, n=100: 4 * 2 * 100 floats
     assert lib.qmm_workspace_bytes(1, 2, 100, 4096, 4) == 4 * 2 * 100 * 4
-    # GEMM: fp16 activations + transposed f32 scales, 256-byte rounded
+    # GEMM: fp16 activations + one 16-byte scale row per (block, token),
+    # tokens rounded up to 4, each part 256-byte rounded
     m, k = 512, 4096
     a16 = m * k * 2
-    da = (k // 32) * m * 4
-    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == a16 + da
+    rows = (k // 32) * m * 16
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == a16 + rows
+    m = 3
+    a16 = (m * k * 2 + 255) // 256 * 256
+    rows = ((k // 32) * 4 * 16 + 255) // 256 * 256
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == a16 + rows
     bad = ctypes.c_size_t(-1).value
     assert lib.qmm_workspace_bytes(9, 1, 1, 32, 0) == bad        # unknown op
     assert lib.qmm_workspace_bytes(1, 1, 1, 33, 0) == bad        # k not a block multiple
