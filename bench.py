@@ -472,7 +472,12 @@ def run_prefill(q, steps, warmup, dist, peaks):
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): the block sums run "
                          "on tcgen05 kind::f16 because sm_103a has no int8 MMA",
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "traffic": recorded_traffic("gemm_q4_0_q8_0_kernel<128,0>"),
+            "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
+                            "(profiles/traffic.txt); algorithmic: 33.0 MB weights + 2.1 MB "
+                            "activations + 29.4 MB y (y is written back from L2 after the "
+                            "kernel)"}
 
 
 def run_vocab(q, steps, warmup, dist, peaks):
