@@ -25,10 +25,11 @@
 //               128 x 32 B nibble tile, the BN x 64 fp16 activation tile
 //               (128-byte swizzle) and the two BN x 16 B scale rows (da in
 //               the first fp16 of each row, written by the prepass).
-//   warp 1      allocates TMEM; its lane 0 issues, per block, the two K=16
+//   warps 1, 2  warp 1 allocates TMEM; lane 0 of warp 1 (even blocks) and of
+//               warp 2 (odd blocks) issues, per block, the two K=16
 //               block-sum MMAs and the scale MMA into accumulator slot
 //               b % NACC (2 * BN columns: sums, then S) and commits.
-//   warps 2..   converters (up to four; the stage count is a multiple of
+//   warps 3..   converters (up to four; the stage count is a multiple of
 //               their number C): converter c owns the ring slots c, c+C, ...
 //               and converts every stage that lands in them, in order, so C
 //               stages convert at once; it turns the nibbles into the
@@ -63,7 +64,8 @@ namespace {
 
 constexpr int kBM = 128;       // weight rows per tile (MMA M)
 constexpr int kBK = 64;        // k-elements per pipeline stage (two blocks)
-constexpr int kConvWarp0 = 2;  // converters follow the producer and MMA warps
+constexpr int kMmaWarps = 2;   // warps 1 and 2 issue the MMAs of even and odd blocks
+constexpr int kConvWarp0 = 1 + kMmaWarps;  // converters follow the producer and MMA warps
 constexpr int kSmemBudget = 200 * 1024;  // per SM
 constexpr int kZeroBytes = 2048;         // zeros behind every scale tile's second K half
 
@@ -416,7 +418,7 @@ struct Smem {
     static constexpr int kOffBs = kOffAs + kStages * kAs;
     static constexpr int kOffZ = kOffBs + kStages * kBs;
     static constexpr int kOffBar = kOffZ + kZeroBytes;
-    static constexpr int kNumBars = 3 * kStages + 2 * kNacc + 1;
+    static constexpr int kNumBars = 3 * kStages + 2 * kNacc + kMmaWarps;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for the 1024-byte round-up
@@ -439,16 +441,17 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
     constexpr int kConvWarps = conv_warps<BN>();
     constexpr int kEpiWarp0 = epi_warp0<BN>();
     static_assert(kStages % kConvWarps == 0, "converter c owns the slots c (mod converters)");
+    static_assert(kNacc % kMmaWarps == 0, "block b's slot b % NACC belongs to issuer b % 2");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + S::kOffBar);
     uint64_t *bar_load = bar;                  // TMA landed (tx) + producer arrive
     uint64_t *bar_conv = bar + kStages;        // A and dw tiles written (one converter)
-    uint64_t *bar_empty = bar + 2 * kStages;   // the stage's MMAs completed
+    uint64_t *bar_empty = bar + 2 * kStages;   // the stage's MMAs completed (both issuers)
     uint64_t *bar_accf = bar + 3 * kStages;    // accumulator slot full (one block)
     uint64_t *bar_acce = bar_accf + kNacc;     // accumulator slot drained
-    uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion
+    uint64_t *bar_drain = bar_acce + kNacc;    // final MMA completion, one per issuer
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kOffMisc + 4);
 
@@ -466,13 +469,13 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
             mbar_init(&bar_conv[s], 1);
-            mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_empty[s], kMmaWarps);
         }
         for (int b = 0; b < kNacc; ++b) {
             mbar_init(&bar_accf[b], 1);
             mbar_init(&bar_acce[b], kEpiWarps);
         }
-        mbar_init(bar_drain, 1);
+        for (int w = 0; w < kMmaWarps; ++w) mbar_init(&bar_drain[w], 1);
         *abort_flag = 0;
         fence_mbar_init();
         tmap_prefetch(&tm_nib);
@@ -513,57 +516,53 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
             wait_bounded_warp(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
                               &no_abort);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Lane 0 alone waits and issues.  Per block: two K=16 block-sum MMAs
-        // and the scale MMA into the block's slot, then one commit for the
-        // slot; per stage one more commit frees the stage's tiles.
+    } else if (warp >= 1 && warp < 1 + kMmaWarps) {
+        // ------------------------------------------------------------ MMA issuers
+        // Lane 0 of warp 1 issues the even blocks, lane 0 of warp 2 the odd
+        // ones: one thread's tcgen05 instructions issue one after another, so
+        // two issuers keep the tensor core fed.  NACC is even, so block b's
+        // slot b % NACC always belongs to the same issuer.  Per block: two
+        // K=16 block-sum MMAs and the scale MMA, then a commit for the slot;
+        // per stage each issuer commits to the stage's "empty" barrier.
+        const int h = warp - 1;  // block parity
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kBM, BN);
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffA));
             const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + S::kOffB));
             const uint32_t zaddr = smem_u32(smem + S::kOffZ);
             int issued_any = 0;
-            bool ok = true;
-            for (int it = 0; it < num_stages && ok; ++it) {
+            for (int it = 0; it < num_stages; ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                const int kbi = 2 * it + h;
+                const int slot = kbi % kNacc;
+                const uint32_t sph = (uint32_t)(kbi / kNacc) & 1u;
+                // operands first, so the MMAs issue back to back after the waits
+                const uint64_t a_desc = a_desc0 + (uint64_t)(s * (S::kA >> 4)) + 4 * h;
+                const uint64_t b_desc = b_desc0 + (uint64_t)(s * (S::kB >> 4)) + 4 * h;
+                const uint32_t d = tmem_base + (uint32_t)(slot * 2 * BN);
+                const uint32_t as = smem_u32(smem + S::kOffAs + s * S::kAs + h * kBM * 16);
+                const uint32_t bs = smem_u32(smem + S::kOffBs + s * S::kBs + h * BN * 16);
+                const uint64_t as_desc = smem_desc_scale(as, zaddr - as);
+                const uint64_t bs_desc = smem_desc_scale(bs, zaddr - bs);
                 if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag)) break;
-                tc_fence_after();
-                // descriptor start address advances 32 bytes (2 in units of
-                // 16 bytes) per K=16 step inside the 128-byte swizzle row
-                const uint64_t a_desc = a_desc0 + (uint64_t)(s * (S::kA >> 4));
-                const uint64_t b_desc = b_desc0 + (uint64_t)(s * (S::kB >> 4));
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int kbi = 2 * it + h;
-                    if (kbi >= kb_total) break;
-                    const int slot = kbi % kNacc;
-                    const uint32_t sph = (uint32_t)(kbi / kNacc) & 1u;
-                    // operands first, so the MMAs issue back to back after the wait
-                    const uint32_t d = tmem_base + (uint32_t)(slot * 2 * BN);
-                    const uint32_t as = smem_u32(smem + S::kOffAs + s * S::kAs + h * kBM * 16);
-                    const uint32_t bs = smem_u32(smem + S::kOffBs + s * S::kBs + h * BN * 16);
-                    const uint64_t as_desc = smem_desc_scale(as, zaddr - as);
-                    const uint64_t bs_desc = smem_desc_scale(bs, zaddr - bs);
-                    if (!wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                if (kbi < kb_total) {
+                    if (!wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag)) break;
                     tc_fence_after();
-                    mma_f16(d, a_desc + 4 * h, b_desc + 4 * h, idesc, 0u);
-                    mma_f16(d, a_desc + 4 * h + 2, b_desc + 4 * h + 2, idesc, 1u);
+                    mma_f16(d, a_desc, b_desc, idesc, 0u);
+                    mma_f16(d, a_desc + 2, b_desc + 2, idesc, 1u);
                     if (!EMIT) mma_f16(d + BN, as_desc, bs_desc, idesc, 0u);
                     mma_commit(&bar_accf[slot]);
                     issued_any = 1;
                 }
+                // the stage's tiles are free once both issuers' MMAs completed
                 mma_commit(&bar_empty[s]);
             }
             // Wait until every MMA issued here has finished.
             if (issued_any) {
-                mma_commit(bar_drain);
+                mma_commit(&bar_drain[h]);
                 volatile int no_abort = 0;
-                wait_bounded(bar_drain, 0, kDrainLimit, &no_abort);
+                wait_bounded(&bar_drain[h], 0, kDrainLimit, &no_abort);
             }
         }
         __syncwarp();
