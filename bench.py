@@ -449,6 +449,33 @@ def run_bitnet(q, steps, warmup, dist, peaks):
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
 
 
+def run_bitnet_prefill(q, steps, warmup, dist, peaks):
+    import torch
+    from quantized_matmul_gb300 import synthetic
+    m, n, k = 2048, 6912, 2560
+    t, x, absmean = synthetic.bitnet_case(3, n, k, m)
+    tw = q.pack_ternary(_up(t))
+    rot = copies_for(n * k // 4 + m * k)
+    tws = [tw] + [tw.clone() for _ in range(rot - 1)]
+    aq, s, _ = q.quantize_act_bitnet(_up(x))
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    ws = torch.empty((q.workspace_bytes(q.OP_BITNET_GEMM, m, n, k),), dtype=torch.uint8,
+                     device="cuda")
+
+    def step(i):
+        q.bitnet_gemm(tws[i % rot], absmean, aq, s, y=y, workspace=ws)
+
+    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": "BitNet ternary prefill m=2048 K=2560 N=6912 (seed 3), tensor cores",
+            "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
+            "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
+            "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): codes - 1 and "
+                         "int8 activations run exactly on tcgen05 kind::f16",
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+
+
 def run_prefill(q, steps, warmup, dist, peaks):
     import torch
     m, n, k = 512, 14336, 4096
@@ -595,7 +622,8 @@ def main():
                     help="seconds of oracle work for --impl reference (warm-up + steps)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
-    ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab"], default=None,
+    ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill"],
+                    default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
     args = ap.parse_args()
@@ -615,7 +643,9 @@ def main():
             run = {"gemv": lambda: run_single_gemv(q, args.steps, args.warmup, dist, peaks),
                    "bitnet": lambda: run_bitnet(q, args.steps, args.warmup, dist, peaks),
                    "prefill": lambda: run_prefill(q, args.steps, args.warmup, dist, peaks),
-                   "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks)}
+                   "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks),
+                   "bitnet_prefill": lambda: run_bitnet_prefill(q, args.steps, args.warmup, dist,
+                                                                peaks)}
             res = run[args.only]()
             if dist.rank == 0:
                 print(json.dumps({"only": args.only, "result": res}), flush=True)
@@ -627,6 +657,8 @@ def main():
             configs["gemv_4096x4096"] = run_single_gemv(q, short * 5, args.warmup, dist, peaks)
             configs["bitnet_2560x6912"] = run_bitnet(q, short * 5, args.warmup, dist, peaks)
             configs["prefill_512x14336x4096"] = run_prefill(q, max(50, short // 20), 10, dist, peaks)
+            configs["bitnet_prefill_2048x6912x2560"] = run_bitnet_prefill(q, max(50, short // 20),
+                                                                          10, dist, peaks)
             configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks)
         cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
         if dist.rank == 0:

@@ -65,7 +65,8 @@ typedef enum qmm_status {
 /* Workspace-taking operations, for qmm_workspace_bytes(). */
 enum {
     QMM_OP_GEMV_Q4_0_Q8_0 = 1,
-    QMM_OP_GEMM_Q4_0_Q8_0 = 2
+    QMM_OP_GEMM_Q4_0_Q8_0 = 2,
+    QMM_OP_BITNET_GEMM = 3
 };
 
 /* Largest m accepted by the GEMV entry points (decode and small batches). */
@@ -233,6 +234,22 @@ qmm_status qmm_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t *w,
 qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean,
                            const int8_t *aq, const float *act_scale, const int32_t *act_sum,
                            float *y, int64_t m, int64_t n, int64_t k, void *stream);
+
+/* BitNet ternary matrix product for prefill (any m >= 1), on the tensor
+ * cores.  Same result as qmm_bitnet_gemv, bit for bit:
+ *   dot[i, r] = sum_j (code[r, j] - 1) * aq[i, j]    (exact; equal to the
+ *               identity sum(code * q) - sum(q), so no act_sum is needed)
+ *   y[i, r]   = act_scale[i] == 0 ? 0 : ((float)dot * weight_absmean) / act_scale[i]
+ * Every operand is exact in fp16 and |dot| < 2^24, so the tensor core's f32
+ * accumulation over all of k is exact.
+ *   w uint32 [n, k/16] 16-byte aligned; aq int8 [m, k] 16-byte aligned;
+ *   act_scale f32 [m]; y f32 [m, n]; k % 64 == 0 and k <= 131072.
+ *   workspace 256-byte aligned, at least
+ *   qmm_workspace_bytes(QMM_OP_BITNET_GEMM, m, n, k, 0) bytes (an fp16 copy
+ *   of the activations).  Not reentrant on one workspace. */
+qmm_status qmm_bitnet_gemm(const uint32_t *w, float weight_absmean, const int8_t *aq,
+                           const float *act_scale, float *y, int64_t m, int64_t n, int64_t k,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* Workspace size in bytes for `op` (QMM_OP_*) at this shape; 0 when none is

@@ -26,6 +26,7 @@ QK = 32
 GEMV_MAX_M = 16
 OP_GEMV = 1
 OP_GEMM = 2
+OP_BITNET_GEMM = 3
 
 STATUS_NAMES = {0: "ok", 1: "null pointer", 2: "invalid shape", 3: "misaligned pointer",
                 4: "workspace missing or too small", 5: "unsupported device", 6: "CUDA error",
@@ -64,6 +65,7 @@ def load() -> ctypes.CDLL:
             "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
             "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
             "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
+            "qmm_bitnet_gemm": (I, [P, F, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_workspace_bytes": (SZ, [I, I64, I64, I64, I]),
             "qmm_gemv_auto_split": (I, [I64, I64, I64]),
             "qmm_check_device_error": (I, [P]),
@@ -348,6 +350,24 @@ def bitnet_gemv(tw, weight_absmean: float, aq, act_scale, act_sum, y=None):
                                 act_scale.data_ptr(), act_sum.data_ptr(),
                                 _dev(y, torch.float32, "y", (m, n)), m, n, k, _stream())
     _check(st, "qmm_bitnet_gemv")
+    return y
+
+
+def bitnet_gemm(tw, weight_absmean: float, aq, act_scale, y=None, workspace=None):
+    """BitNet prefill on the tensor cores (any m, k % 64 == 0): y f32 [m, n],
+    bit for bit what bitnet_gemv gives."""
+    torch = _torch()
+    n = tw.shape[0]
+    m, k = aq.shape
+    _dev(tw, torch.int32, "tw", (n, k // 16))
+    _dev(aq, torch.int8, "aq", (m, k))
+    _dev(act_scale, torch.float32, "act_scale", (m,))
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_BITNET_GEMM, m, n, k), aq)
+    st = load().qmm_bitnet_gemm(tw.data_ptr(), float(weight_absmean), aq.data_ptr(),
+                                act_scale.data_ptr(), _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
+    _check(st, "qmm_bitnet_gemm")
     return y
 
 

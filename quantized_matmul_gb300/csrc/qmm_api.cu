@@ -235,7 +235,28 @@ qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean, const int8_t
                                                  nullptr, m, n, k, as_stream(stream)));
 }
 
+qmm_status qmm_bitnet_gemm(const uint32_t *w, float weight_absmean, const int8_t *aq,
+                           const float *act_scale, float *y, int64_t m, int64_t n, int64_t k,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    if (!w || !aq || !act_scale || !y) return QMM_ERR_NULL;
+    if (m <= 0 || n <= 0 || k <= 0 || k % 64 != 0 || k > (int64_t(1) << 17)) return QMM_ERR_SHAPE;
+    if (m >= (int64_t(1) << 31) || n >= (int64_t(1) << 31) || m * k > kMaxElems ||
+        n * k > kMaxElems || m * n > kMaxElems)
+        return QMM_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(aq, 16) || !aligned(act_scale, 4) || !aligned(y, 4))
+        return QMM_ERR_ALIGN;
+    const size_t need = qmm::bitnet_gemm_workspace_bytes(m, k);
+    if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_bitnet_gemm(w, weight_absmean, aq, act_scale, y, m, n, k,
+                                                 workspace, as_stream(stream)));
+}
+
 size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k) {
+    if (op == QMM_OP_BITNET_GEMM)
+        return (m <= 0 || n <= 0 || k <= 0 || k % 64 != 0) ? SIZE_MAX
+                                                           : qmm::bitnet_gemm_workspace_bytes(m, k);
     if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return SIZE_MAX;
     switch (op) {
         case QMM_OP_GEMV_Q4_0_Q8_0: {
@@ -257,11 +278,13 @@ int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k) {
 }
 
 qmm_status qmm_check_device_error(void *stream) {
-    unsigned int word = 0, word2 = 0;
+    unsigned int word = 0, word2 = 0, word3 = 0;
     if (qmm::gemm_read_and_clear_error(&word, as_stream(stream)) != cudaSuccess) return QMM_ERR_CUDA;
     if (qmm::stream_read_and_clear_error(&word2, as_stream(stream)) != cudaSuccess)
         return QMM_ERR_CUDA;
-    return (word | word2) ? QMM_ERR_TIMEOUT : QMM_OK;
+    if (qmm::bitnet_gemm_read_and_clear_error(&word3, as_stream(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return (word | word2 | word3) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 const char *qmm_status_string(qmm_status status) {
@@ -320,6 +343,7 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
 void qmm_debug_set_wait_limit(uint32_t iterations) {
     qmm::gemm_set_wait_limit(iterations);
     qmm::stream_set_wait_limit(iterations);
+    qmm::bitnet_gemm_set_wait_limit(iterations);
 }
 
 void qmm_debug_withhold_gemm_loads(int enable) { qmm::gemm_set_withhold_loads(enable); }

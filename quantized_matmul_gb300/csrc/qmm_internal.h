@@ -106,6 +106,15 @@ cudaError_t stream_read_and_clear_error(unsigned int *word, cudaStream_t s);
 void stream_set_wait_limit(uint32_t iterations);
 void stream_set_withhold_loads(int enable);
 
+// bitnet_gemm.cu: BitNet ternary product on the tensor cores (any m, k % 64
+// == 0, k <= 2^17); workspace: fp16 copy of the activations.
+size_t bitnet_gemm_workspace_bytes(int64_t m, int64_t k);
+cudaError_t launch_bitnet_gemm(const uint32_t *w, float absmean, const int8_t *aq,
+                               const float *act_scale, float *y, int64_t m, int64_t n, int64_t k,
+                               void *workspace, cudaStream_t s);
+void bitnet_gemm_set_wait_limit(uint32_t iterations);
+cudaError_t bitnet_gemm_read_and_clear_error(unsigned int *word, cudaStream_t s);
+
 // gemm.cu
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 // sumi != nullptr selects the block-sum emitting variant.

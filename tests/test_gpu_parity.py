@@ -189,6 +189,48 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
 
 
 # ---------------------------------------------------------------------------
+# BitNet prefill on the tensor cores
+
+BITNET_GEMM_SHAPES = [(1, 1, 64), (17, 130, 256), (100, 300, 2560), (256, 128, 512),
+                      (300, 257, 1024), (600, 1000, 128)]
+
+
+def _bitnet_operands(orc, seed, m, n, k):
+    t, x, absmean = synthetic.bitnet_case(seed, n, k, m)
+    x = x.copy()
+    if m > 1:
+        x[1] = 0.0  # zero row: scale 0, y 0
+    tw = orc.pack_ternary(t)
+    aq, scale, asum = orc.quantize_act_bitnet(x)
+    return tw, absmean, aq, scale, asum
+
+
+@pytest.mark.parametrize("m,n,k", BITNET_GEMM_SHAPES)
+def test_bitnet_gemm_bit_exact(qmm, orc, m, n, k):
+    """The tensor-core product gives the oracle's y bit for bit (and the
+    GEMV's, where m allows it)."""
+    tw, absmean, aq, scale, asum = _bitnet_operands(orc, 8000 + m + n, m, n, k)
+    y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), absmean, to_dev(aq), to_dev(scale)))
+    ref = orc.bitnet_gemv(tw, absmean, aq, scale, asum)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+    if m <= 16:
+        y2 = to_np(qmm.bitnet_gemv(to_dev(tw.view(np.int32)), absmean, to_dev(aq), to_dev(scale),
+                                   to_dev(asum)))
+        assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+def test_bitnet_gemm_prefill_size_sampled_rows(qmm, orc):
+    """The benchmark shape (m=2048, N=6912, K=2560), checked against the
+    oracle on a sample of weight rows."""
+    m, n, k = 2048, 6912, 2560
+    tw, absmean, aq, scale, asum = _bitnet_operands(orc, 8100, m, n, k)
+    y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), absmean, to_dev(aq), to_dev(scale)))
+    rows = np.r_[0:3, 127:130, 3400:3403, n - 3:n]
+    ref = orc.bitnet_gemv(np.ascontiguousarray(tw[rows]), absmean, aq, scale, asum)
+    assert np.array_equal(y[:, rows].view(np.uint32), ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
 # the two decode GEMV kernels (shared-memory streaming and register streaming)
 
 def _misaligned_copy(t):
