@@ -384,6 +384,11 @@ cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, co
 template <int MT, int ROWS>
 cudaError_t launch_grouped(LinearGroup tab, bool pdl, cudaStream_t s) {
     const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
+    // Longest CTAs first: a CTA's time grows with its problem's k, and CTAs
+    // start in index order, so the long ones must not form the last wave.
+    // (The problems are independent; their order changes no result.)
+    std::stable_sort(tab.p, tab.p + tab.count,
+                     [](const LinearProblem &a, const LinearProblem &b) { return a.k > b.k; });
     int64_t total = 0;
     for (int p = 0; p < tab.count; ++p) {
         total += (tab.p[p].n + rows_per_cta - 1) / rows_per_cta;
