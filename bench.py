@@ -473,7 +473,12 @@ def run_bitnet_prefill(q, steps, warmup, dist, peaks):
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): codes - 1 and "
                          "int8 activations run exactly on tcgen05 kind::f16",
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "traffic": recorded_traffic("bitnet_gemm_kernel"),
+            "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
+                            "(profiles/traffic.txt); algorithmic: 4.4 MB codes + 10.5 MB fp16 "
+                            "activations + 56.6 MB y (most of y is written back from L2 after "
+                            "the kernel)"}
 
 
 def run_prefill(q, steps, warmup, dist, peaks):
