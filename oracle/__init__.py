@@ -6,7 +6,8 @@ test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 library in ``quantized_matmul_gb300/`` and neither side imports the other.
 
 Sources: llama.cpp visual guide, lesson 31 "The CPU backend", section "How the
-quantized dot product works" (Q4_0 x Q8_0); Loom docs, "Plan 9 SIMD Forward",
+quantized dot product works" (Q4_0 x Q8_0; the Q8_0 block, which the Fucina
+reference, section 9, also uses as a weight format: Q8_0 x Q8_0); Loom docs, "Plan 9 SIMD Forward",
 section "BitNet ternary MAD kernel" (ternary path); Fucina course ch. 06,
 section 6.4 (the scalar referee).  The readings taken where the pages are
 silent are listed at the top of ``qmm_oracle.c``.
@@ -67,6 +68,9 @@ def _load():
                 "orc_gemm_q4_0_q8_0": (None, [P, P, P, P, I, I, I, P]),
                 "orc_gemm_q4_0_q8_0_f64": (None, [P, P, P, P, I, I, I, P]),
                 "orc_gemm_q4_0_q8_0_absterms": (None, [P, P, P, P, I, I, I, P]),
+                "orc_block_sums_q8_0_q8_0": (None, [P, P, I, I, I, P]),
+                "orc_gemm_q8_0_q8_0": (None, [P, P, P, P, I, I, I, P]),
+                "orc_gemm_q8_0_q8_0_f64": (None, [P, P, P, P, I, I, I, P, P]),
                 "orc_q4_0_blocks_to_planes": (None, [P, I, I, P, P]),
                 "orc_q4_0_planes_to_blocks": (None, [P, P, I, I, P]),
                 "orc_quantize_act_bitnet": (None, [P, I, I, P, P, P]),
@@ -205,6 +209,49 @@ def q4_0_planes_to_blocks(wq, wd) -> np.ndarray:
     out = np.empty(n * (k // QK) * 18, np.uint8)
     _load().orc_q4_0_planes_to_blocks(_p(wq), _p(wd), n, k, _p(out))
     return out
+
+
+# --------------------------------------------------------------------------
+# Q8_0 weights x Q8_0 activations (weights quantized by quantize_q8_0)
+
+def _q8w_args(w8, wd, aq, ad):
+    w8 = _c(w8, np.int8)
+    wd = _c(wd, np.uint16)
+    aq = _c(aq, np.int8)
+    ad = _c(ad, np.uint16)
+    n = w8.shape[0]
+    m, k = aq.shape
+    assert w8.shape == (n, k) and wd.shape == (n, k // QK) and ad.shape == (m, k // QK)
+    return w8, wd, aq, ad, m, n, k
+
+
+def block_sums_q8_0(w8, aq) -> np.ndarray:
+    """int32 [m, n, k/32]: sum_j q_w * q_a per block."""
+    w8 = _c(w8, np.int8)
+    aq = _c(aq, np.int8)
+    n = w8.shape[0]
+    m, k = aq.shape
+    assert w8.shape[1] == k
+    out = np.empty((m, n, k // QK), np.int32)
+    _load().orc_block_sums_q8_0_q8_0(_p(w8), _p(aq), m, n, k, _p(out))
+    return out
+
+
+def gemm_q8_0_q8_0(w8, wd, aq, ad) -> np.ndarray:
+    """y f32 [m, n] = sum_b fma(sumi, dw*da, acc), blocks ascending."""
+    w8, wd, aq, ad, m, n, k = _q8w_args(w8, wd, aq, ad)
+    y = np.empty((m, n), np.float32)
+    _load().orc_gemm_q8_0_q8_0(_p(w8), _p(wd), _p(aq), _p(ad), m, n, k, _p(y))
+    return y
+
+
+def gemm_q8_0_q8_0_f64(w8, wd, aq, ad) -> tuple[np.ndarray, np.ndarray]:
+    """(y in double, per-output sum of |sumi*dw*da|)."""
+    w8, wd, aq, ad, m, n, k = _q8w_args(w8, wd, aq, ad)
+    y = np.empty((m, n), np.float64)
+    a = np.empty((m, n), np.float64)
+    _load().orc_gemm_q8_0_q8_0_f64(_p(w8), _p(wd), _p(aq), _p(ad), m, n, k, _p(y), _p(a))
+    return y, a
 
 
 # --------------------------------------------------------------------------

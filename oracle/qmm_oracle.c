@@ -26,6 +26,10 @@
  *   [WORKLOAD] the quantizer recipe of the benchmark workloads: Q4_0 with
  *            d = (signed absmax)/-8 and q = clamp(round(w/d)+8, 0, 15);
  *            Q8_0 with d = absmax/127 and q = round(x/d).
+ *   [FUC09]  Fucina reference, "9. Backends: CPU SIMD, BLAS, threading, and
+ *            GPU offload": Q8_0 also serves as a weight (right-hand side)
+ *            format next to Q4_0 (9.2 quantizeMatmulRhsQ8_0, 9.7 the Q8_0 arm
+ *            and its packed layout, 9.9.2 Q8_0 decode and prefill).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   R1 "round" is round-half-away-from-zero (C roundf).
@@ -44,11 +48,15 @@
  *   R9 the f32 output accumulates blocks in ascending order:
  *      acc = fmaf((float)sumi, f32(dw)*f32(da), acc), acc starting at +0.
  *  R10 BitNet y = ((float)dot * absmean) / scale, left to right in f32.
+ *  R16 Q8_0 weights use the Q8_0 activation block and recipe unchanged: per
+ *      32-block d = absmax/127, q = clamp(round(w/d), -127, 127), fp16(d)
+ *      stored; the block dot is sum_j q_w * q_a (no offset) and y follows R9.
  *
  * Layouts (row-major throughout):
  *   x   f32  [m, k] with row stride ldx elements
  *   aq  int8 [m, k]            ad fp16 bits [m, k/32]
  *   wq  u8   [n, k/2]          wd fp16 bits [n, k/32]   (two planes of block_q4_0)
+ *   w8  int8 [n, k]            wd fp16 bits [n, k/32]   (two planes of Q8_0 weight blocks)
  *   y   f32  [m, n]
  *   sumi int32 [m, n, k/32]
  *   tw  u32  [n, k/16]         (ternary, 16 codes per word)
@@ -288,6 +296,78 @@ void orc_gemm_q4_0_q8_0_absterms(const uint8_t *wq, const uint16_t *wd,
                                       * (double)orc_fp16_to_fp32(ad[i * kb + b]));
             }
             y[i * n + r] = acc;
+        }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Q8_0 weights x Q8_0 activations [LCG31] [FUC09], reading R16.  Weights are
+ * quantized by orc_quantize_q8_0 like activations; the two planes are the
+ * int8 codes w8 [n, k] and the fp16 scales wd [n, k/32]. */
+
+/* Per-block integer dot: sumi[i, r, b] = sum_j q_w * q_a. */
+void orc_block_sums_q8_0_q8_0(const int8_t *w8, const int8_t *aq,
+                              int64_t m, int64_t n, int64_t k, int32_t *sumi)
+{
+    int64_t kb = k / ORC_QK;
+    for (int64_t i = 0; i < m; i++)
+        for (int64_t r = 0; r < n; r++)
+            for (int64_t b = 0; b < kb; b++) {
+                const int8_t *qw = w8 + r * k + b * ORC_QK;
+                const int8_t *qa = aq + i * k + b * ORC_QK;
+                int32_t s = 0;
+                for (int j = 0; j < ORC_QK; j++)
+                    s += (int32_t)qw[j] * (int32_t)qa[j];
+                sumi[(i * n + r) * kb + b] = s;
+            }
+}
+
+/* The f32 product, reading R9: blocks ascending, acc = fma((float)sumi,
+ * dw*da, acc), dw*da exact in f32. */
+void orc_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
+                        const int8_t *aq, const uint16_t *ad,
+                        int64_t m, int64_t n, int64_t k, float *y)
+{
+    int64_t kb = k / ORC_QK;
+    for (int64_t i = 0; i < m; i++)
+        for (int64_t r = 0; r < n; r++) {
+            float acc = 0.0f;
+            for (int64_t b = 0; b < kb; b++) {
+                const int8_t *qw = w8 + r * k + b * ORC_QK;
+                const int8_t *qa = aq + i * k + b * ORC_QK;
+                int32_t s = 0;
+                for (int j = 0; j < ORC_QK; j++)
+                    s += (int32_t)qw[j] * (int32_t)qa[j];
+                float scale = orc_fp16_to_fp32(wd[r * kb + b]) * orc_fp16_to_fp32(ad[i * kb + b]);
+                acc = fmaf((float)s, scale, acc);
+            }
+            y[i * n + r] = acc;
+        }
+}
+
+/* Double-precision product (|sumi| <= 32*127*127 < 2^19, so each term
+ * sumi*dw*da is exact in double) and the per-output sum of |terms|, as for
+ * Q4_0. */
+void orc_gemm_q8_0_q8_0_f64(const int8_t *w8, const uint16_t *wd,
+                            const int8_t *aq, const uint16_t *ad,
+                            int64_t m, int64_t n, int64_t k, double *y, double *absterms)
+{
+    int64_t kb = k / ORC_QK;
+    for (int64_t i = 0; i < m; i++)
+        for (int64_t r = 0; r < n; r++) {
+            double acc = 0.0, abs_acc = 0.0;
+            for (int64_t b = 0; b < kb; b++) {
+                const int8_t *qw = w8 + r * k + b * ORC_QK;
+                const int8_t *qa = aq + i * k + b * ORC_QK;
+                int64_t s = 0;
+                for (int j = 0; j < ORC_QK; j++)
+                    s += (int64_t)qw[j] * qa[j];
+                double t = (double)s * (double)orc_fp16_to_fp32(wd[r * kb + b])
+                                     * (double)orc_fp16_to_fp32(ad[i * kb + b]);
+                acc += t;
+                abs_acc += fabs(t);
+            }
+            y[i * n + r] = acc;
+            absterms[i * n + r] = abs_acc;
         }
 }
 

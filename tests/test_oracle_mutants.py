@@ -82,6 +82,24 @@ MUTANTS = [
     ("bitnet_sum_skips_clamp",
      "aq[i * k + j] = (int8_t)q;\n            sum += (int32_t)q;",
      "aq[i * k + j] = (int8_t)q;\n            sum += (int32_t)q + (j == 0);", 1),
+    # Q8_0 weights x Q8_0 activations
+    ("q8w_block_sums_offset_8",
+     "s += (int32_t)qw[j] * (int32_t)qa[j];\n                sumi",
+     "s += ((int32_t)qw[j] - 8) * (int32_t)qa[j];\n                sumi", 1),
+    ("q8w_gemm_weight_row_stride_k_half",
+     "const int8_t *qw = w8 + r * k + b * ORC_QK;\n                const int8_t *qa = aq + i * k + b * ORC_QK;\n                int32_t s = 0;\n                for (int j = 0; j < ORC_QK; j++)\n                    s += (int32_t)qw[j] * (int32_t)qa[j];\n                float scale",
+     "const int8_t *qw = w8 + r * (k / 2) + b * ORC_QK;\n                const int8_t *qa = aq + i * k + b * ORC_QK;\n                int32_t s = 0;\n                for (int j = 0; j < ORC_QK; j++)\n                    s += (int32_t)qw[j] * (int32_t)qa[j];\n                float scale", 1),
+    ("q8w_gemm_reversed_elements",
+     "s += (int32_t)qw[j] * (int32_t)qa[j];\n                float scale",
+     "s += (int32_t)qw[ORC_QK - 1 - j] * (int32_t)qa[j];\n                float scale", 1),
+    ("q8w_gemm_weight_scale_only",
+     "float scale = orc_fp16_to_fp32(wd[r * kb + b]) * orc_fp16_to_fp32(ad[i * kb + b]);\n                acc = fmaf((float)s, scale, acc);\n            }\n            y[i * n + r] = acc;\n        }\n}\n\n/* Double-precision product (|sumi| <= 32*127*127",
+     "float scale = orc_fp16_to_fp32(wd[r * kb + b]);\n                acc = fmaf((float)s, scale, acc);\n            }\n            y[i * n + r] = acc;\n        }\n}\n\n/* Double-precision product (|sumi| <= 32*127*127", 1),
+    ("q8w_f64_block_index_off_by_one",
+     "double t = (double)s * (double)orc_fp16_to_fp32(wd[r * kb + b])",
+     "double t = (double)s * (double)orc_fp16_to_fp32(wd[r * kb + (b + 1) % kb])", 1),
+    ("q8w_absterms_signed",
+     "abs_acc += fabs(t);", "abs_acc += t;", 1),
 ]
 
 PIN_FUNCS = [getattr(pins, n) for n in dir(pins)

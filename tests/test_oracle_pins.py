@@ -202,6 +202,78 @@ def test_row_independence(orc):
 
 
 # ---------------------------------------------------------------------------
+# Q8_0 weights x Q8_0 activations (the same block on both sides)
+
+def test_q8_0_weight_hand_block(orc):
+    g = load_golden("q8_0_q8_0_hand_block.txt")
+    w8, wd = orc.quantize_q8_0(floats(g["w"]).astype(np.float32)[None])
+    assert np.array_equal(w8[0].astype(np.int64), ints(g["wq"]))
+    assert int(wd[0, 0]) == int(g["wd_bits"][0], 0)
+    aq, ad = orc.quantize_q8_0(floats(g["x"]).astype(np.float32)[None])
+    assert np.array_equal(aq[0].astype(np.int64), ints(g["aq"]))
+    assert int(ad[0, 0]) == int(g["ad_bits"][0], 0)
+    assert int(orc.block_sums_q8_0(w8, aq)[0, 0, 0]) == int(g["sumi"][0])
+    assert float(orc.gemm_q8_0_q8_0(w8, wd, aq, ad)[0, 0]) == float(g["y"][0])
+    y64, absterms = orc.gemm_q8_0_q8_0_f64(w8, wd, aq, ad)
+    assert float(y64[0, 0]) == float(g["y"][0]) and float(absterms[0, 0]) == abs(float(g["y"][0]))
+
+
+def test_q8_0_weight_block_sums_vs_integer_einsum(orc):
+    for i, (m, n, k) in enumerate(SMALL_SHAPES):
+        w, x = _small_case(600 + i, m, n, k)
+        w8, _ = orc.quantize_q8_0(w)
+        aq, _ = orc.quantize_q8_0(x)
+        wv = w8.astype(np.int64).reshape(n, k // QK, QK)
+        av = aq.astype(np.int64).reshape(m, k // QK, QK)
+        ref = np.einsum("nbj,mbj->mnb", wv, av)
+        assert np.array_equal(orc.block_sums_q8_0(w8, aq), ref), (m, n, k)
+
+
+def test_q8_0_weight_brute_force_dequantize_then_dot(orc):
+    for i, (m, n, k) in enumerate(SMALL_SHAPES):
+        w, x = _small_case(700 + i, m, n, k)
+        w8, wd = orc.quantize_q8_0(w)
+        aq, ad = orc.quantize_q8_0(x)
+        wf = w8.astype(np.float64) * np.repeat(fp16_bits_to_f64(wd), QK, axis=1)
+        af = aq.astype(np.float64) * np.repeat(fp16_bits_to_f64(ad), QK, axis=1)
+        y_bf = af @ wf.T
+        y64, at = orc.gemm_q8_0_q8_0_f64(w8, wd, aq, ad)
+        np.testing.assert_allclose(y64, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+        y32 = orc.gemm_q8_0_q8_0(w8, wd, aq, ad).astype(np.float64)
+        absterms = np.abs(af) @ np.abs(wf).T  # >= the per-block |terms| sum
+        assert (np.abs(y32 - y_bf) <= 1e-6 * absterms + 1e-30).all(), (m, n, k)
+        assert (at <= absterms * (1 + 1e-12)).all() and (at >= np.abs(y_bf) * (1 - 1e-12)).all()
+
+
+def test_q8_0_weight_integer_matmul_reduction(orc):
+    """With every scale fp16(1.0) the product is the plain integer matmul
+    (exact in f32 here: |y| <= 127 * 127 * 256 < 2^24)."""
+    rng = np.random.default_rng(4)
+    for (m, n, k) in [(1, 5, 64), (3, 17, 96), (7, 33, 256)]:
+        w8 = rng.integers(-127, 128, size=(n, k), dtype=np.int64).astype(np.int8)
+        aq = rng.integers(-127, 128, size=(m, k), dtype=np.int64).astype(np.int8)
+        one = np.uint16(0x3C00)
+        wd = np.full((n, k // QK), one, np.uint16)
+        ad = np.full((m, k // QK), one, np.uint16)
+        ref = aq.astype(np.int64) @ w8.astype(np.int64).T
+        y = orc.gemm_q8_0_q8_0(w8, wd, aq, ad)
+        assert np.array_equal(y.astype(np.int64), ref)
+        assert np.array_equal(orc.block_sums_q8_0(w8, aq).sum(axis=2), ref)
+        y64, _ = orc.gemm_q8_0_q8_0_f64(w8, wd, aq, ad)
+        assert np.array_equal(y64.astype(np.int64), ref)
+
+
+def test_q8_0_weight_row_independence(orc):
+    w, x = _small_case(8, 6, 23, 128)
+    w8, wd = orc.quantize_q8_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    y = orc.gemm_q8_0_q8_0(w8, wd, aq, ad)
+    rows, cols = [1, 4], [0, 5, 22]
+    ys = orc.gemm_q8_0_q8_0(w8[cols], wd[cols], aq[rows], ad[rows])
+    assert np.array_equal(ys.view(np.uint32), y[np.ix_(rows, cols)].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
 # quantizer invariants
 
 def _adversarial_rows(rng, k):
