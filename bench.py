@@ -428,6 +428,66 @@ def run_single_gemv(q, steps, warmup, dist, peaks):
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
 
 
+def q8_weight_bytes(n, k):
+    return n * k + 2 * n * (k // QK)
+
+
+def _q8_weights(q, seed, n, k, m, copies, **kw):
+    """As _quantized_weights, with Q8_0 weights (the activation recipe)."""
+    from quantized_matmul_gb300 import synthetic
+    w, x = synthetic.q4_0_case(seed, n, k, m, **kw)
+    wdev = _up(w)
+    w8, wd = q.quantize_weight_q8_0(wdev)
+    del wdev
+    return [(w8, wd)] + [(w8.clone(), wd.clone()) for _ in range(copies - 1)], x
+
+
+def run_q8_gemv(q, steps, warmup, dist, peaks):
+    """Q8_0 weights x Q8_0 decode GEMV at the 4096 x 4096 shape (seed 0)."""
+    import torch
+    n, k = 4096, 4096
+    rot = copies_for(q8_weight_bytes(n, k))
+    wts, x = _q8_weights(q, 0, n, k, 1, rot)
+    aq, ad = q.quantize_act_q8_0(_up(x))
+    y = torch.empty((1, n), dtype=torch.float32, device="cuda")
+
+    def step(i):
+        w8, wd = wts[i % rot]
+        q.gemv_q8_0_q8_0(w8, wd, aq, ad, y=y, split_k=1)
+
+    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    nbytes = q8_weight_bytes(n, k) + k + 2 * (k // QK) + 4 * n
+    gbs = dist.world * nbytes * steps / (ms * 1e-3) / 1e9
+    return {"workload": "Q8_0xQ8_0 GEMV m=1 K=4096 N=4096 (seed 0; Q8_0 weights)",
+            "value": round(gbs, 1), "unit": "GB/s",
+            "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+
+
+def run_q8_prefill(q, steps, warmup, dist, peaks):
+    """Q8_0 weights x Q8_0 prefill GEMM at the 512 x 14336 x 4096 shape."""
+    import torch
+    m, n, k = 512, 14336, 4096
+    rot = copies_for(q8_weight_bytes(n, k) + m * k)
+    wts, x = _q8_weights(q, 11, n, k, m, rot, outlier_p=0.01)
+    aq, ad = q.quantize_act_q8_0(_up(x))
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    ws = torch.empty((q.workspace_bytes(q.OP_GEMM_Q8, m, n, k),), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        w8, wd = wts[i % rot]
+        q.gemm_q8_0_q8_0(w8, wd, aq, ad, y=y, workspace=ws)
+
+    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": "Q8_0xQ8_0 prefill GEMM m=512 K=4096 N=14336, 1% outliers x20 "
+                        "(seed 11; Q8_0 weights)",
+            "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
+            "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+
+
 def run_bitnet(q, steps, warmup, dist, peaks):
     import torch
     from quantized_matmul_gb300 import synthetic
@@ -627,7 +687,8 @@ def main():
                     help="seconds of oracle work for --impl reference (warm-up + steps)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
-    ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill"],
+    ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill",
+                                       "q8_gemv", "q8_prefill"],
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
@@ -650,7 +711,9 @@ def main():
                    "prefill": lambda: run_prefill(q, args.steps, args.warmup, dist, peaks),
                    "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks),
                    "bitnet_prefill": lambda: run_bitnet_prefill(q, args.steps, args.warmup, dist,
-                                                                peaks)}
+                                                                peaks),
+                   "q8_gemv": lambda: run_q8_gemv(q, args.steps, args.warmup, dist, peaks),
+                   "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks)}
             res = run[args.only]()
             if dist.rank == 0:
                 print(json.dumps({"only": args.only, "result": res}), flush=True)
@@ -665,6 +728,9 @@ def main():
             configs["bitnet_prefill_2048x6912x2560"] = run_bitnet_prefill(q, max(50, short // 20),
                                                                           10, dist, peaks)
             configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks)
+            configs["q8_0_gemv_4096x4096"] = run_q8_gemv(q, short * 5, args.warmup, dist, peaks)
+            configs["q8_0_prefill_512x14336x4096"] = run_q8_prefill(q, max(50, short // 20), 10,
+                                                                    dist, peaks)
         cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
         if dist.rank == 0:
             line = {

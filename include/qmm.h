@@ -66,7 +66,9 @@ typedef enum qmm_status {
 enum {
     QMM_OP_GEMV_Q4_0_Q8_0 = 1,
     QMM_OP_GEMM_Q4_0_Q8_0 = 2,
-    QMM_OP_BITNET_GEMM = 3
+    QMM_OP_BITNET_GEMM = 3,
+    QMM_OP_GEMV_Q8_0_Q8_0 = 4,
+    QMM_OP_GEMM_Q8_0_Q8_0 = 5
 };
 
 /* Largest m accepted by the GEMV entry points (decode and small batches). */
@@ -209,6 +211,38 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* Q8_0 weights x Q8_0 activations.  The Q8_0 block (lesson 31: 32 int8 codes
+ * and one fp16 scale) also serves as a weight format (Fucina reference,
+ * section 9: the Q8_0 right-hand side of 9.2 and 9.7, Q8_0 decode and
+ * prefill in 9.9.2).  Weights are quantized with the activation recipe:
+ * qmm_quantize_act_q8_0 on the f32 weight rows gives the two planes, codes
+ * w8 int8 [n, k] and scales wd fp16 bits [n, k/32].  The block dot is
+ * sumi = sum_j q_w * q_a (no offset), exact in int32 (|sumi| <= 516,128),
+ * and y follows the same rule as the Q4_0 products.
+ *
+ * The decode GEMV (1 <= m <= QMM_GEMV_MAX_M): arguments, split_k and
+ * workspace as for qmm_gemv_q4_0_q8_0 (workspace size from
+ * qmm_workspace_bytes(QMM_OP_GEMV_Q8_0_Q8_0, ...)); w8 16-byte aligned.
+ * Each warp streams its rows through registers, two 16-byte loads per
+ * block. */
+qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
+                              const int8_t *aq, const uint16_t *ad, float *y,
+                              int64_t m, int64_t n, int64_t k, int split_k,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* The prefill product (any m >= 1) on the tensor cores, as
+ * qmm_gemm_q4_0_q8_0: the int8 codes are exact in fp16, the block sums exact
+ * in the f32 TMEM accumulators, and each f32 output accumulates
+ * fma(sumi, dw*da, acc) over blocks in ascending order, bit for bit the
+ * serial definition.  Workspace: qmm_workspace_bytes(QMM_OP_GEMM_Q8_0_Q8_0,
+ * m, n, k, 0) bytes, 256-byte aligned; w8 16-byte aligned; the rest as for
+ * qmm_gemm_q4_0_q8_0. */
+qmm_status qmm_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
+                              const int8_t *aq, const uint16_t *ad, float *y,
+                              int64_t m, int64_t n, int64_t k,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* BitNet activation quantization (Loom, "BitNet ternary MAD kernel"): per row
  * s = 127 / max|x| (s = 0 for an all-zero row), q = clamp(round(x * s),
  * -127, 127), act_sum = sum q.
@@ -283,6 +317,14 @@ int qmm_version(void);
  * core GEMM kernel (needs the GEMM workspace).  Same alignment rules as the
  * product entry points; sumi 4-byte aligned. */
 qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int8_t *aq,
+                                          int32_t *sumi, int64_t m, int64_t n, int64_t k,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream);
+
+/* Per-block sums sumi int32 [m, n, k/32] = sum_j q_w * q_a of the Q8_0-weight
+ * kernels: path 0 the decode GEMV, path 1 the tensor-core GEMM (needs its
+ * workspace).  Rules as for qmm_debug_block_sums_q4_0_q8_0. */
+qmm_status qmm_debug_block_sums_q8_0_q8_0(int path, const int8_t *w8, const int8_t *aq,
                                           int32_t *sumi, int64_t m, int64_t n, int64_t k,
                                           void *workspace, size_t workspace_bytes,
                                           void *stream);

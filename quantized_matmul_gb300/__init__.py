@@ -27,6 +27,8 @@ GEMV_MAX_M = 16
 OP_GEMV = 1
 OP_GEMM = 2
 OP_BITNET_GEMM = 3
+OP_GEMV_Q8 = 4
+OP_GEMM_Q8 = 5
 
 STATUS_NAMES = {0: "ok", 1: "null pointer", 2: "invalid shape", 3: "misaligned pointer",
                 4: "workspace missing or too small", 5: "unsupported device", 6: "CUDA error",
@@ -60,6 +62,8 @@ def load() -> ctypes.CDLL:
             "qmm_gemv_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
             "qmm_gemm_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_gemv_q4_0_q8_0_noalloc": (I, [P, P, P, P, P, I64, I64, I64, I, P]),
+            "qmm_gemv_q8_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
+            "qmm_gemm_q8_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_linear_q4_0": (I, [P, P, P, I64, P, P, P, I64, I64, I64, I, P]),
             "qmm_linear_q4_0_grouped": (I, [P, I, I64, I, P]),
             "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
@@ -72,6 +76,7 @@ def load() -> ctypes.CDLL:
             "qmm_status_string": (ctypes.c_char_p, [I]),
             "qmm_version": (I, []),
             "qmm_debug_block_sums_q4_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
+            "qmm_debug_block_sums_q8_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_debug_bitnet_dot": (I, [P, P, P, P, I64, I64, I64, P]),
             "qmm_debug_set_wait_limit": (None, [U32]),
             "qmm_debug_withhold_gemm_loads": (None, [I]),
@@ -222,6 +227,50 @@ def gemm_q4_0_q8_0(wq, wd, aq, ad, y=None, workspace=None):
                                    _dev(y, torch.float32, "y", (m, n)), m, n, k,
                                    ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
     _check(st, "qmm_gemm_q4_0_q8_0")
+    return y
+
+
+def quantize_weight_q8_0(w):
+    """Q8_0 weights: the activation recipe on the f32 weight rows, giving
+    (w8 int8 [n, k], wd fp16 [n, k/32])."""
+    return quantize_act_q8_0(w)
+
+
+def _q8_shapes(w8, wd, aq, ad):
+    torch = _torch()
+    n = w8.shape[0]
+    m, k = aq.shape
+    _dev(w8, torch.int8, "w8", (n, k))
+    _dev(wd, torch.float16, "wd", (n, k // QK))
+    _dev(aq, torch.int8, "aq", (m, k))
+    _dev(ad, torch.float16, "ad", (m, k // QK))
+    return m, n, k
+
+
+def gemv_q8_0_q8_0(w8, wd, aq, ad, y=None, split_k: int = 0, workspace=None):
+    """Decode GEMV with Q8_0 weights (m <= 16): y f32 [m, n]."""
+    torch = _torch()
+    m, n, k = _q8_shapes(w8, wd, aq, ad)
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMV_Q8, m, n, k, split_k)
+                              if m <= GEMV_MAX_M else 0, aq)
+    st = load().qmm_gemv_q8_0_q8_0(w8.data_ptr(), wd.data_ptr(), aq.data_ptr(), ad.data_ptr(),
+                                   _dev(y, torch.float32, "y", (m, n)), m, n, k, split_k,
+                                   ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
+    _check(st, "qmm_gemv_q8_0_q8_0")
+    return y
+
+
+def gemm_q8_0_q8_0(w8, wd, aq, ad, y=None, workspace=None):
+    """Prefill GEMM with Q8_0 weights on the tensor cores: y f32 [m, n]."""
+    torch = _torch()
+    m, n, k = _q8_shapes(w8, wd, aq, ad)
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM_Q8, m, n, k), aq)
+    st = load().qmm_gemm_q8_0_q8_0(w8.data_ptr(), wd.data_ptr(), aq.data_ptr(), ad.data_ptr(),
+                                   _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                   ws.data_ptr() if ws is not None else None, ws_bytes, _stream())
+    _check(st, "qmm_gemm_q8_0_q8_0")
     return y
 
 
@@ -395,6 +444,25 @@ def debug_block_sums(path: int, wq, aq, workspace=None):
                                                m, n, k, ws.data_ptr() if ws is not None else None,
                                                ws_bytes, _stream())
     _check(st, "qmm_debug_block_sums_q4_0_q8_0")
+    return sumi
+
+
+def debug_block_sums_q8(path: int, w8, aq, workspace=None):
+    """int32 [m, n, k/32] block sums of the Q8_0-weight GEMV (path 0) or GEMM
+    (path 1) kernel."""
+    torch = _torch()
+    n = w8.shape[0]
+    m, k = aq.shape
+    _dev(w8, torch.int8, "w8", (n, k))
+    _dev(aq, torch.int8, "aq", (m, k))
+    sumi = _empty((m, n, k // QK), torch.int32, aq)
+    ws, ws_bytes = (None, 0)
+    if path == 1:
+        ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM_Q8, m, n, k), aq)
+    st = load().qmm_debug_block_sums_q8_0_q8_0(path, w8.data_ptr(), aq.data_ptr(), sumi.data_ptr(),
+                                               m, n, k, ws.data_ptr() if ws is not None else None,
+                                               ws_bytes, _stream())
+    _check(st, "qmm_debug_block_sums_q8_0_q8_0")
     return sumi
 
 

@@ -1,10 +1,15 @@
-// Prefill-shaped Q4_0 x Q8_0 product on the 5th-generation tensor cores.
+// Prefill-shaped Q4_0 x Q8_0 and Q8_0 x Q8_0 products on the 5th-generation
+// tensor cores.
 //
 // What it computes (llama.cpp visual guide, lesson 31 "The CPU backend",
 // section "How the quantized dot product works"): for every output
 // y[t, n] = sum over blocks b of sumi[t, n, b] * (dw[n, b] * da[t, b]) where
 // sumi is the exact integer dot of the 32 nibbles (minus 8) with the 32 int8
 // activations of the block, accumulated block by block in ascending order.
+// With Q8_0 weights (the Fucina reference, section 9, uses the Q8_0 block as
+// a weight format too) the weight values are the 32 int8 codes of the block
+// (|sumi| <= 32 * 127 * 127 < 2^24); only the weight tile and its converter
+// differ (template parameter WB, the weight bytes per row and stage).
 //
 // How (GB300, sm_103a).  There is no int8 MMA on sm_103a, but every operand
 // value is a small integer that fp16 holds exactly (weights -8..7,
@@ -22,7 +27,7 @@
 // One CTA computes a tile of 128 weight rows (the MMA's M, TMEM lanes) by BN
 // tokens (the MMA's N, TMEM columns).  Roles:
 //   warp 0      TMA producer: per stage of two blocks (64 k-elements) the
-//               128 x 32 B nibble tile, the BN x 64 fp16 activation tile
+//               128 x 32 B nibble tile (128 x 64 B of codes for Q8_0), the BN x 64 fp16 activation tile
 //               (128-byte swizzle) and the two BN x 16 B scale rows (da in
 //               the first fp16 of each row, written by the prepass).
 //   warps 1, 2  warp 1 allocates TMEM; lane 0 of warp 1 (even blocks) and of
@@ -75,31 +80,33 @@ template <int BN>
 __host__ __device__ constexpr int drain_groups() { return BN >= 64 ? BN / 32 : 1; }
 template <int BN>
 __host__ __device__ constexpr int ctas_per_sm() { return BN <= 32 ? 2 : 1; }
-// bytes of one pipeline stage: A tile, B tile, nibbles, dw tile, da tile
-template <int BN>
+// WB: weight bytes per row and stage (two blocks): 32 for Q4_0 nibbles, 64
+// for Q8_0 codes.
+// bytes of one pipeline stage: A tile, B tile, weight tile, dw tile, da tile
+template <int BN, int WB>
 __host__ __device__ constexpr int stage_bytes() {
-    return kBM * kBK * 2 + BN * kBK * 2 + kBM * (kBK / 2) + 2 * kBM * 16 + 2 * BN * 16;
+    return kBM * kBK * 2 + BN * kBK * 2 + kBM * WB + 2 * kBM * 16 + 2 * BN * 16;
 }
-template <int BN>
+template <int BN, int WB>
 __host__ __device__ constexpr int stages_fit() {
-    return ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN>() < 8
-               ? ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN>()
+    return ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN, WB>() < 8
+               ? ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN, WB>()
                : 8;
 }
 // Converter warps: up to four, and the stage count a multiple of them, so
 // converter c owns the ring slots s = c (mod converters) and handles every
 // use of them in order.  (A warp that took stages round robin could reach a
 // slot's barrier two phases early, which a parity wait cannot tell apart.)
-template <int BN>
-__host__ __device__ constexpr int conv_warps() { return stages_fit<BN>() < 4 ? stages_fit<BN>() : 4; }
-template <int BN>
+template <int BN, int WB>
+__host__ __device__ constexpr int conv_warps() { return stages_fit<BN, WB>() < 4 ? stages_fit<BN, WB>() : 4; }
+template <int BN, int WB>
 __host__ __device__ constexpr int stages_for() {
-    return stages_fit<BN>() / conv_warps<BN>() * conv_warps<BN>();
+    return stages_fit<BN, WB>() / conv_warps<BN, WB>() * conv_warps<BN, WB>();
 }
-template <int BN>
-__host__ __device__ constexpr int epi_warp0() { return kConvWarp0 + conv_warps<BN>(); }
-template <int BN>
-__host__ __device__ constexpr int threads_for() { return 32 * (epi_warp0<BN>() + 4 * drain_groups<BN>()); }
+template <int BN, int WB>
+__host__ __device__ constexpr int epi_warp0() { return kConvWarp0 + conv_warps<BN, WB>(); }
+template <int BN, int WB>
+__host__ __device__ constexpr int threads_for() { return 32 * (epi_warp0<BN, WB>() + 4 * drain_groups<BN>()); }
 // TMEM accumulator slots, one per block in flight (2 * BN columns each)
 template <int BN>
 constexpr int nacc_for() {
@@ -176,6 +183,25 @@ __device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
     out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // elements 24..31
 }
 
+// 32 int8 codes of one Q8_0 block (two 16-byte words, elements in order) ->
+// 32 fp16 values.  Exact: the fp16 pattern 0x6400 | u is 1024 + u for
+// u < 1024, and u = b ^ 0x80 = b + 128 for a signed byte b, so subtracting
+// 1152 leaves b.
+__device__ __forceinline__ void unpack_block_q8_f16(uint4 v0, uint4 v1, uint4 (&out)[4]) {
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const __half2 off = u32_as_h2(0x64806480u);  // (1152, 1152)
+    uint32_t h[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t p0 = __byte_perm(w[i], 0, 0x4140);  // bytes 0, 1 -> halves
+        const uint32_t p1 = __byte_perm(w[i], 0, 0x4342);  // bytes 2, 3 -> halves
+        h[2 * i] = h2_as_u32(__hsub2(u32_as_h2((p0 ^ 0x00800080u) | 0x64006400u), off));
+        h[2 * i + 1] = h2_as_u32(__hsub2(u32_as_h2((p1 ^ 0x00800080u) | 0x64006400u), off));
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) out[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+}
+
 
 // Shared-memory descriptor for the scale tiles: K-major, no swizzle, 16-byte
 // rows, 8-row groups 128 bytes apart (stride offset), the second K core
@@ -192,14 +218,14 @@ __device__ __forceinline__ uint64_t smem_desc_scale(uint32_t saddr, uint32_t lea
 // ---------------------------------------------------------------------------
 // Shared memory plan (dynamic; the base is rounded up to 1024 bytes)
 
-template <int BN>
+template <int BN, int WB>
 struct Smem {
-    static constexpr int kStages = stages_for<BN>();
+    static constexpr int kStages = stages_for<BN, WB>();
     static constexpr int kNacc = nacc_for<BN>();
     static constexpr int kEpiWarps = 4 * drain_groups<BN>();
     static constexpr int kA = kBM * kBK * 2;   // fp16 weights, 16 KB
     static constexpr int kB = BN * kBK * 2;    // fp16 activations
-    static constexpr int kNib = kBM * (kBK / 2);  // nibble bytes, 4 KB
+    static constexpr int kNib = kBM * WB;      // weight bytes (nibbles or int8 codes)
     static constexpr int kAs = 2 * kBM * 16;   // dw tiles of the two blocks
     static constexpr int kBs = 2 * BN * 16;    // da tiles of the two blocks
     static constexpr int kOffA = 0;
@@ -217,20 +243,20 @@ struct Smem {
     static_assert(kOffB % 1024 == 0 && kB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 };
 
-template <int BN, bool EMIT>
-__global__ void __launch_bounds__(threads_for<BN>(), ctas_per_sm<BN>())
-gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
+template <int BN, bool EMIT, int WB>
+__global__ void __launch_bounds__(threads_for<BN, WB>(), ctas_per_sm<BN>())
+gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       const __grid_constant__ CUtensorMap tm_act,
                       const __grid_constant__ CUtensorMap tm_bs,
                       const unsigned short *__restrict__ wd, float *__restrict__ y,
                       int32_t *__restrict__ sumi, int m, int n, int kb_total, int m4,
                       uint32_t wait_limit, int withhold_loads) {
-    using S = Smem<BN>;
+    using S = Smem<BN, WB>;
     constexpr int kStages = S::kStages;
     constexpr int kNacc = S::kNacc;
     constexpr int kEpiWarps = S::kEpiWarps;
-    constexpr int kConvWarps = conv_warps<BN>();
-    constexpr int kEpiWarp0 = epi_warp0<BN>();
+    constexpr int kConvWarps = conv_warps<BN, WB>();
+    constexpr int kEpiWarp0 = epi_warp0<BN, WB>();
     static_assert(kStages % kConvWarps == 0, "converter c owns the slots c (mod converters)");
     static_assert(kNacc % kMmaWarps == 0, "block b's slot b % NACC belongs to issuer b % 2");
     extern __shared__ uint8_t smem_raw[];
@@ -292,7 +318,7 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
             if (lane == 0) {
                 const bool two = 2 * it + 1 < kb_total;
                 mbar_arrive_expect_tx(&bar_load[s], S::kTx - (two ? 0u : (uint32_t)(BN * 16)));
-                tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * (kBK / 2), n0);
+                tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * WB, n0);
                 tma_load_2d(smem + S::kOffB + s * S::kB, &tm_act, &bar_load[s], it * kBK, t0);
                 uint8_t *bs = smem + S::kOffBs + s * S::kBs;
                 tma_load_2d(bs, &tm_bs, &bar_load[s], 0, (2 * it) * m4 + t0);
@@ -383,25 +409,33 @@ gemm_q4_0_q8_0_kernel(const __grid_constant__ CUtensorMap tm_nib,
             const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
             uint8_t *as_tile = smem + S::kOffAs + s * S::kAs;
+            // units in flight per batch: four nibble blocks, or two blocks of
+            // codes (the same bytes in registers)
+            constexpr int kBatch = WB == 32 ? 4 : 2;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {  // four units at a time
-                uint4 v[4];
+            for (int g = 0; g < 8 / kBatch; ++g) {
+                uint4 v[kBatch][WB / 32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v[i] = *reinterpret_cast<const uint4 *>(nib + (32 * (4 * half + i) + lane) * 16);
+                for (int i = 0; i < kBatch; ++i)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int u = 32 * (4 * half + i) + lane;
+                    for (int j = 0; j < WB / 32; ++j)
+                        v[i][j] = *reinterpret_cast<const uint4 *>(nib + (32 * (kBatch * g + i) + lane) * (WB / 2) + 16 * j);
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    const int u = 32 * (kBatch * g + i) + lane;
                     const int row = u >> 1, blk = u & 1;
                     uint4 out[4];
-                    unpack_block_f16(v[i], out);
+                    if constexpr (WB == 32)
+                        unpack_block_f16(v[i][0], out);
+                    else
+                        unpack_block_q8_f16(v[i][0], v[i][WB / 32 - 1], out);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4 *>(a_tile + row * 128 +
                                                    (((blk * 4 + c) ^ (row & 7)) * 16)) = out[c];
                     if (!EMIT)
                         *reinterpret_cast<uint4 *>(as_tile + blk * kBM * 16 + row * 16) =
-                            make_uint4((uint32_t)dwv[4 * half + i], 0u, 0u, 0u);
+                            make_uint4((uint32_t)dwv[kBatch * g + i], 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
@@ -544,23 +578,23 @@ WsPlan plan_ws(int64_t m, int64_t k) {
 uint32_t g_wait_limit = kDefaultWaitLimit;
 int g_withhold_loads = 0;
 
-template <int BN>
+template <int BN, int WB>
 cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &bs,
                         const uint16_t *wd, float *y, int32_t *sumi, int64_t m, int64_t n,
                         int64_t k, int64_t m4, cudaStream_t s) {
-    using S = Smem<BN>;
+    using S = Smem<BN, WB>;
     const int kb = (int)(k / kQK);
     dim3 grid((unsigned)((m + BN - 1) / BN), (unsigned)((n + kBM - 1) / kBM));
     const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
     if (sumi) {
-        auto kern = gemm_q4_0_q8_0_kernel<BN, true>;
+        auto kern = gemm_blocks_kernel<BN, true, WB>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
+        kern<<<grid, threads_for<BN, WB>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
                                                         (int)m4, g_wait_limit, g_withhold_loads);
     } else {
-        auto kern = gemm_q4_0_q8_0_kernel<BN, false>;
+        auto kern = gemm_blocks_kernel<BN, false, WB>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-        kern<<<grid, threads_for<BN>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
+        kern<<<grid, threads_for<BN, WB>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
                                                         (int)m4, g_wait_limit, g_withhold_loads);
     }
     return cudaPeekAtLastError();
@@ -589,9 +623,15 @@ cudaError_t gemm_read_and_clear_error(unsigned int *word, cudaStream_t s) {
     return e;
 }
 
-cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
-                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
-                                  int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+namespace {
+
+// Shared host path of both weight formats: prepass, tensor maps, launch.
+// WB = weight bytes per row and stage (32: Q4_0 nibbles [n, k/2]; 64: Q8_0
+// codes [n, k]).
+template <int WB>
+cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, const uint16_t *ad,
+                        float *y, int32_t *sumi, int64_t m, int64_t n, int64_t k, void *workspace,
+                        cudaStream_t s) {
     const WsPlan p = plan_ws(m, k);
     auto *ws = static_cast<uint8_t *>(workspace);
     __half *a16 = reinterpret_cast<__half *>(ws + p.a16_off);
@@ -606,10 +646,11 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
         if (e != cudaSuccess) return e;
     }
     const int bn = choose_bn(m);
+    const uint64_t row_bytes = (uint64_t)(k * WB / kBK);  // k/2 (Q4_0) or k (Q8_0)
     CUtensorMap tm_nib, tm_act, tm_bs;
-    // nibbles: u8 [n rows, k/2 bytes], box 32 bytes x 128 rows
-    if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)(k / 2), (uint64_t)n,
-                     (uint64_t)(k / 2), kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+    // weights: u8 [n rows, row_bytes], box WB bytes x 128 rows
+    if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, (uint64_t)n, row_bytes,
+                     WB, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     // activations: fp16 [m rows, k], box 64 x BN, 128-byte swizzle
     if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, (uint64_t)k, (uint64_t)m,
@@ -620,11 +661,25 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
                      8, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     switch (bn) {
-        case 16: return launch_tile<16>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        case 32: return launch_tile<32>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        case 64: return launch_tile<64>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        default: return launch_tile<128>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 16: return launch_tile<16, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 32: return launch_tile<32, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 64: return launch_tile<64, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        default: return launch_tile<128, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    return launch_gemm<32>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+}
+
+cudaError_t launch_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    return launch_gemm<64>(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }
 
 }  // namespace qmm

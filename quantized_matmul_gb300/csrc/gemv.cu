@@ -454,6 +454,14 @@ cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
     return cudaPeekAtLastError();
 }
 
+cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count, int split,
+                                 cudaStream_t s) {
+    const int threads = 256;
+    const dim3 grid((unsigned)((count + threads - 1) / threads));
+    splitk_reduce_kernel<false><<<grid, threads, 0, s>>>(partials, y, count, split);
+    return cudaPeekAtLastError();
+}
+
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s) {

@@ -193,6 +193,37 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_
                                                     as_stream(stream)));
 }
 
+qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                              const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                              int split_k, void *workspace, size_t workspace_bytes, void *stream) {
+    const auto *wb = reinterpret_cast<const uint8_t *>(w8);
+    if (qmm_status st = check_q4_common(wb, wd, aq, ad, y, m, n, k)) return st;
+    if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    int split = 1;
+    if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
+    const size_t need = qmm::gemv_workspace_bytes(m, n, k, split);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return QMM_ERR_WORKSPACE;
+    if (need > 0 && !aligned(workspace, 16)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemv_q8_0_q8_0(w8, wd, aq, ad, y, nullptr, m, n, k, split,
+                                                    static_cast<float *>(workspace),
+                                                    as_stream(stream)));
+}
+
+qmm_status qmm_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                              const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    const auto *wb = reinterpret_cast<const uint8_t *>(w8);
+    if (qmm_status st = check_q4_common(wb, wd, aq, ad, y, m, n, k)) return st;
+    if (qmm_status st = gemm_shape_ok(m, n, 2 * k)) return st;  // Q8_0 rows are k bytes
+    const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+    if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemm_q8_0_q8_0(w8, wd, aq, ad, y, nullptr, m, n, k, workspace,
+                                                    as_stream(stream)));
+}
+
 qmm_status qmm_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t *aq,
                                    float *act_scale, int32_t *act_sum, void *stream) {
     if (!x || !aq || !act_scale || !act_sum) return QMM_ERR_NULL;
@@ -265,7 +296,14 @@ size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k)
             if (gemv_split(split_k, m, n, k, &split) != QMM_OK) return SIZE_MAX;
             return qmm::gemv_workspace_bytes(m, n, k, split);
         }
+        case QMM_OP_GEMV_Q8_0_Q8_0: {
+            if (m > QMM_GEMV_MAX_M) return SIZE_MAX;
+            int split = 1;
+            if (gemv_split(split_k, m, n, k, &split) != QMM_OK) return SIZE_MAX;
+            return qmm::gemv_workspace_bytes(m, n, k, split);
+        }
         case QMM_OP_GEMM_Q4_0_Q8_0:
+        case QMM_OP_GEMM_Q8_0_Q8_0:
             return qmm::gemm_workspace_bytes(m, n, k);
         default:
             return SIZE_MAX;
@@ -326,6 +364,31 @@ qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int
         if (qmm_status st = check_device()) return st;
         // The block-sum variant reads no scale planes (passed as NULL).
         return launch_status(qmm::launch_gemm_q4_0_q8_0(wq, nullptr, aq, nullptr, nullptr, sumi, m,
+                                                        n, k, workspace, as_stream(stream)));
+    }
+    return QMM_ERR_ARG;
+}
+
+qmm_status qmm_debug_block_sums_q8_0_q8_0(int path, const int8_t *w8, const int8_t *aq,
+                                          int32_t *sumi, int64_t m, int64_t n, int64_t k,
+                                          void *workspace, size_t workspace_bytes, void *stream) {
+    static const uint16_t dummy[8] = {0};
+    if (!sumi) return QMM_ERR_NULL;
+    const auto *wb = reinterpret_cast<const uint8_t *>(w8);
+    if (qmm_status st = check_q4_common(wb, dummy, aq, dummy, sumi, m, n, k)) return st;
+    if (path == 0) {
+        if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemv_q8_0_q8_0(w8, nullptr, aq, nullptr, nullptr, sumi, m,
+                                                        n, k, 1, nullptr, as_stream(stream)));
+    }
+    if (path == 1) {
+        if (qmm_status st = gemm_shape_ok(m, n, 2 * k)) return st;  // Q8_0 rows are k bytes
+        const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+        if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemm_q8_0_q8_0(w8, nullptr, aq, nullptr, nullptr, sumi, m,
                                                         n, k, workspace, as_stream(stream)));
     }
     return QMM_ERR_ARG;

@@ -93,6 +93,9 @@ cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s);
+// y[i] = sum over slices s of partials[s * count + i], slices in order.
+cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count, int split,
+                                 cudaStream_t s);
 // Quantizer then GEMV (unsplit) for every problem of the group: two launches.
 cudaError_t launch_linear_grouped(const LinearGroup &g, bool pdl, cudaStream_t s);
 
@@ -115,10 +118,22 @@ cudaError_t launch_bitnet_gemm(const uint32_t *w, float absmean, const int8_t *a
 void bitnet_gemm_set_wait_limit(uint32_t iterations);
 cudaError_t bitnet_gemm_read_and_clear_error(unsigned int *word, cudaStream_t s);
 
+// gemv_q8.cu: Q8_0 weights (int8 [n, k] + fp16 scales [n, k/32]) x Q8_0
+// activations, m <= 16; same workspace rule as the Q4_0 GEMV; sumi != nullptr
+// selects the block-sum variant (split must be 1).
+cudaError_t launch_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, int split, float *partials,
+                                  cudaStream_t s);
+
 // gemm.cu
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 // sumi != nullptr selects the block-sum emitting variant.
 cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                  const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                  int64_t n, int64_t k, void *workspace, cudaStream_t s);
+// The same product with Q8_0 weights (int8 [n, k]); same workspace.
+cudaError_t launch_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s);
 // Reads and clears the GEMM kernels' device error word (after the caller

@@ -79,6 +79,28 @@ def test_workspace_queries(lib):
     assert lib.qmm_workspace_bytes(1, 1, 1, 64, 3) == bad        # more slices than blocks
 
 
+def test_q8_0_weight_entry_points(lib):
+    A16 = _p(0x10000)  # never dereferenced: every call below fails its host checks
+    A2 = _p(0x10002)
+    # workspace queries: the Q4_0 formulas
+    assert lib.qmm_workspace_bytes(4, 2, 100, 4096, 4) == lib.qmm_workspace_bytes(1, 2, 100, 4096, 4)
+    assert lib.qmm_workspace_bytes(5, 512, 14336, 4096, 0) == lib.qmm_workspace_bytes(2, 512, 14336, 4096, 0)
+    assert lib.qmm_workspace_bytes(4, 17, 1, 32, 0) == ctypes.c_size_t(-1).value
+    # argument errors
+    assert lib.qmm_gemv_q8_0_q8_0(None, A16, A16, A16, A16, 1, 1, 32, 1, None, 0, None) == QMM_ERR_NULL
+    assert lib.qmm_gemv_q8_0_q8_0(A16, A16, A16, A16, A16, 17, 1, 32, 1, None, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemv_q8_0_q8_0(A16, A16, A16, A16, A16, 1, 1, 48, 1, None, 0, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemv_q8_0_q8_0(A2, A16, A16, A16, A16, 1, 1, 32, 1, None, 0, None) == QMM_ERR_ALIGN
+    assert lib.qmm_gemv_q8_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, 2, None, 0, None) == QMM_ERR_WORKSPACE
+    assert lib.qmm_gemv_q8_0_q8_0(A16, A16, A16, A16, A16, 1, 4, 64, 3, A16, 1 << 20, None) == QMM_ERR_ARG
+    assert lib.qmm_gemm_q8_0_q8_0(A16, A16, A16, None, A16, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_NULL
+    assert lib.qmm_gemm_q8_0_q8_0(A16, A16, A16, A16, A16, 1, 1, 40, A16, 1 << 20, None) == QMM_ERR_SHAPE
+    assert lib.qmm_gemm_q8_0_q8_0(A16, A16, A2, A16, A16, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_ALIGN
+    assert lib.qmm_gemm_q8_0_q8_0(A16, A16, A16, A16, A16, 4, 4, 32, A16, 16, None) == QMM_ERR_WORKSPACE
+    assert lib.qmm_debug_block_sums_q8_0_q8_0(2, A16, A16, A16, 1, 1, 32, None, 0, None) == QMM_ERR_ARG
+    assert lib.qmm_debug_block_sums_q8_0_q8_0(0, A16, A16, None, 1, 1, 32, None, 0, None) == QMM_ERR_NULL
+
+
 def test_auto_split_policy(lib):
     # a narrow output with a long reduction is split, a wide one is not
     assert lib.qmm_gemv_auto_split(1, 256, 16384) > 1

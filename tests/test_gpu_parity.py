@@ -191,6 +191,84 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
 # ---------------------------------------------------------------------------
 # BitNet prefill on the tensor cores
 
+# ---------------------------------------------------------------------------
+# Q8_0 weights x Q8_0 activations (GEMV and tensor-core GEMM)
+
+def q8_case(orc, seed, m, n, k):
+    """Oracle-quantized Q8_0 weights (the activation recipe) and activations."""
+    w, x = synthetic.q4_0_case(seed, n, k, m)
+    w = w.copy()
+    w[0, :QK] = 0.0  # an all-zero weight block: d = 0, codes 0
+    w8, wd = orc.quantize_q8_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    return w8, wd, aq, ad
+
+
+def test_quantize_weight_q8_0_is_the_activation_recipe(qmm, orc):
+    w, _ = synthetic.q4_0_case(31, 37, 4096, 1)
+    w8_ref, wd_ref = orc.quantize_q8_0(w)
+    w8, wd = qmm.quantize_weight_q8_0(to_dev(w))
+    assert np.array_equal(to_np(w8), w8_ref)
+    assert np.array_equal(f16_bits(wd), wd_ref)
+
+
+@pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
+def test_gemv_q8_0_block_sums_bit_exact(qmm, orc, m, n, k):
+    w8, wd, aq, ad = q8_case(orc, 6000 + m * 7 + n, m, n, k)
+    ref = orc.block_sums_q8_0(w8, aq)
+    got = qmm.debug_block_sums_q8(0, to_dev(w8), to_dev(aq))
+    assert np.array_equal(to_np(got), ref)
+
+
+@pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
+@pytest.mark.parametrize("split", [1, 0, 3])
+def test_gemv_q8_0_matches_oracle(qmm, orc, m, n, k, split):
+    if split > k // QK:
+        pytest.skip("more slices than blocks")
+    w8, wd, aq, ad = q8_case(orc, 6500 + m * 7 + n, m, n, k)
+    y_ref = orc.gemm_q8_0_q8_0(w8, wd, aq, ad)
+    _, absterms = orc.gemm_q8_0_q8_0_f64(w8, wd, aq, ad)
+    y = qmm.gemv_q8_0_q8_0(to_dev(w8), to_dev(wd.view(np.float16)), to_dev(aq),
+                           to_dev(ad.view(np.float16)), split_k=split)
+    ok, worst, maxrel = rel_gate(to_np(y), y_ref, absterms)
+    assert ok, (worst, maxrel)
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
+def test_gemm_q8_0_block_sums_bit_exact(qmm, orc, m, n, k):
+    w8, wd, aq, ad = q8_case(orc, 7000 + m + n, m, n, k)
+    ref = orc.block_sums_q8_0(w8, aq)
+    got = qmm.debug_block_sums_q8(1, to_dev(w8), to_dev(aq))
+    assert np.array_equal(to_np(got), ref)
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
+def test_gemm_q8_0_is_bit_identical_to_serial_order(qmm, orc, m, n, k):
+    """The Q8_0-weight GEMM accumulates fma(sumi, dw*da, acc) over blocks in
+    ascending order, the oracle's order: identical f32 bits (so the 1e-5
+    gate holds a fortiori)."""
+    w8, wd, aq, ad = q8_case(orc, 7500 + m + n, m, n, k)
+    y_ref = orc.gemm_q8_0_q8_0(w8, wd, aq, ad)
+    y = to_np(qmm.gemm_q8_0_q8_0(to_dev(w8), to_dev(wd.view(np.float16)), to_dev(aq),
+                                 to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
+def test_gemm_and_gemv_q8_0_agree_with_adversarial_activations(qmm, orc):
+    m, n, k = 9, 200, 4096
+    w, _ = synthetic.q4_0_case(63, n, k, 1)
+    x = adversarial_x(64, m, k)
+    w8, wd = orc.quantize_q8_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    y_ref = orc.gemm_q8_0_q8_0(w8, wd, aq, ad)
+    _, absterms = orc.gemm_q8_0_q8_0_f64(w8, wd, aq, ad)
+    args = (to_dev(w8), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    y_gemm = to_np(qmm.gemm_q8_0_q8_0(*args))
+    assert np.array_equal(y_gemm.view(np.uint32), y_ref.view(np.uint32))
+    ok, worst, maxrel = rel_gate(to_np(qmm.gemv_q8_0_q8_0(*args)), y_ref, absterms)
+    assert ok, (worst, maxrel)
+
+
 BITNET_GEMM_SHAPES = [(1, 1, 64), (17, 130, 256), (100, 300, 2560), (256, 128, 512),
                       (300, 257, 1024), (600, 1000, 128)]
 
