@@ -461,7 +461,9 @@ def run_q8_gemv(q, steps, warmup, dist, peaks):
     return {"workload": "Q8_0xQ8_0 GEMV m=1 K=4096 N=4096 (seed 0; Q8_0 weights)",
             "value": round(gbs, 1), "unit": "GB/s",
             "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "traffic": recorded_traffic("gemv_q8_0_q8_0_kernel<1,2,0>"),
+            "algorithmic_bytes_per_launch": nbytes}
 
 
 def run_q8_prefill(q, steps, warmup, dist, peaks):
@@ -485,7 +487,8 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
                         "(seed 11; Q8_0 weights)",
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64>")}
 
 
 def run_bitnet(q, steps, warmup, dist, peaks):
@@ -565,7 +568,7 @@ def run_prefill(q, steps, warmup, dist, peaks):
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): the block sums run "
                          "on tcgen05 kind::f16 because sm_103a has no int8 MMA",
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
-            "traffic": recorded_traffic("gemm_q4_0_q8_0_kernel<128,0>"),
+            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32>"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
                             "(profiles/traffic.txt); algorithmic: 33.0 MB weights + 2.1 MB "
                             "activations + 29.4 MB y (y is written back from L2 after the "
