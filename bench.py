@@ -373,21 +373,26 @@ def run_layer_set(q, args, dist, peaks):
         "value": gbs(ms_g, gemv_step_bytes), "unit": "GB/s",
         "bytes": "weights + Q8_0 activations + f32 y", "ms_per_step": round(ms_g / args.steps, 6)}
 
-    # end to end through the public Python API, eager calls: pinned host x in,
-    # host y out, every step
-    xs_h = [torch.from_numpy(mt["x_host"]).pin_memory() for mt in mats]
-    ys_h = [torch.empty((1, mt["n"]), dtype=torch.float32).pin_memory() for mt in mats]
+    # end to end through the public Python API, eager calls: the 7 activation
+    # rows in one pinned host buffer go in with one copy, one prepared grouped
+    # call runs the step, and the 7 outputs (one device buffer) come back with
+    # one copy, every step
+    k_off = [int(v) for v in np.cumsum([0] + [k for _, k in LAYER_SET])]
+    n_off = [int(v) for v in np.cumsum([0] + [n for n, _ in LAYER_SET])]
+    x_h = torch.from_numpy(np.concatenate([mt["x_host"].ravel() for mt in mats])).pin_memory()
+    y_h = torch.empty((n_off[-1],), dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x_h, device="cuda")
+    y_d = torch.empty((n_off[-1],), dtype=torch.float32, device="cuda")
     e2e_steps = max(20, min(args.steps, 400))
-
-    e2e_tables = [[(mt["x"], *mt["wts"][c], mt["y"], mt["aq"], mt["ad"]) for mt in mats]
-                  for c in range(rot)]
+    calls = [q.GroupedLinear([(x_d[k_off[j]:k_off[j + 1]].view(1, -1), *mt["wts"][c],
+                               y_d[n_off[j]:n_off[j + 1]].view(1, -1), mt["aq"], mt["ad"])
+                              for j, mt in enumerate(mats)], pdl=True)
+             for c in range(rot)]
 
     def e2e_step(i):
-        for j, mt in enumerate(mats):
-            mt["x"].copy_(xs_h[j], non_blocking=True)
-        q.linear_q4_0_grouped(e2e_tables[i % rot], pdl=True)
-        for j, mt in enumerate(mats):
-            ys_h[j].copy_(mt["y"], non_blocking=True)
+        x_d.copy_(x_h, non_blocking=True)
+        calls[i % rot]()
+        y_h.copy_(y_d, non_blocking=True)
 
     for i in range(max(3, min(args.warmup, 50))):
         e2e_step(i)
@@ -401,9 +406,10 @@ def run_layer_set(q, args, dist, peaks):
     e2e = {"value": round(dist.world * step_bytes * e2e_steps / e2e_s / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * k for _, k in LAYER_SET),
            "d2h_bytes_per_step": sum(4 * n for n, _ in LAYER_SET),
-           "steps": e2e_steps, "path": "eager Python API calls: 7 pinned host->device copies "
-                                       "of x, linear_q4_0_grouped (PDL), 7 device->host copies "
-                                       "of y"}
+           "steps": e2e_steps, "path": "eager Python API calls per step: one pinned "
+                                       "host->device copy of the 7 activation rows, one "
+                                       "prepared grouped call (GroupedLinear, PDL), one "
+                                       "device->host copy of the 7 outputs"}
     return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e,
                 launches=2 * args.steps, rot=rot, set_bytes=set_bytes,
                 step_bytes=step_bytes, variants=variants)

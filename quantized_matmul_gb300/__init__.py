@@ -325,6 +325,40 @@ def linear_q4_0_grouped(problems, pdl: bool = False):
     problems: a list of (x, wq, wd) or (x, wq, wd, y, aq, ad) tuples (missing
     outputs are allocated).  Returns the list of (y, aq, ad).  Each result is
     bit for bit that of linear_q4_0 on the problem alone."""
+    table, m, outs = _grouped_table(problems)
+    st = load().qmm_linear_q4_0_grouped(ctypes.addressof(table), len(problems), m,
+                                        LINEAR_PDL if pdl else 0, _stream())
+    _check(st, "qmm_linear_q4_0_grouped")
+    return outs
+
+
+class GroupedLinear:
+    """A prepared linear_q4_0_grouped call for a decode loop.
+
+    The problem table is built and checked once, here; each call then only
+    enqueues the two launches on the current stream with one ctypes call.
+    The tensors given (and the outputs allocated here) are used in place on
+    every call: keep them alive and write new activations into the same x
+    tensors between calls.  `outputs` is the list of (y, aq, ad)."""
+
+    def __init__(self, problems, pdl: bool = False):
+        self._table, self._m, self.outputs = _grouped_table(problems)
+        self._keep = [tuple(p) for p in problems]  # the tensors the table points at
+        self._count = len(problems)
+        self._flags = LINEAR_PDL if pdl else 0
+        self._fn = load().qmm_linear_q4_0_grouped
+        self._addr = ctypes.addressof(self._table)
+
+    def __call__(self):
+        st = self._fn(self._addr, self._count, self._m, self._flags, _stream())
+        if st != 0:
+            raise QmmError(st, "qmm_linear_q4_0_grouped")
+        return self.outputs
+
+
+def _grouped_table(problems):
+    """The qmm_linear_problem table for a list of problems (checked), the
+    common m, and the (y, aq, ad) of every problem (allocated when missing)."""
     torch = _torch()
     if not 1 <= len(problems) <= GROUP_MAX:
         raise ValueError(f"1..{GROUP_MAX} problems, got {len(problems)}")
@@ -352,10 +386,7 @@ def linear_q4_0_grouped(problems, pdl: bool = False):
                                  _dev(ad, torch.float16, "ad", (m, k // QK)),
                                  _dev(y, torch.float32, "y", (m, n)), n, k)
         outs.append((y, aq, ad))
-    st = load().qmm_linear_q4_0_grouped(ctypes.addressof(table), len(problems), m,
-                                        LINEAR_PDL if pdl else 0, _stream())
-    _check(st, "qmm_linear_q4_0_grouped")
-    return outs
+    return table, m, outs
 
 
 # ---------------------------------------------------------------------------

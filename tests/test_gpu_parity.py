@@ -460,6 +460,28 @@ def test_linear_grouped_matches_single_calls_and_oracle(qmm, orc, m, pdl, shapes
         assert ok, (worst, maxrel)
 
 
+def test_prepared_grouped_linear_matches_the_one_shot_call(qmm, orc):
+    """GroupedLinear builds the table once; every call then gives the bits of
+    linear_q4_0_grouped, and reads the x tensors' current contents."""
+    import torch
+    shapes = [(300, 4096), (77, 1024), (129, 11008)]
+    probs, refs = [], []
+    for j, (n, k) in enumerate(shapes):
+        w, x = synthetic.q4_0_case(900 + j, n, k, 1)
+        wq, wd = orc.quantize_q4_0(w)
+        probs.append((to_dev(x), to_dev(wq), to_dev(wd.view(np.float16))))
+    once = qmm.linear_q4_0_grouped(probs, pdl=True)
+    call = qmm.GroupedLinear(probs, pdl=True)
+    for (y1, aq1, ad1), (y2, aq2, ad2) in zip(once, call()):
+        assert torch.equal(y1, y2) and torch.equal(aq1, aq2) and torch.equal(ad1, ad2)
+    # new activations written in place are picked up by the next call
+    for j, (x, _, _) in enumerate(probs):
+        x.mul_(-0.5)
+    again = qmm.linear_q4_0_grouped([(x, wq, wd) for x, wq, wd in probs], pdl=False)
+    for (y1, _, _), (y2, _, _) in zip(again, call()):
+        assert torch.equal(y1, y2)
+
+
 def test_linear_grouped_full_table(qmm, orc):
     """A table of QMM_GROUP_MAX problems, all of one tiny shape."""
     probs, refs = [], []
