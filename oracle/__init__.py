@@ -71,6 +71,8 @@ def _load():
                 "orc_block_sums_q8_0_q8_0": (None, [P, P, I, I, I, P]),
                 "orc_gemm_q8_0_q8_0": (None, [P, P, P, P, I, I, I, P]),
                 "orc_gemm_q8_0_q8_0_f64": (None, [P, P, P, P, I, I, I, P, P]),
+                "orc_repack_q4_0_gemm": (None, [P, I, I, P]),
+                "orc_unrepack_q4_0_gemm": (None, [P, I, I, P]),
                 "orc_q4_0_blocks_to_planes": (None, [P, I, I, P, P]),
                 "orc_q4_0_planes_to_blocks": (None, [P, P, I, I, P]),
                 "orc_quantize_act_bitnet": (None, [P, I, I, P, P, P]),
@@ -208,6 +210,27 @@ def q4_0_planes_to_blocks(wq, wd) -> np.ndarray:
     n, k = wq.shape[0], wq.shape[1] * 2
     out = np.empty(n * (k // QK) * 18, np.uint8)
     _load().orc_q4_0_planes_to_blocks(_p(wq), _p(wd), n, k, _p(out))
+    return out
+
+
+def repack_q4_0_gemm_bytes(n: int, k: int) -> int:
+    return ((n + 127) // 128) * ((k // QK + 1) // 2) * 4096
+
+
+def repack_q4_0_gemm(wq) -> np.ndarray:
+    """Q4_0 nibble plane [n, k/2] -> the GEMM tile order (uint8, flat)."""
+    wq = _c(wq, np.uint8)
+    n, k = wq.shape[0], wq.shape[1] * 2
+    out = np.empty(repack_q4_0_gemm_bytes(n, k), np.uint8)
+    _load().orc_repack_q4_0_gemm(_p(wq), n, k, _p(out))
+    return out
+
+
+def unrepack_q4_0_gemm(wr, n: int, k: int) -> np.ndarray:
+    wr = _c(wr, np.uint8)
+    assert wr.size == repack_q4_0_gemm_bytes(n, k)
+    out = np.zeros((n, k // 2), np.uint8)
+    _load().orc_unrepack_q4_0_gemm(_p(wr), n, k, _p(out))
     return out
 
 

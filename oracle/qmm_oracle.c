@@ -48,6 +48,13 @@
  *   R9 the f32 output accumulates blocks in ascending order:
  *      acc = fmaf((float)sumi, f32(dw)*f32(da), acc), acc starting at +0.
  *  R10 BitNet y = ((float)dot * absmean) / scale, left to right in f32.
+ *  R18 the load-time repack of Q4_0 nibbles for the tensor-core GEMM is a
+ *      pure byte/nibble permutation (no value changes): tiles of 128 rows x
+ *      2 blocks, each 4096 contiguous bytes; inside a tile, unit u = 2*r +
+ *      blk (row r, block blk) holds the block's 32 nibbles in 16 bytes as 4
+ *      words; word c carries elements 8c..8c+7, element 8c + 2i + h at bits
+ *      4i + 16h (i = 0..3, h = 0..1).  Rows past n and blocks past k/32 are
+ *      nibble 8 (value 0).
  *  R16 Q8_0 weights use the Q8_0 activation block and recipe unchanged: per
  *      32-block d = absmax/127, q = clamp(round(w/d), -127, 127), fp16(d)
  *      stored; the block dot is sum_j q_w * q_a (no offset) and y follows R9.
@@ -57,6 +64,7 @@
  *   aq  int8 [m, k]            ad fp16 bits [m, k/32]
  *   wq  u8   [n, k/2]          wd fp16 bits [n, k/32]   (two planes of block_q4_0)
  *   w8  int8 [n, k]            wd fp16 bits [n, k/32]   (two planes of Q8_0 weight blocks)
+ *   wr  u8   [ceil(n/128), ceil(k/64), 4096]   (Q4_0 nibbles in GEMM tile order, R18)
  *   y   f32  [m, n]
  *   sumi int32 [m, n, k/32]
  *   tw  u32  [n, k/16]         (ternary, 16 codes per word)
@@ -368,6 +376,58 @@ void orc_gemm_q8_0_q8_0_f64(const int8_t *w8, const uint16_t *wd,
             }
             y[i * n + r] = acc;
             absterms[i * n + r] = abs_acc;
+        }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Load-time repack of Q4_0 nibbles into the GEMM's tile order, reading R18
+ * (Fucina reference, section 9.7: weights packed once at load time into the
+ * kernel's interleaved layout).  wr holds ceil(n/128) * ceil(k/64) tiles of
+ * 4096 bytes. */
+static int64_t orc_repack_offset(int64_t n_tiles_k, int64_t r, int64_t b, int e, int *shift)
+{
+    int64_t g = r / 128, rr = r % 128, j = b / 2;
+    int blk = (int)(b % 2);
+    int64_t unit = 2 * rr + blk;
+    int c = e / 8, i = (e % 8) / 2, h = e % 2;
+    int bit = 4 * i + 16 * h;        /* bit inside word c */
+    *shift = bit % 8;
+    return (g * n_tiles_k + j) * 4096 + unit * 16 + c * 4 + bit / 8;
+}
+
+void orc_repack_q4_0_gemm(const uint8_t *wq, int64_t n, int64_t k, uint8_t *wr)
+{
+    int64_t kb = k / ORC_QK;
+    int64_t tiles_n = (n + 127) / 128, tiles_k = (kb + 1) / 2;
+    int64_t bytes = tiles_n * tiles_k * 4096;
+    for (int64_t i = 0; i < bytes; i++) wr[i] = 0x88;  /* nibble 8 everywhere */
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < kb; b++)
+            for (int e = 0; e < ORC_QK; e++) {
+                int shift;
+                int64_t off = orc_repack_offset(tiles_k, r, b, e, &shift);
+                int v = orc_q4_nibble(wq + r * (k / 2) + b * (ORC_QK / 2), e);
+                wr[off] = (uint8_t)((wr[off] & ~(0x0f << shift)) | (v << shift));
+            }
+}
+
+/* The inverse, for the round-trip pin: planes wq [n, k/2] from wr. */
+void orc_unrepack_q4_0_gemm(const uint8_t *wr, int64_t n, int64_t k, uint8_t *wq)
+{
+    int64_t kb = k / ORC_QK;
+    int64_t tiles_k = (kb + 1) / 2;
+    for (int64_t r = 0; r < n; r++)
+        for (int64_t b = 0; b < kb; b++) {
+            uint8_t *qs = wq + r * (k / 2) + b * (ORC_QK / 2);
+            for (int e = 0; e < ORC_QK; e++) {
+                int shift;
+                int64_t off = orc_repack_offset(tiles_k, r, b, e, &shift);
+                int v = (wr[off] >> shift) & 0x0f;
+                if (e < ORC_QK / 2)
+                    qs[e] = (uint8_t)((qs[e] & 0xf0) | v);
+                else
+                    qs[e - ORC_QK / 2] = (uint8_t)((qs[e - ORC_QK / 2] & 0x0f) | (v << 4));
+            }
         }
 }
 

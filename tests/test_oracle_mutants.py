@@ -100,6 +100,16 @@ MUTANTS = [
      "double t = (double)s * (double)orc_fp16_to_fp32(wd[r * kb + (b + 1) % kb])", 1),
     ("q8w_absterms_signed",
      "abs_acc += fabs(t);", "abs_acc += t;", 1),
+    # load-time repack for the GEMM
+    ("repack_halves_swapped",
+     "int bit = 4 * i + 16 * h;", "int bit = 4 * i + 16 * (1 - h);", 1),
+    ("repack_stages_reversed",  # (every planted mistake stays inside the buffers)
+     "return (g * n_tiles_k + j) * 4096 + unit * 16 + c * 4 + bit / 8;",
+     "return (g * n_tiles_k + (n_tiles_k - 1 - j)) * 4096 + unit * 16 + c * 4 + bit / 8;", 1),
+    ("repack_unit_row_major",
+     "int64_t unit = 2 * rr + blk;", "int64_t unit = rr + 128 * blk;", 1),
+    ("repack_pads_with_zero_nibbles",
+     "for (int64_t i = 0; i < bytes; i++) wr[i] = 0x88;", "for (int64_t i = 0; i < bytes; i++) wr[i] = 0x00;", 1),
 ]
 
 PIN_FUNCS = [getattr(pins, n) for n in dir(pins)

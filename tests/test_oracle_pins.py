@@ -202,6 +202,57 @@ def test_row_independence(orc):
 
 
 # ---------------------------------------------------------------------------
+# load-time repack of Q4_0 nibbles for the tensor-core GEMM (the layout the
+# GEMM's converter decodes with shifts and masks only)
+
+def _decode_repacked(wr, n, k):
+    """Read every element back the way the GEMM converter does: tile
+    (row group, 2-block stage) of 4096 bytes, unit 2*row + block of 16 bytes,
+    word c holding elements 8c..8c+7, (word >> 4i) & 0x000F000F giving
+    elements 8c+2i and 8c+2i+1 in the low and high 16-bit halves."""
+    kb = k // QK
+    tiles_k = (kb + 1) // 2
+    words = wr.view(np.uint32)
+    out = np.zeros((n, k), np.int64)
+    for r in range(n):
+        for b in range(kb):
+            tile = (r // 128) * tiles_k + b // 2
+            unit = 2 * (r % 128) + b % 2
+            base = (tile * 4096 + unit * 16) // 4
+            for c in range(4):
+                w = int(words[base + c])
+                for i in range(4):
+                    pair = (w >> (4 * i)) & 0x000F000F
+                    out[r, b * QK + 8 * c + 2 * i] = pair & 0xF
+                    out[r, b * QK + 8 * c + 2 * i + 1] = pair >> 16
+    return out
+
+
+def test_repack_decodes_with_shifts_and_masks(orc):
+    rng = np.random.default_rng(9)
+    for (n, k) in [(1, 32), (3, 96), (130, 64), (129, 160)]:
+        wq = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+        wr = orc.repack_q4_0_gemm(wq)
+        assert wr.size == ((n + 127) // 128) * ((k // QK + 1) // 2) * 4096
+        assert np.array_equal(_decode_repacked(wr, n, k), unpack_q4_0(wq)), (n, k)
+        assert np.array_equal(orc.unrepack_q4_0_gemm(wr, n, k), wq)
+
+
+def test_repack_pads_with_value_zero(orc):
+    """Rows past n and the block past an odd k/32 hold nibble 8 (value 0)."""
+    n, k = 3, 96  # 3 blocks: the second stage has one block; 125 padding rows
+    wq = np.zeros((n, k // 2), np.uint8)  # every real nibble 0
+    wr = orc.repack_q4_0_gemm(wq)
+    words = wr.view(np.uint32).reshape(-1, 4096 // 4)
+    real = np.zeros(words.shape, bool)
+    for r in range(n):
+        for b in range(k // QK):
+            unit = 2 * r + b % 2
+            real[b // 2, unit * 4:unit * 4 + 4] = True
+    assert (words[real] == 0).all() and (words[~real] == 0x88888888).all()
+
+
+# ---------------------------------------------------------------------------
 # Q8_0 weights x Q8_0 activations (the same block on both sides)
 
 def test_q8_0_weight_hand_block(orc):
