@@ -434,6 +434,33 @@ def run_single_gemv(q, steps, warmup, dist, peaks):
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
 
 
+def run_prefill_repacked(q, steps, warmup, dist, peaks):
+    """The prefill workload on Q4_0 weights repacked at load time."""
+    import torch
+    m, n, k = 512, 14336, 4096
+    rot = copies_for(q4_weight_bytes(n, k) + m * k)
+    wts, x = _quantized_weights(q, 11, n, k, m, rot, outlier_p=0.01)
+    reps = [(q.repack_q4_0_gemm(wq), wd) for wq, wd in wts]
+    del wts
+    aq, ad = q.quantize_act_q8_0(_up(x))
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    ws = torch.empty((q.workspace_bytes(q.OP_GEMM, m, n, k),), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        wr, wd = reps[i % rot]
+        q.gemm_q4_0_q8_0_repacked(wr, wd, aq, ad, y=y, workspace=ws)
+
+    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"workload": "Q4_0xQ8_0 prefill GEMM m=512 K=4096 N=14336, 1% outliers x20 "
+                        "(seed 11; weights repacked at load time)",
+            "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
+            "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,1>")}
+
+
 def q8_weight_bytes(n, k):
     return n * k + 2 * n * (k // QK)
 
@@ -494,7 +521,7 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
-            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64>")}
+            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64,0>")}
 
 
 def run_bitnet(q, steps, warmup, dist, peaks):
@@ -574,7 +601,7 @@ def run_prefill(q, steps, warmup, dist, peaks):
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): the block sums run "
                          "on tcgen05 kind::f16 because sm_103a has no int8 MMA",
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
-            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32>"),
+            "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,0>"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
                             "(profiles/traffic.txt); algorithmic: 33.0 MB weights + 2.1 MB "
                             "activations + 29.4 MB y (y is written back from L2 after the "
@@ -697,7 +724,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
     ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill",
-                                       "q8_gemv", "q8_prefill"],
+                                       "q8_gemv", "q8_prefill", "prefill_repacked"],
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
@@ -722,7 +749,9 @@ def main():
                    "bitnet_prefill": lambda: run_bitnet_prefill(q, args.steps, args.warmup, dist,
                                                                 peaks),
                    "q8_gemv": lambda: run_q8_gemv(q, args.steps, args.warmup, dist, peaks),
-                   "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks)}
+                   "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks),
+                   "prefill_repacked": lambda: run_prefill_repacked(q, args.steps, args.warmup,
+                                                                    dist, peaks)}
             res = run[args.only]()
             if dist.rank == 0:
                 print(json.dumps({"only": args.only, "result": res}), flush=True)
@@ -737,6 +766,8 @@ def main():
             configs["bitnet_prefill_2048x6912x2560"] = run_bitnet_prefill(q, max(50, short // 20),
                                                                           10, dist, peaks)
             configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks)
+            configs["prefill_repacked_512x14336x4096"] = run_prefill_repacked(
+                q, max(50, short // 20), 10, dist, peaks)
             configs["q8_0_gemv_4096x4096"] = run_q8_gemv(q, short * 5, args.warmup, dist, peaks)
             configs["q8_0_prefill_512x14336x4096"] = run_q8_prefill(q, max(50, short // 20), 10,
                                                                     dist, peaks)

@@ -211,6 +211,33 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* Load-time repack of Q4_0 weights for the prefill GEMM (Fucina reference,
+ * section 9.7: weights are packed once, at load time, into the layout the
+ * kernel reads).  A pure permutation of the nibble plane wq [n, k/2]:
+ * ceil(n/128) * ceil(k/64) tiles of 4096 bytes, tile (g, j) for rows
+ * 128g..128g+127 and blocks 2j, 2j+1, at byte (g * ceil(k/64) + j) * 4096.
+ * Inside a tile, 16-byte unit u = 2 * row + block holds one block as four
+ * 32-bit words; word c carries elements 8c..8c+7, element 8c + 2i + h at
+ * bits 4i + 16h, so (word >> 4i) & 0x000F000F yields a pair of elements in
+ * the two 16-bit halves.  Rows past n and the block past an odd k/32 hold
+ * nibble 8 (value 0).  The scales wd are not repacked.
+ *   qmm_repack_q4_0_gemm_bytes: size of wr (SIZE_MAX for a bad shape).
+ *   wq, wr 16-byte aligned; k % 32 == 0. */
+size_t qmm_repack_q4_0_gemm_bytes(int64_t n, int64_t k);
+qmm_status qmm_repack_q4_0_gemm(const uint8_t *wq, int64_t n, int64_t k, uint8_t *wr,
+                                size_t wr_bytes, void *stream);
+
+/* qmm_gemm_q4_0_q8_0 on repacked weights: identical results, bit for bit.
+ * Each pipeline stage's weight tile then arrives as one contiguous bulk copy
+ * and unpacks with shifts and masks only.  wr of at least
+ * qmm_repack_q4_0_gemm_bytes(n, k) bytes, 16-byte aligned; other arguments
+ * as for qmm_gemm_q4_0_q8_0. */
+qmm_status qmm_gemm_q4_0_q8_0_repacked(const uint8_t *wr, size_t wr_bytes, const uint16_t *wd,
+                                       const int8_t *aq, const uint16_t *ad, float *y,
+                                       int64_t m, int64_t n, int64_t k,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* Q8_0 weights x Q8_0 activations.  The Q8_0 block (lesson 31: 32 int8 codes
  * and one fp16 scale) also serves as a weight format (Fucina reference,
  * section 9: the Q8_0 right-hand side of 9.2 and 9.7, Q8_0 decode and
@@ -314,7 +341,8 @@ int qmm_version(void);
 
 /* Per-block sums sumi int32 [m, n, k/32] = sum_j (nibble_j - 8) * q_j.
  * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the tensor-
- * core GEMM kernel (needs the GEMM workspace).  Same alignment rules as the
+ * core GEMM kernel (needs the GEMM workspace); path 2: the GEMM on repacked
+ * weights (wq then points at the repacked tiles, see qmm_repack_q4_0_gemm).  Same alignment rules as the
  * product entry points; sumi 4-byte aligned. */
 qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int8_t *aq,
                                           int32_t *sumi, int64_t m, int64_t n, int64_t k,

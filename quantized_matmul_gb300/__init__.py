@@ -63,6 +63,9 @@ def load() -> ctypes.CDLL:
             "qmm_gemm_q4_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_gemv_q4_0_q8_0_noalloc": (I, [P, P, P, P, P, I64, I64, I64, I, P]),
             "qmm_gemv_q8_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, I, P, SZ, P]),
+            "qmm_repack_q4_0_gemm_bytes": (SZ, [I64, I64]),
+            "qmm_repack_q4_0_gemm": (I, [P, I64, I64, P, SZ, P]),
+            "qmm_gemm_q4_0_q8_0_repacked": (I, [P, SZ, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_gemm_q8_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_linear_q4_0": (I, [P, P, P, I64, P, P, P, I64, I64, I64, I, P]),
             "qmm_linear_q4_0_grouped": (I, [P, I, I64, I, P]),
@@ -274,6 +277,40 @@ def gemm_q8_0_q8_0(w8, wd, aq, ad, y=None, workspace=None):
     return y
 
 
+def repack_q4_0_gemm(wq):
+    """Load-time repack of the Q4_0 nibble plane [n, k/2] into the GEMM's tile
+    order (uint8, flat; see qmm_repack_q4_0_gemm in include/qmm.h)."""
+    torch = _torch()
+    n, k = wq.shape[0], wq.shape[1] * 2
+    nbytes = load().qmm_repack_q4_0_gemm_bytes(n, k)
+    if nbytes == ctypes.c_size_t(-1).value:
+        raise ValueError(f"invalid shape n={n} k={k}")
+    wr = _empty((nbytes,), torch.uint8, wq)
+    st = load().qmm_repack_q4_0_gemm(_dev(wq, torch.uint8, "wq"), n, k, wr.data_ptr(), nbytes,
+                                     _stream())
+    _check(st, "qmm_repack_q4_0_gemm")
+    return wr
+
+
+def gemm_q4_0_q8_0_repacked(wr, wd, aq, ad, y=None, workspace=None):
+    """The prefill GEMM on repacked weights (bit for bit gemm_q4_0_q8_0)."""
+    torch = _torch()
+    n = wd.shape[0]
+    m, k = aq.shape
+    _dev(wd, torch.float16, "wd", (n, k // QK))
+    _dev(aq, torch.int8, "aq", (m, k))
+    _dev(ad, torch.float16, "ad", (m, k // QK))
+    y = _empty((m, n), torch.float32, aq) if y is None else y
+    ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM, m, n, k), aq)
+    st = load().qmm_gemm_q4_0_q8_0_repacked(_dev(wr, torch.uint8, "wr"), wr.numel(), wd.data_ptr(),
+                                            aq.data_ptr(), ad.data_ptr(),
+                                            _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                            ws.data_ptr() if ws is not None else None, ws_bytes,
+                                            _stream())
+    _check(st, "qmm_gemm_q4_0_q8_0_repacked")
+    return y
+
+
 LINEAR_PDL = 1
 GROUP_MAX = 16
 
@@ -460,16 +497,21 @@ def check_device_error() -> int:
     return int(load().qmm_check_device_error(_stream()))
 
 
-def debug_block_sums(path: int, wq, aq, workspace=None):
-    """int32 [m, n, k/32] block sums from the GEMV (path 0) or GEMM (path 1) kernel."""
+def debug_block_sums(path: int, wq, aq, workspace=None, n=None):
+    """int32 [m, n, k/32] block sums from the GEMV (path 0) or GEMM (path 1)
+    kernel, or the GEMM on repacked weights (path 2: wq is the repacked
+    tile array and n must be given)."""
     torch = _torch()
-    n = wq.shape[0]
     m, k = aq.shape
-    _dev(wq, torch.uint8, "wq", (n, k // 2))
+    if path == 2:
+        _dev(wq, torch.uint8, "wr")
+    else:
+        n = wq.shape[0]
+        _dev(wq, torch.uint8, "wq", (n, k // 2))
     _dev(aq, torch.int8, "aq", (m, k))
     sumi = _empty((m, n, k // QK), torch.int32, aq)
     ws, ws_bytes = (None, 0)
-    if path == 1:
+    if path in (1, 2):
         ws, ws_bytes = _workspace(workspace, workspace_bytes(OP_GEMM, m, n, k), aq)
     st = load().qmm_debug_block_sums_q4_0_q8_0(path, wq.data_ptr(), aq.data_ptr(), sumi.data_ptr(),
                                                m, n, k, ws.data_ptr() if ws is not None else None,

@@ -10,6 +10,11 @@
 // a weight format too) the weight values are the 32 int8 codes of the block
 // (|sumi| <= 32 * 127 * 127 < 2^24); only the weight tile and its converter
 // differ (template parameter WB, the weight bytes per row and stage).
+// Q4_0 weights repacked at load time into the tile order (template flag RP;
+// Fucina reference, section 9.7, packs weights once into the kernel's
+// interleaved layout) arrive as one contiguous 4 KB bulk copy per stage, and
+// the converter decodes each word with one shift and masks.  (A tile is 16
+// rows of 256 bytes in the copy's 2-D view.)
 //
 // How (GB300, sm_103a).  There is no int8 MMA on sm_103a, but every operand
 // value is a small integer that fp16 holds exactly (weights -8..7,
@@ -183,6 +188,28 @@ __device__ __forceinline__ void unpack_block_f16(uint4 v, uint4 (&out)[4]) {
     out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);  // elements 24..31
 }
 
+// One repacked Q4_0 block (16 bytes, word c carrying elements 8c..8c+7 with
+// element 8c + 2i + h at bits 4i + 16h) -> 32 fp16 values (nibble - 8).  The
+// pairs at bits 0-3/16-19 and 8-11/24-27 (after one 8-bit shift) become
+// (0x6400 | v) - 1032; the pairs at bits 4-7/20-23 and 12-15/28-31 become
+// (0x6400 | 16 v) / 16 - 72, with no shift: nine operations per word, all
+// exact.
+__device__ __forceinline__ void unpack_repacked_f16(uint4 v, uint4 (&out)[4]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const __half2 off = u32_as_h2(0x64086408u);        // (1032, 1032)
+    const __half2 sixteenth = u32_as_h2(0x2C002C00u);  // (1/16, 1/16)
+    const __half2 m72 = u32_as_h2(0xD480D480u);        // (-72, -72)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t w8 = w[c] >> 8;
+        out[c] = make_uint4(
+            h2_as_u32(__hsub2(u32_as_h2((w[c] & 0x000F000Fu) | 0x64006400u), off)),
+            h2_as_u32(__hfma2(u32_as_h2((w[c] & 0x00F000F0u) | 0x64006400u), sixteenth, m72)),
+            h2_as_u32(__hsub2(u32_as_h2((w8 & 0x000F000Fu) | 0x64006400u), off)),
+            h2_as_u32(__hfma2(u32_as_h2((w8 & 0x00F000F0u) | 0x64006400u), sixteenth, m72)));
+    }
+}
+
 // 32 int8 codes of one Q8_0 block (two 16-byte words, elements in order) ->
 // 32 fp16 values.  Exact: the fp16 pattern 0x6400 | u is 1024 + u for
 // u < 1024, and u = b ^ 0x80 = b + 128 for a signed byte b, so subtracting
@@ -243,14 +270,15 @@ struct Smem {
     static_assert(kOffB % 1024 == 0 && kB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 };
 
-template <int BN, bool EMIT, int WB>
+template <int BN, bool EMIT, int WB, bool RP>
 __global__ void __launch_bounds__(threads_for<BN, WB>(), ctas_per_sm<BN>())
 gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
                       const __grid_constant__ CUtensorMap tm_act,
                       const __grid_constant__ CUtensorMap tm_bs,
                       const unsigned short *__restrict__ wd, float *__restrict__ y,
                       int32_t *__restrict__ sumi, int m, int n, int kb_total, int m4,
-                      uint32_t wait_limit, int withhold_loads) {
+                      uint32_t wait_limit, int withhold_loads, const uint8_t *__restrict__ wr) {
+    static_assert(!RP || WB == 32, "the repacked layout holds Q4_0 nibbles");
     using S = Smem<BN, WB>;
     constexpr int kStages = S::kStages;
     constexpr int kNacc = S::kNacc;
@@ -318,7 +346,11 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
             if (lane == 0) {
                 const bool two = 2 * it + 1 < kb_total;
                 mbar_arrive_expect_tx(&bar_load[s], S::kTx - (two ? 0u : (uint32_t)(BN * 16)));
-                tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * WB, n0);
+                if constexpr (RP)  // tile (row group, stage): 4096 contiguous bytes = 16 map rows
+                    tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], 0,
+                                (int)(((int64_t)blockIdx.y * num_stages + it) * 16));
+                else
+                    tma_load_2d(smem + S::kOffNib + s * S::kNib, &tm_nib, &bar_load[s], it * WB, n0);
                 tma_load_2d(smem + S::kOffB + s * S::kB, &tm_act, &bar_load[s], it * kBK, t0);
                 uint8_t *bs = smem + S::kOffBs + s * S::kBs;
                 tma_load_2d(bs, &tm_bs, &bar_load[s], 0, (2 * it) * m4 + t0);
@@ -425,7 +457,9 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
                     const int u = 32 * (kBatch * g + i) + lane;
                     const int row = u >> 1, blk = u & 1;
                     uint4 out[4];
-                    if constexpr (WB == 32)
+                    if constexpr (RP)
+                        unpack_repacked_f16(v[i][0], out);
+                    else if constexpr (WB == 32)
                         unpack_block_f16(v[i][0], out);
                     else
                         unpack_block_q8_f16(v[i][0], v[i][WB / 32 - 1], out);
@@ -578,24 +612,24 @@ WsPlan plan_ws(int64_t m, int64_t k) {
 uint32_t g_wait_limit = kDefaultWaitLimit;
 int g_withhold_loads = 0;
 
-template <int BN, int WB>
+template <int BN, int WB, bool RP>
 cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CUtensorMap &bs,
                         const uint16_t *wd, float *y, int32_t *sumi, int64_t m, int64_t n,
-                        int64_t k, int64_t m4, cudaStream_t s) {
+                        int64_t k, int64_t m4, const uint8_t *wr, cudaStream_t s) {
     using S = Smem<BN, WB>;
     const int kb = (int)(k / kQK);
     dim3 grid((unsigned)((m + BN - 1) / BN), (unsigned)((n + kBM - 1) / kBM));
     const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
     if (sumi) {
-        auto kern = gemm_blocks_kernel<BN, true, WB>;
+        auto kern = gemm_blocks_kernel<BN, true, WB, RP>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
         kern<<<grid, threads_for<BN, WB>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
-                                                        (int)m4, g_wait_limit, g_withhold_loads);
+                                                        (int)m4, g_wait_limit, g_withhold_loads, wr);
     } else {
-        auto kern = gemm_blocks_kernel<BN, false, WB>;
+        auto kern = gemm_blocks_kernel<BN, false, WB, RP>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
         kern<<<grid, threads_for<BN, WB>(), S::kAlloc, s>>>(nib, act, bs, wdp, y, sumi, (int)m, (int)n, kb,
-                                                        (int)m4, g_wait_limit, g_withhold_loads);
+                                                        (int)m4, g_wait_limit, g_withhold_loads, wr);
     }
     return cudaPeekAtLastError();
 }
@@ -628,7 +662,7 @@ namespace {
 // Shared host path of both weight formats: prepass, tensor maps, launch.
 // WB = weight bytes per row and stage (32: Q4_0 nibbles [n, k/2]; 64: Q8_0
 // codes [n, k]).
-template <int WB>
+template <int WB, bool RP>
 cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, const uint16_t *ad,
                         float *y, int32_t *sumi, int64_t m, int64_t n, int64_t k, void *workspace,
                         cudaStream_t s) {
@@ -648,10 +682,18 @@ cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, con
     const int bn = choose_bn(m);
     const uint64_t row_bytes = (uint64_t)(k * WB / kBK);  // k/2 (Q4_0) or k (Q8_0)
     CUtensorMap tm_nib, tm_act, tm_bs;
-    // weights: u8 [n rows, row_bytes], box WB bytes x 128 rows
-    if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, (uint64_t)n, row_bytes,
-                     WB, kBM, CU_TENSOR_MAP_SWIZZLE_NONE))
+    // weights: u8 [n rows, row_bytes], box WB bytes x 128 rows; the repacked
+    // tiles as u8 [tiles * 16 rows, 256 bytes], box 256 x 16 (one tile)
+    if (RP) {
+        const uint64_t map_rows = (uint64_t)((n + kBM - 1) / kBM) * (uint64_t)((k / kQK + 1) / 2) * 16;
+        if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 256, map_rows, 256, 256, 16,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else if (!make_map_2d(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, (uint64_t)n,
+                            row_bytes, WB, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
+    }
+    const uint8_t *wr = RP ? static_cast<const uint8_t *>(w) : nullptr;
     // activations: fp16 [m rows, k], box 64 x BN, 128-byte swizzle
     if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, (uint64_t)k, (uint64_t)m,
                      (uint64_t)k * 2, kBK, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -661,10 +703,10 @@ cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, con
                      8, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     switch (bn) {
-        case 16: return launch_tile<16, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        case 32: return launch_tile<32, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        case 64: return launch_tile<64, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
-        default: return launch_tile<128, WB>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, s);
+        case 16: return launch_tile<16, WB, RP>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, wr, s);
+        case 32: return launch_tile<32, WB, RP>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, wr, s);
+        case 64: return launch_tile<64, WB, RP>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, wr, s);
+        default: return launch_tile<128, WB, RP>(tm_nib, tm_act, tm_bs, wd, y, sumi, m, n, k, p.m4, wr, s);
     }
 }
 
@@ -673,13 +715,70 @@ cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, con
 cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s) {
-    return launch_gemm<32>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+    return launch_gemm<32, false>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }
 
 cudaError_t launch_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s) {
-    return launch_gemm<64>(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+    return launch_gemm<64, false>(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+}
+
+size_t repack_q4_0_gemm_bytes(int64_t n, int64_t k) {
+    return (size_t)((n + kBM - 1) / kBM) * (size_t)((k / kQK + 1) / 2) * (size_t)(kBM * 32);
+}
+
+cudaError_t launch_gemm_q4_0_q8_0_repacked(const uint8_t *wr, const uint16_t *wd, const int8_t *aq,
+                                           const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                           int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    return launch_gemm<32, true>(wr, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+}
+
+// Load-time repack: thread t writes 16-byte unit t of the tiles (row group g,
+// stage j, unit u = 2 * row + block), from block b = 2j + u % 2 of row
+// r = 128 g + u / 2: word c carries elements 8c..8c+7 (low nibbles of bytes
+// 8c.. for c < 2, high nibbles of bytes 8(c-2).. for c >= 2), element
+// 8c + 2i + h at bits 4i + 16h.  Rows past n and blocks past k/32: nibble 8.
+__global__ void repack_q4_0_gemm_kernel(const uint8_t *__restrict__ wq, int64_t n, int64_t k,
+                                        uint4 *__restrict__ wr, int64_t units, int64_t tiles_k) {
+    const int64_t kb = k / kQK;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < units;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = t / 256;
+        const int u = (int)(t % 256);
+        const int64_t g = tile / tiles_k, j = tile % tiles_k;
+        const int64_t r = g * kBM + u / 2, b = 2 * j + u % 2;
+        uint4 out = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        if (r < n && b < kb) {
+            const uint4 src = *reinterpret_cast<const uint4 *>(wq + r * (k / 2) + b * 16);
+            const uint32_t bw[4] = {src.x, src.y, src.z, src.w};
+            uint32_t word[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t acc = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int byte = 8 * (c & 1) + e;
+                    const uint32_t v = (bw[byte >> 2] >> (8 * (byte & 3) + (c >= 2 ? 4 : 0))) & 0xFu;
+                    acc |= v << (4 * (e >> 1) + 16 * (e & 1));
+                }
+                word[c] = acc;
+            }
+            out = make_uint4(word[0], word[1], word[2], word[3]);
+        }
+        wr[t] = out;
+    }
+}
+
+cudaError_t launch_repack_q4_0_gemm(const uint8_t *wq, int64_t n, int64_t k, uint8_t *wr,
+                                    cudaStream_t s) {
+    const int64_t tiles_k = (k / kQK + 1) / 2;
+    const int64_t units = ((n + kBM - 1) / kBM) * tiles_k * 256;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 152 * 16);
+    repack_q4_0_gemm_kernel<<<(unsigned)blocks, threads, 0, s>>>(wq, n, k, reinterpret_cast<uint4 *>(wr),
+                                                                 units, tiles_k);
+    return cudaPeekAtLastError();
 }
 
 }  // namespace qmm

@@ -193,6 +193,36 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_
                                                     as_stream(stream)));
 }
 
+size_t qmm_repack_q4_0_gemm_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || k % kQK != 0 || n * k > kMaxElems) return SIZE_MAX;
+    return qmm::repack_q4_0_gemm_bytes(n, k);
+}
+
+qmm_status qmm_repack_q4_0_gemm(const uint8_t *wq, int64_t n, int64_t k, uint8_t *wr,
+                                size_t wr_bytes, void *stream) {
+    if (!wq || !wr) return QMM_ERR_NULL;
+    if (n <= 0 || k <= 0 || k % kQK != 0 || n * k > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(wq, 16) || !aligned(wr, 16)) return QMM_ERR_ALIGN;
+    if (wr_bytes < qmm::repack_q4_0_gemm_bytes(n, k)) return QMM_ERR_WORKSPACE;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_repack_q4_0_gemm(wq, n, k, wr, as_stream(stream)));
+}
+
+qmm_status qmm_gemm_q4_0_q8_0_repacked(const uint8_t *wr, size_t wr_bytes, const uint16_t *wd,
+                                       const int8_t *aq, const uint16_t *ad, float *y, int64_t m,
+                                       int64_t n, int64_t k, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+    if (qmm_status st = check_q4_common(wr, wd, aq, ad, y, m, n, k)) return st;
+    if (qmm_status st = gemm_shape_ok(m, n, k)) return st;
+    if (wr_bytes < qmm::repack_q4_0_gemm_bytes(n, k)) return QMM_ERR_WORKSPACE;
+    const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+    if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    return launch_status(qmm::launch_gemm_q4_0_q8_0_repacked(wr, wd, aq, ad, y, nullptr, m, n, k,
+                                                             workspace, as_stream(stream)));
+}
+
 qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
                               const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
                               int split_k, void *workspace, size_t workspace_bytes, void *stream) {
@@ -365,6 +395,16 @@ qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int
         // The block-sum variant reads no scale planes (passed as NULL).
         return launch_status(qmm::launch_gemm_q4_0_q8_0(wq, nullptr, aq, nullptr, nullptr, sumi, m,
                                                         n, k, workspace, as_stream(stream)));
+    }
+    if (path == 2) {  // wq: the repacked tiles
+        if (qmm_status st = gemm_shape_ok(m, n, k)) return st;
+        const size_t need = qmm::gemm_workspace_bytes(m, n, k);
+        if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemm_q4_0_q8_0_repacked(wq, nullptr, aq, nullptr, nullptr,
+                                                                 sumi, m, n, k, workspace,
+                                                                 as_stream(stream)));
     }
     return QMM_ERR_ARG;
 }

@@ -132,6 +132,14 @@ size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s);
+// Load-time repack of the Q4_0 nibble plane into the GEMM tile order
+// (ceil(n/128) * ceil(k/64) tiles of 4096 bytes), and the GEMM reading it.
+size_t repack_q4_0_gemm_bytes(int64_t n, int64_t k);
+cudaError_t launch_repack_q4_0_gemm(const uint8_t *wq, int64_t n, int64_t k, uint8_t *wr,
+                                    cudaStream_t s);
+cudaError_t launch_gemm_q4_0_q8_0_repacked(const uint8_t *wr, const uint16_t *wd, const int8_t *aq,
+                                           const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
+                                           int64_t n, int64_t k, void *workspace, cudaStream_t s);
 // The same product with Q8_0 weights (int8 [n, k]); same workspace.
 cudaError_t launch_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,

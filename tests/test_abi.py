@@ -101,6 +101,27 @@ def test_q8_0_weight_entry_points(lib):
     assert lib.qmm_debug_block_sums_q8_0_q8_0(0, A16, A16, None, 1, 1, 32, None, 0, None) == QMM_ERR_NULL
 
 
+def test_repack_entry_points(lib):
+    A16 = _p(0x10000)
+    A2 = _p(0x10002)
+    bad = ctypes.c_size_t(-1).value
+    lib.qmm_repack_q4_0_gemm_bytes.restype = ctypes.c_size_t
+    lib.qmm_repack_q4_0_gemm_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    # ceil(n/128) row groups x ceil(k/64) stages x 4096 bytes
+    assert lib.qmm_repack_q4_0_gemm_bytes(14336, 4096) == 112 * 64 * 4096
+    assert lib.qmm_repack_q4_0_gemm_bytes(129, 96) == 2 * 2 * 4096
+    assert lib.qmm_repack_q4_0_gemm_bytes(1, 33) == bad
+    assert lib.qmm_repack_q4_0_gemm(None, 1, 32, A16, 1 << 20, None) == QMM_ERR_NULL
+    assert lib.qmm_repack_q4_0_gemm(A16, 1, 48, A16, 1 << 20, None) == QMM_ERR_SHAPE
+    assert lib.qmm_repack_q4_0_gemm(A16, 1, 32, A2, 1 << 20, None) == QMM_ERR_ALIGN
+    assert lib.qmm_repack_q4_0_gemm(A16, 1, 32, A16, 4095, None) == QMM_ERR_WORKSPACE
+    gemm = lib.qmm_gemm_q4_0_q8_0_repacked
+    assert gemm(A16, 1 << 20, A16, A16, A16, None, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_NULL
+    assert gemm(A16, 4095, A16, A16, A16, A16, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_WORKSPACE
+    assert gemm(A16, 1 << 20, A16, A16, A16, A16, 4, 4, 32, A16, 16, None) == QMM_ERR_WORKSPACE
+    assert gemm(A2, 1 << 20, A16, A16, A16, A16, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_ALIGN
+
+
 def test_auto_split_policy(lib):
     # a narrow output with a long reduction is split, a wide one is not
     assert lib.qmm_gemv_auto_split(1, 256, 16384) > 1

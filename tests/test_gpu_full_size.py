@@ -110,6 +110,22 @@ def test_prefill_512x14336x4096_sampled_rows(qmm, orc):
     assert np.array_equal(y[r].view(np.uint32), ref.view(np.uint32))
 
 
+def test_prefill_repacked_weights_sampled_rows(qmm, orc):
+    """The prefill shape on weights repacked at load time on the GPU: the
+    repacked tiles equal the oracle's, and the sampled rows the serial
+    definition, bit for bit."""
+    m, n, k = 512, 14336, 4096
+    w, x = synthetic.q4_0_case(11, n, k, m, outlier_p=0.01)
+    wq, wd = orc.quantize_q4_0(w)
+    aq, ad = orc.quantize_q8_0(x)
+    wr = qmm.repack_q4_0_gemm(to_dev(wq))
+    assert np.array_equal(to_np(wr), orc.repack_q4_0_gemm(wq))
+    y = to_np(qmm.gemm_q4_0_q8_0_repacked(wr, f16(wd), to_dev(aq), f16(ad)))
+    r = PREFILL_ROWS
+    ref = orc.gemm_q4_0_q8_0(wq, wd, np.ascontiguousarray(aq[r]), np.ascontiguousarray(ad[r]))
+    assert np.array_equal(y[r].view(np.uint32), ref.view(np.uint32))
+
+
 def test_prefill_q8_0_weights_sampled_rows(qmm, orc):
     """The prefill shape with Q8_0 weights (the widened row), as timed."""
     m, n, k = 512, 14336, 4096

@@ -192,6 +192,30 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
 # BitNet prefill on the tensor cores
 
 # ---------------------------------------------------------------------------
+# load-time repack for the GEMM
+
+@pytest.mark.parametrize("n,k", [(1, 32), (3, 96), (130, 64), (257, 4096), (1000, 11008)])
+def test_repack_q4_0_gemm_bit_exact(qmm, orc, n, k):
+    rng = np.random.default_rng(n + k)
+    wq = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    assert np.array_equal(to_np(qmm.repack_q4_0_gemm(to_dev(wq))), orc.repack_q4_0_gemm(wq))
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES)
+def test_gemm_on_repacked_weights_is_identical(qmm, orc, m, n, k):
+    """The repacked tiles give the planes' GEMM bit for bit, and its block
+    sums match the oracle's."""
+    wq, wd, aq, ad = q4_case(orc, 8500 + m + n, m, n, k)
+    wr = to_dev(orc.repack_q4_0_gemm(wq))
+    args = (to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    y_planes = to_np(qmm.gemm_q4_0_q8_0(to_dev(wq), *args))
+    y_rep = to_np(qmm.gemm_q4_0_q8_0_repacked(wr, *args))
+    assert np.array_equal(y_rep.view(np.uint32), y_planes.view(np.uint32))
+    sumi = to_np(qmm.debug_block_sums(2, wr, to_dev(aq), n=n))
+    assert np.array_equal(sumi, orc.block_sums(wq, aq))
+
+
+# ---------------------------------------------------------------------------
 # Q8_0 weights x Q8_0 activations (GEMV and tensor-core GEMM)
 
 def q8_case(orc, seed, m, n, k):
