@@ -21,9 +21,10 @@
 //   warp 1      allocates TMEM; lane 0 issues the four K=16 MMAs of a stage
 //               into the tile's accumulator (two in TMEM, so one tile's
 //               epilogue overlaps the next tile's MMAs).
-//   warps 2-5   converters: converter c owns ring slot c (the stage count is
-//               4) and turns each stage's codes into the 128-byte-swizzled
-//               K-major fp16 A tile (value code - 1).
+//   warps 2-5   converters: all four convert every stage together, 32 rows
+//               each, turning the codes into the 128-byte-swizzled K-major
+//               fp16 A tile (value code - 1); the stage is ready when all
+//               four have arrived.
 //   warps 6-21  epilogue: thread (warp % 4, lane) owns a weight row (a TMEM
 //               lane quarter is readable only from the sub-partition with the
 //               same index) and BN / 4 columns of the tile.
@@ -46,7 +47,7 @@ constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBK = 64;         // k-elements per stage
 constexpr int kBN = 256;        // tokens per tile (MMA N)
 constexpr int kStages = 4;
-constexpr int kConvWarps = 4;   // one per ring slot
+constexpr int kConvWarps = 4;   // each converts 32 rows of every stage
 constexpr int kConvWarp0 = 2;
 constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kEpiWarps = 16;   // 4 lane quarters x 4 column groups
@@ -64,7 +65,7 @@ constexpr int kNumBars = 3 * kStages + 2 * kAccBufs + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // slack for the 1024-byte round-up
 static_assert(kOffB % 1024 == 0 && kB % 1024 == 0, "swizzled tiles are 1024-byte aligned");
-static_assert(kStages % kConvWarps == 0, "converter c owns ring slot c");
+static_assert(kBM == 32 * kConvWarps, "one row per converter lane and stage");
 
 __device__ unsigned int g_bitnet_gemm_error = 0;
 
@@ -121,7 +122,7 @@ bitnet_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
-            mbar_init(&bar_conv[s], 1);
+            mbar_init(&bar_conv[s], kConvWarps);
             mbar_init(&bar_empty[s], 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
@@ -215,31 +216,28 @@ bitnet_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
         __syncwarp();
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        // Converter c owns ring slot c: the stages st = c, c + 4, ... of the
-        // CTA's stage sequence.  Lane l converts rows l, l+32, l+64, l+96:
-        // one 16-byte read (64 codes) and eight swizzled 16-byte stores per row.
+        // Every converter takes every stage of the CTA's stage sequence, in
+        // order: converter c, lane l converts row 32c + l, one 16-byte read
+        // (64 codes) and eight swizzled 16-byte stores.
         const int cw = warp - kConvWarp0;
+        const int row = 32 * cw + lane;
         const int per_cta = ((tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * ksteps;
-        for (int stg = cw; stg < per_cta; stg += kConvWarps) {
+        for (int stg = 0; stg < per_cta; ++stg) {
             const int s = stg % kStages;
             const uint32_t ph = (uint32_t)(stg / kStages) & 1u;
             if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
             const uint8_t *codes = smem + kOffCodes + s * kCodes;
             uint8_t *a_tile = smem + kOffA + s * kA;
+            const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + row * 16);
+            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-            for (int i = 0; i < kBM / 32; ++i) {
-                const int row = 32 * i + lane;
-                const uint4 w4 = *reinterpret_cast<const uint4 *>(codes + row * 16);
-                const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {  // word q: elements 16q .. 16q+15 (chunks 2q, 2q+1)
-                    uint32_t h[8];
-                    codes_to_f16(w[q], h);
-                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((2 * q) ^ (row & 7)) * 16)) =
-                        make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((2 * q + 1) ^ (row & 7)) * 16)) =
-                        make_uint4(h[4], h[5], h[6], h[7]);
-                }
+            for (int q = 0; q < 4; ++q) {  // word q: elements 16q .. 16q+15 (chunks 2q, 2q+1)
+                uint32_t h[8];
+                codes_to_f16(w[q], h);
+                *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((2 * q) ^ (row & 7)) * 16)) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(a_tile + row * 128 + (((2 * q + 1) ^ (row & 7)) * 16)) =
+                    make_uint4(h[4], h[5], h[6], h[7]);
             }
             fence_proxy_async_smem();
             __syncwarp();
