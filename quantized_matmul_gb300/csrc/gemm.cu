@@ -39,12 +39,10 @@
 //               warp 2 (odd blocks) issues, per block, the two K=16
 //               block-sum MMAs and the scale MMA into accumulator slot
 //               b % NACC (2 * BN columns: sums, then S) and commits.
-//   warps 3..   converters (up to four; the stage count is a multiple of
-//               their number C): converter c owns the ring slots c, c+C, ...
-//               and converts every stage that lands in them, in order, so C
-//               stages convert at once; it turns the nibbles into the
-//               128-byte-swizzled K-major fp16 A tile and writes the 128 rows
-//               x 16 B dw tile of each block.
+//   warps 3..6  converters: all four convert every stage together, each a
+//               quarter of its 256 (row, block) units, turning the weights
+//               into the 128-byte-swizzled K-major fp16 A tile and writing
+//               the 128 rows x 16 B dw tile of each block.
 //   then        drains: thread (warp % 4, lane) owns weight row n (a TMEM
 //               lane quarter is readable only from the sub-partition with the
 //               same index) and BN / groups columns; per block it loads the
@@ -98,15 +96,14 @@ __host__ __device__ constexpr int stages_fit() {
                ? ((kSmemBudget / ctas_per_sm<BN>()) - kZeroBytes - 1024) / stage_bytes<BN, WB>()
                : 8;
 }
-// Converter warps: up to four, and the stage count a multiple of them, so
-// converter c owns the ring slots s = c (mod converters) and handles every
-// use of them in order.  (A warp that took stages round robin could reach a
-// slot's barrier two phases early, which a parity wait cannot tell apart.)
+// Converter warps: four (their number divides the 8 units per lane of a
+// stage).  Every converter visits every stage in order, so no waiter can run
+// a phase ahead of a barrier.
 template <int BN, int WB>
-__host__ __device__ constexpr int conv_warps() { return stages_fit<BN, WB>() < 4 ? stages_fit<BN, WB>() : 4; }
+__host__ __device__ constexpr int conv_warps() { return 4; }
 template <int BN, int WB>
 __host__ __device__ constexpr int stages_for() {
-    return stages_fit<BN, WB>() / conv_warps<BN, WB>() * conv_warps<BN, WB>();
+    return stages_fit<BN, WB>();
 }
 template <int BN, int WB>
 __host__ __device__ constexpr int epi_warp0() { return kConvWarp0 + conv_warps<BN, WB>(); }
@@ -285,7 +282,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
     constexpr int kEpiWarps = S::kEpiWarps;
     constexpr int kConvWarps = conv_warps<BN, WB>();
     constexpr int kEpiWarp0 = epi_warp0<BN, WB>();
-    static_assert(kStages % kConvWarps == 0, "converter c owns the slots c (mod converters)");
+    static_assert(8 % kConvWarps == 0, "every converter takes a whole number of units per lane");
     static_assert(kNacc % kMmaWarps == 0, "block b's slot b % NACC belongs to issuer b % 2");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -313,7 +310,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_load[s], 1);
-            mbar_init(&bar_conv[s], 1);
+            mbar_init(&bar_conv[s], kConvWarps);
             mbar_init(&bar_empty[s], kMmaWarps);
         }
         for (int b = 0; b < kNacc; ++b) {
@@ -417,22 +414,24 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
         __syncwarp();
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        // Converter c owns the ring slots c (mod kConvWarps), i.e. the stages
-        // c, c + kConvWarps, ... in order: all 256 (row, block) units of a
-        // stage, eight per lane (unit u = 32 i + lane: row u / 2, block u % 2),
-        // so the conversions of kConvWarps stages overlap.  Contiguous
-        // 16-byte nibble reads; the swizzled 16-byte stores of 8 consecutive
-        // lanes hit 8 different bank groups.
+        // Every converter takes every stage, in order, and converts its share
+        // of the stage's 256 (row, block) units, kUpl per lane: unit
+        // u = 32 (kUpl c + i) + lane is row u / 2, block u % 2.  A stage is
+        // ready when all converters have arrived, so its conversion latency
+        // is a fraction of one warp's pass.  Contiguous 16-byte reads; the
+        // swizzled 16-byte stores of 8 consecutive lanes hit 8 different bank
+        // groups.
         const int cw = warp - kConvWarp0;
-        for (int j = cw; j < num_stages; j += kConvWarps) {
+        constexpr int kUpl = 8 / kConvWarps;
+        for (int j = 0; j < num_stages; ++j) {
             const int s = j % kStages;
             const uint32_t ph = (uint32_t)(j / kStages) & 1u;
             // the stage's weight scales (global, L2) are requested before the
             // wait so their latency overlaps it
-            unsigned short dwv[8];
+            unsigned short dwv[kUpl];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int u = 32 * i + lane;
+            for (int i = 0; i < kUpl; ++i) {
+                const int u = 32 * (kUpl * cw + i) + lane;
                 const int row = n0 + (u >> 1), kbi = 2 * j + (u & 1);
                 dwv[i] = (!EMIT && row < n && kbi < kb_total) ? __ldg(wd + (int64_t)row * kb_total + kbi)
                                                                : (unsigned short)0;
@@ -441,20 +440,21 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
             const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
             uint8_t *as_tile = smem + S::kOffAs + s * S::kAs;
-            // units in flight per batch: four nibble blocks, or two blocks of
-            // codes (the same bytes in registers)
-            constexpr int kBatch = WB == 32 ? 4 : 2;
+            // units in flight per batch: up to four nibble blocks, or two
+            // blocks of codes (the same bytes in registers)
+            constexpr int kBatch = (WB == 32 ? 4 : 2) < kUpl ? (WB == 32 ? 4 : 2) : kUpl;
 #pragma unroll
-            for (int g = 0; g < 8 / kBatch; ++g) {
+            for (int g = 0; g < kUpl / kBatch; ++g) {
                 uint4 v[kBatch][WB / 32];
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i)
 #pragma unroll
-                    for (int j = 0; j < WB / 32; ++j)
-                        v[i][j] = *reinterpret_cast<const uint4 *>(nib + (32 * (kBatch * g + i) + lane) * (WB / 2) + 16 * j);
+                    for (int jj = 0; jj < WB / 32; ++jj)
+                        v[i][jj] = *reinterpret_cast<const uint4 *>(
+                            nib + (32 * (kUpl * cw + kBatch * g + i) + lane) * (WB / 2) + 16 * jj);
 #pragma unroll
                 for (int i = 0; i < kBatch; ++i) {
-                    const int u = 32 * (kBatch * g + i) + lane;
+                    const int u = 32 * (kUpl * cw + kBatch * g + i) + lane;
                     const int row = u >> 1, blk = u & 1;
                     uint4 out[4];
                     if constexpr (RP)
