@@ -116,14 +116,24 @@ constexpr int nacc_for() {
 }
 __device__ unsigned int g_gemm_error = 0;
 
+// Polls of a phase before a waiter asks to be suspended.  A CTA that has the
+// SM to itself (BN >= 64) polls for a while: a suspended warp resumes later
+// than a polling one sees the phase complete (4% at the prefill shape).  Two
+// CTAs per SM share the issue slots, and there polling costs more than it
+// saves (8% at m = 16), so their waiters suspend at once.
+template <int BN>
+__host__ __device__ constexpr int spin_polls() { return ctas_per_sm<BN>() == 1 ? 200 : 1; }
+
 // the shared bounded waits, reporting into this kernel's error word
+template <int BN>
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit,
                                              volatile int *abort_flag) {
-    return wait_bounded_err(bar, parity, limit, abort_flag, &g_gemm_error);
+    return wait_bounded_err(bar, parity, limit, abort_flag, &g_gemm_error, spin_polls<BN>());
 }
+template <int BN>
 __device__ __forceinline__ bool wait_bounded_warp(uint64_t *bar, uint32_t parity, uint32_t limit,
                                                   volatile int *abort_flag) {
-    return wait_bounded_warp_err(bar, parity, limit, abort_flag, &g_gemm_error);
+    return wait_bounded_warp_err(bar, parity, limit, abort_flag, &g_gemm_error, spin_polls<BN>());
 }
 
 
@@ -339,7 +349,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
         for (int it = 0; it < (withhold_loads ? 0 : num_stages); ++it) {
             const int s = it % kStages;
             const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            if (!wait_bounded_warp(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
+            if (!wait_bounded_warp<BN>(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) break;
             if (lane == 0) {
                 const bool two = 2 * it + 1 < kb_total;
                 mbar_arrive_expect_tx(&bar_load[s], S::kTx - (two ? 0u : (uint32_t)(BN * 16)));
@@ -359,7 +369,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
         // Never leave a copy in flight: wait for every stage still pending.
         for (int it = issued > kStages ? issued - kStages : 0; it < issued; ++it) {
             volatile int no_abort = 0;
-            wait_bounded_warp(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
+            wait_bounded_warp<BN>(&bar_load[it % kStages], (uint32_t)(it / kStages) & 1u, kDrainLimit,
                               &no_abort);
         }
     } else if (warp >= 1 && warp < 1 + kMmaWarps) {
@@ -391,9 +401,9 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
                 const uint32_t bs = smem_u32(smem + S::kOffBs + s * S::kBs + h * BN * 16);
                 const uint64_t as_desc = smem_desc_scale(as, zaddr - as);
                 const uint64_t bs_desc = smem_desc_scale(bs, zaddr - bs);
-                if (!wait_bounded(&bar_conv[s], ph, wait_limit, abort_flag)) break;
+                if (!wait_bounded<BN>(&bar_conv[s], ph, wait_limit, abort_flag)) break;
                 if (kbi < kb_total) {
-                    if (!wait_bounded(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag)) break;
+                    if (!wait_bounded<BN>(&bar_acce[slot], sph ^ 1u, wait_limit, abort_flag)) break;
                     tc_fence_after();
                     mma_f16(d, a_desc, b_desc, idesc, 0u);
                     mma_f16(d, a_desc + 2, b_desc + 2, idesc, 1u);
@@ -408,7 +418,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
             if (issued_any) {
                 mma_commit(&bar_drain[h]);
                 volatile int no_abort = 0;
-                wait_bounded(&bar_drain[h], 0, kDrainLimit, &no_abort);
+                wait_bounded<BN>(&bar_drain[h], 0, kDrainLimit, &no_abort);
             }
         }
         __syncwarp();
@@ -436,7 +446,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
                 dwv[i] = (!EMIT && row < n && kbi < kb_total) ? __ldg(wd + (int64_t)row * kb_total + kbi)
                                                                : (unsigned short)0;
             }
-            if (!wait_bounded_warp(&bar_load[s], ph, wait_limit, abort_flag)) break;
+            if (!wait_bounded_warp<BN>(&bar_load[s], ph, wait_limit, abort_flag)) break;
             const uint8_t *nib = smem + S::kOffNib + s * S::kNib;
             uint8_t *a_tile = smem + S::kOffA + s * S::kA;
             uint8_t *as_tile = smem + S::kOffAs + s * S::kAs;
@@ -492,7 +502,7 @@ gemm_blocks_kernel(const __grid_constant__ CUtensorMap tm_nib,
         bool ok = true;
         for (int kbi = 0; kbi < kb_total; ++kbi) {
             const int slot = kbi % kNacc;
-            if (!wait_bounded_warp(&bar_accf[slot], (uint32_t)(kbi / kNacc) & 1u, wait_limit,
+            if (!wait_bounded_warp<BN>(&bar_accf[slot], (uint32_t)(kbi / kNacc) & 1u, wait_limit,
                                    abort_flag)) {
                 ok = false;
                 break;

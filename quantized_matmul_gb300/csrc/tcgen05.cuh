@@ -76,10 +76,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait: true when the phase completed; false after `limit` polls or
-// when another role raised the abort flag (the error word is then set).
+// when another role raised the abort flag (the error word is then set).  The
+// first `spin` polls do not suspend.
 __device__ __forceinline__ bool wait_bounded_err(uint64_t *bar, uint32_t parity, uint32_t limit,
-                                                 volatile int *abort_flag, unsigned int *err) {
-    if (mbar_test_wait(bar, parity)) return true;
+                                                 volatile int *abort_flag, unsigned int *err,
+                                                 int spin = 1) {
+    for (int i = 0; i < spin; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag || it >= limit) {
@@ -93,8 +96,9 @@ __device__ __forceinline__ bool wait_bounded_err(uint64_t *bar, uint32_t parity,
 // Warp-uniform bounded wait for roles whose lanes all wait and then run
 // warp-collective code: if any lane gave up, every lane sees failure.
 __device__ __forceinline__ bool wait_bounded_warp_err(uint64_t *bar, uint32_t parity, uint32_t limit,
-                                                      volatile int *abort_flag, unsigned int *err) {
-    const bool ok = wait_bounded_err(bar, parity, limit, abort_flag, err);
+                                                      volatile int *abort_flag, unsigned int *err,
+                                                      int spin = 1) {
+    const bool ok = wait_bounded_err(bar, parity, limit, abort_flag, err, spin);
     return __all_sync(0xffffffffu, ok);
 }
 
