@@ -271,9 +271,13 @@ bitnet_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                         const int t = t0 + grp * kCols + 16 * g + c;
                         if (t < m) {
                             const float s = __ldg(act_scale + t);
-                            // dot is the exact integer the accumulator holds
-                            const float out =
-                                s == 0.0f ? 0.0f : __fdiv_rn(__fmul_rn(__uint_as_float(v[c]), absmean), s);
+                            // dot is the exact integer the accumulator holds; a
+                            // zero dot gives the integer's +0, whatever sign the
+                            // accumulator's zero carries
+                            const float dot = __uint_as_float(v[c]);
+                            const float out = (s == 0.0f || dot == 0.0f)
+                                                  ? 0.0f
+                                                  : __fdiv_rn(__fmul_rn(dot, absmean), s);
                             y[(int64_t)t * n + row] = out;
                         }
                     }

@@ -321,6 +321,30 @@ def test_bitnet_gemm_bit_exact(qmm, orc, m, n, k):
         assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+def test_bitnet_gemm_division_over_wide_scales(qmm, orc):
+    """The epilogue's scaling against the oracle's IEEE operations, bit for
+    bit: activation rows scaled across 40 decades (act_scale from ~1e-19 to
+    ~1e22), a zero row (scale 0), a zero weight row against an all-negative
+    activation row (products of -0, which the accumulator sums to -0, while
+    the integer dot is +0), and absmean of 2^40 and 2^-40 besides the drawn
+    one."""
+    m, n, k = 1024, 256, 64
+    t, x, absmean = synthetic.bitnet_case(8200, n, k, m)
+    rng = np.random.default_rng(8201)
+    x = (x * (10.0 ** rng.uniform(-20.0, 20.0, size=(m, 1)))).astype(np.float32)
+    x[3] = 0.0
+    x[5] = -np.abs(x[5]) - 1.0
+    t = t.copy()
+    t[7] = 0  # weight value 0: code 1
+    tw = orc.pack_ternary(t)
+    aq, scale, asum = orc.quantize_act_bitnet(x)
+    assert scale[scale > 0].min() < 1e-18 and scale.max() > 1e21
+    for am in (absmean, np.float32(2.0 ** 40), np.float32(2.0 ** -40)):
+        y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), float(am), to_dev(aq), to_dev(scale)))
+        ref = orc.bitnet_gemv(tw, float(am), aq, scale, asum)
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), float(am)
+
+
 def test_bitnet_gemm_prefill_size_sampled_rows(qmm, orc):
     """The benchmark shape (m=2048, N=6912, K=2560), checked against the
     oracle on a sample of weight rows."""
