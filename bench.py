@@ -373,10 +373,11 @@ def run_layer_set(q, args, dist, peaks):
         "value": gbs(ms_g, gemv_step_bytes), "unit": "GB/s",
         "bytes": "weights + Q8_0 activations + f32 y", "ms_per_step": round(ms_g / args.steps, 6)}
 
-    # end to end through the public Python API, eager calls: the 7 activation
-    # rows in one pinned host buffer go in with one copy, one prepared grouped
-    # call runs the step, and the 7 outputs (one device buffer) come back with
-    # one copy, every step
+    # end to end through the public API, one eager call per step: the 7
+    # activation rows in one pinned host buffer go in with one copy, the
+    # grouped step runs, and the 7 outputs (one device buffer) come back to
+    # one pinned host buffer with one copy, all enqueued by one C-ABI call
+    # (qmm_linear_q4_0_grouped_host, through GroupedLinear(host_io=...))
     k_off = [int(v) for v in np.cumsum([0] + [k for _, k in LAYER_SET])]
     n_off = [int(v) for v in np.cumsum([0] + [n for n, _ in LAYER_SET])]
     x_h = torch.from_numpy(np.concatenate([mt["x_host"].ravel() for mt in mats])).pin_memory()
@@ -386,13 +387,21 @@ def run_layer_set(q, args, dist, peaks):
     e2e_steps = max(20, min(args.steps, 400))
     calls = [q.GroupedLinear([(x_d[k_off[j]:k_off[j + 1]].view(1, -1), *mt["wts"][c],
                                y_d[n_off[j]:n_off[j + 1]].view(1, -1), mt["aq"], mt["ad"])
-                              for j, mt in enumerate(mats)], pdl=True)
+                              for j, mt in enumerate(mats)], pdl=True,
+                             host_io=(x_h, x_d, y_d, y_h), host_direct=True)
              for c in range(rot)]
 
     def e2e_step(i):
-        x_d.copy_(x_h, non_blocking=True)
         calls[i % rot]()
-        y_h.copy_(y_d, non_blocking=True)
+
+    direct = q.host_addressable(x_h) and q.host_addressable(y_h)
+    e2e_path = ("one eager public-API call per step (GroupedLinear with host_io, host_direct -> "
+                "qmm_linear_q4_0_grouped_host): " +
+                ("the grouped quantizer reads the 7 activation rows from page-locked host "
+                 "memory and the GEMV writes the 7 outputs to page-locked host memory, over "
+                 "NVLink-C2C (the device addresses both buffers)" if direct else
+                 "a pinned host->device copy of the 7 activation rows, the grouped quantizer + "
+                 "GEMV (PDL), a device->host copy of the 7 outputs into pinned memory"))
 
     for i in range(max(3, min(args.warmup, 50))):
         e2e_step(i)
@@ -406,10 +415,7 @@ def run_layer_set(q, args, dist, peaks):
     e2e = {"value": round(dist.world * step_bytes * e2e_steps / e2e_s / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * k for _, k in LAYER_SET),
            "d2h_bytes_per_step": sum(4 * n for n, _ in LAYER_SET),
-           "steps": e2e_steps, "path": "eager Python API calls per step: one pinned "
-                                       "host->device copy of the 7 activation rows, one "
-                                       "prepared grouped call (GroupedLinear, PDL), one "
-                                       "device->host copy of the 7 outputs"}
+           "steps": e2e_steps, "path": e2e_path}
     return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e,
                 launches=2 * args.steps, rot=rot, set_bytes=set_bytes,
                 step_bytes=step_bytes, variants=variants)

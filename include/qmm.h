@@ -162,6 +162,7 @@ qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
  *   after the kernel before it completed, which completed after the one
  *   before that, and so on. */
 #define QMM_LINEAR_PDL 1
+#define QMM_LINEAR_HOST_DIRECT 2  /* qmm_linear_q4_0_grouped_host only */
 qmm_status qmm_linear_q4_0(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
                            int8_t *aq, uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,
                            int flags, void *stream);
@@ -191,6 +192,40 @@ typedef struct qmm_linear_problem {
 #define QMM_GROUP_MAX 16
 qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count, int64_t m,
                                    int flags, void *stream);
+
+/* qmm_linear_q4_0_grouped with its input coming from, and its output going
+ * to, host memory, in one call: a copy of x_bytes from x_host (host) to
+ * x_dev (device), the grouped layers, then a copy of y_bytes from y_dev
+ * (device) to y_host (host).  All three are enqueued on `stream` in that
+ * order (cudaMemcpyAsync).  With page-locked host buffers the call returns
+ * before they run, so the caller must keep x_host and y_host alive and
+ * unchanged until the stream has passed the copies; pageable host memory
+ * makes the copies synchronous.  The problems' x must lie in
+ * [x_dev, x_dev + x_bytes) and their y in [y_dev, y_dev + y_bytes) for the
+ * copies to carry them; without QMM_LINEAR_HOST_DIRECT the library does
+ * not check this.  A size of 0 skips that copy (its pointers may then be
+ * NULL).
+ *   flags: QMM_LINEAR_PDL as for qmm_linear_q4_0, and QMM_LINEAR_HOST_DIRECT:
+ *   where the runtime reports a device address for both host buffers
+ *   (page-locked memory on a system with unified addressing, as over
+ *   NVLink-C2C on GB300), the kernels read x from x_host and write y to
+ *   y_host themselves and x_dev and y_dev are not touched.  The problems' x
+ *   and y must then lie in the device buffers (checked, QMM_ERR_ARG
+ *   otherwise), and each is redirected to the same offset in the host
+ *   buffer.  Where the runtime reports none, the call copies as without the
+ *   flag.
+ * The same checks as qmm_linear_q4_0_grouped run first, and a failure
+ * enqueues nothing; a failed copy or launch returns QMM_ERR_CUDA, possibly
+ * after the earlier steps were enqueued. */
+qmm_status qmm_linear_q4_0_grouped_host(const qmm_linear_problem *problems, int count, int64_t m,
+                                        int flags, const void *x_host, void *x_dev, size_t x_bytes,
+                                        const void *y_dev, void *y_host, size_t y_bytes,
+                                        void *stream);
+
+/* 1 when the current device can address the host memory at `host` itself
+ * (the condition QMM_LINEAR_HOST_DIRECT acts on), else 0.  Asks the runtime
+ * for the pointer's attributes; dereferences nothing. */
+int qmm_host_addressable(const void *host);
 
 /* Q4_0 x Q8_0 matrix product for prefill (m >= 1, any n, k % 32 == 0), same
  * result definition as the GEMV.  The block sums run on the tensor cores

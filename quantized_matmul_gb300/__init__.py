@@ -69,6 +69,8 @@ def load() -> ctypes.CDLL:
             "qmm_gemm_q8_0_q8_0": (I, [P, P, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_linear_q4_0": (I, [P, P, P, I64, P, P, P, I64, I64, I64, I, P]),
             "qmm_linear_q4_0_grouped": (I, [P, I, I64, I, P]),
+            "qmm_linear_q4_0_grouped_host": (I, [P, I, I64, I, P, P, SZ, P, P, SZ, P]),
+            "qmm_host_addressable": (I, [P]),
             "qmm_quantize_act_bitnet": (I, [P, I64, I64, P, P, P, P]),
             "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
             "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
@@ -312,6 +314,7 @@ def gemm_q4_0_q8_0_repacked(wr, wd, aq, ad, y=None, workspace=None):
 
 
 LINEAR_PDL = 1
+LINEAR_HOST_DIRECT = 2
 GROUP_MAX = 16
 
 
@@ -369,6 +372,14 @@ def linear_q4_0_grouped(problems, pdl: bool = False):
     return outs
 
 
+def host_addressable(t) -> bool:
+    """Whether the current GPU can read and write the host tensor t's memory
+    itself (page-locked memory with a device mapping), as host_direct needs."""
+    if t.is_cuda:
+        raise ValueError("a host (CPU) tensor is expected")
+    return bool(load().qmm_host_addressable(t.data_ptr()))
+
+
 class GroupedLinear:
     """A prepared linear_q4_0_grouped call for a decode loop.
 
@@ -376,17 +387,53 @@ class GroupedLinear:
     enqueues the two launches on the current stream with one ctypes call.
     The tensors given (and the outputs allocated here) are used in place on
     every call: keep them alive and write new activations into the same x
-    tensors between calls.  `outputs` is the list of (y, aq, ad)."""
+    tensors between calls.  `outputs` is the list of (y, aq, ad).
 
-    def __init__(self, problems, pdl: bool = False):
+    host_io=(x_host, x_dev, y_dev, y_host) makes every call carry its input
+    from and its output to host memory as well (qmm_linear_q4_0_grouped_host):
+    x_host (CPU) is copied into x_dev (CUDA) before the layers, and y_dev
+    (CUDA) into y_host (CPU) after them, all on the current stream.  Every
+    problem's x must be a view of x_dev and its y a view of y_dev.  Use
+    page-locked host tensors (pin_memory()) to keep the call asynchronous;
+    the host tensors must then stay unchanged until the stream has passed
+    the copies.  host_direct=True lets the kernels read x_host and write
+    y_host themselves where the device can address them (page-locked memory
+    over NVLink-C2C), with no copy engine transfer; elsewhere it copies."""
+
+    def __init__(self, problems, pdl: bool = False, host_io=None, host_direct: bool = False):
         self._table, self._m, self.outputs = _grouped_table(problems)
         self._keep = [tuple(p) for p in problems]  # the tensors the table points at
         self._count = len(problems)
         self._flags = LINEAR_PDL if pdl else 0
         self._fn = load().qmm_linear_q4_0_grouped
         self._addr = ctypes.addressof(self._table)
+        self._host = None
+        if host_direct and host_io is None:
+            raise ValueError("host_direct needs host_io")
+        if host_io is not None:
+            x_host, x_dev, y_dev, y_host = host_io
+            for name, t, cuda in (("x_host", x_host, False), ("x_dev", x_dev, True),
+                                  ("y_dev", y_dev, True), ("y_host", y_host, False)):
+                if t.is_cuda != cuda or not t.is_contiguous():
+                    raise ValueError(f"{name}: a contiguous {'CUDA' if cuda else 'CPU'} tensor")
+            xb = x_dev.numel() * x_dev.element_size()
+            yb = y_dev.numel() * y_dev.element_size()
+            if x_host.numel() * x_host.element_size() != xb or \
+                    y_host.numel() * y_host.element_size() != yb:
+                raise ValueError("host and device tensors of host_io differ in size")
+            self._keep.append(tuple(host_io))
+            self._host = (x_host.data_ptr(), x_dev.data_ptr(), xb,
+                          y_dev.data_ptr(), y_host.data_ptr(), yb)
+            self._fn_host = load().qmm_linear_q4_0_grouped_host
+            self._host_flags = self._flags | (LINEAR_HOST_DIRECT if host_direct else 0)
 
     def __call__(self):
+        if self._host is not None:
+            st = self._fn_host(self._addr, self._count, self._m, self._host_flags, *self._host,
+                               _stream())
+            if st != 0:
+                raise QmmError(st, "qmm_linear_q4_0_grouped_host")
+            return self.outputs
         st = self._fn(self._addr, self._count, self._m, self._flags, _stream())
         if st != 0:
             raise QmmError(st, "qmm_linear_q4_0_grouped")

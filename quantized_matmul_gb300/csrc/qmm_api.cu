@@ -157,12 +157,14 @@ qmm_status qmm_linear_q4_0(const uint8_t *wq, const uint16_t *wd, const float *x
                                                     nullptr, s, pdl));
 }
 
-qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count, int64_t m,
-                                   int flags, void *stream) {
+namespace {
+
+// Checks a grouped call's table and fills its launch table; launches nothing.
+qmm_status build_group(const qmm_linear_problem *problems, int count, int64_t m,
+                       qmm::LinearGroup &tab) {
     if (!problems) return QMM_ERR_NULL;
     if (count < 1 || count > QMM_GROUP_MAX) return QMM_ERR_ARG;
-    if (flags & ~QMM_LINEAR_PDL) return QMM_ERR_ARG;
-    qmm::LinearGroup tab = {};
+    tab = {};
     int64_t ctas = 0, blocks = 0;
     for (int p = 0; p < count; ++p) {
         const qmm_linear_problem &P = problems[p];
@@ -175,10 +177,90 @@ qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count
     if (ctas >= (int64_t(1) << 31) || blocks >= (int64_t(1) << 33)) return QMM_ERR_SHAPE;
     tab.count = count;
     tab.m = (int)m;
+    return QMM_OK;
+}
+
+// The device address of page-locked host memory, or nullptr when the device
+// cannot address it (the runtime's pointer attributes decide; nothing is
+// dereferenced here).
+const void *host_device_address(const void *host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer leaves a (non-sticky) error behind
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// [lo, hi) of bytes inside [base, base + bytes)?
+bool within(const void *lo, size_t len, const void *base, size_t bytes) {
+    const uintptr_t l = reinterpret_cast<uintptr_t>(lo), b = reinterpret_cast<uintptr_t>(base);
+    return l >= b && len <= bytes && l - b <= bytes - len;
+}
+
+}  // namespace
+
+qmm_status qmm_linear_q4_0_grouped(const qmm_linear_problem *problems, int count, int64_t m,
+                                   int flags, void *stream) {
+    if (flags & ~QMM_LINEAR_PDL) return QMM_ERR_ARG;
+    qmm::LinearGroup tab;
+    if (qmm_status st = build_group(problems, count, m, tab)) return st;
     if (qmm_status st = check_device()) return st;
     return launch_status(
         qmm::launch_linear_grouped(tab, (flags & QMM_LINEAR_PDL) != 0, as_stream(stream)));
 }
+
+qmm_status qmm_linear_q4_0_grouped_host(const qmm_linear_problem *problems, int count, int64_t m,
+                                        int flags, const void *x_host, void *x_dev, size_t x_bytes,
+                                        const void *y_dev, void *y_host, size_t y_bytes,
+                                        void *stream) {
+    if (flags & ~(QMM_LINEAR_PDL | QMM_LINEAR_HOST_DIRECT)) return QMM_ERR_ARG;
+    qmm::LinearGroup tab;
+    if (qmm_status st = build_group(problems, count, m, tab)) return st;
+    if (x_bytes && (!x_host || !x_dev)) return QMM_ERR_NULL;
+    if (y_bytes && (!y_dev || !y_host)) return QMM_ERR_NULL;
+    const bool pdl = (flags & QMM_LINEAR_PDL) != 0;
+    if (flags & QMM_LINEAR_HOST_DIRECT) {
+        // every problem's x and y inside the device buffers the host buffers mirror
+        for (int p = 0; p < count; ++p) {
+            const qmm_linear_problem &P = problems[p];
+            const size_t xlen = (size_t)(((m - 1) * P.ldx + P.k) * 4), ylen = (size_t)(m * P.n * 4);
+            if (!within(P.x, xlen, x_dev, x_bytes) || !within(P.y, ylen, y_dev, y_bytes))
+                return QMM_ERR_ARG;
+        }
+    }
+    if (qmm_status st = check_device()) return st;
+    cudaStream_t s = as_stream(stream);
+    if (flags & QMM_LINEAR_HOST_DIRECT) {
+        const auto *xh = static_cast<const uint8_t *>(host_device_address(x_host));
+        auto *yh = static_cast<uint8_t *>(const_cast<void *>(host_device_address(y_host)));
+        if (xh && yh) {
+            // the kernels read x from, and write y to, host memory themselves
+            qmm::LinearGroup direct = tab;
+            bool ok = true;
+            for (int p = 0; p < count && ok; ++p) {
+                auto &D = direct.p[p];
+                D.x = reinterpret_cast<const float *>(
+                    xh + (reinterpret_cast<const uint8_t *>(problems[p].x) -
+                          static_cast<const uint8_t *>(x_dev)));
+                D.y = reinterpret_cast<float *>(
+                    yh + (reinterpret_cast<const uint8_t *>(problems[p].y) -
+                          static_cast<const uint8_t *>(y_dev)));
+                ok = aligned(D.x, 4) && aligned(D.y, 4);
+            }
+            if (ok) return launch_status(qmm::launch_linear_grouped(direct, pdl, s));
+        }
+        // not addressable from the device: copy instead
+    }
+    if (x_bytes && cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    if (qmm_status st = launch_status(qmm::launch_linear_grouped(tab, pdl, s))) return st;
+    if (y_bytes && cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return QMM_OK;
+}
+
+int qmm_host_addressable(const void *host) { return host && host_device_address(host) ? 1 : 0; }
 
 qmm_status qmm_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                               const uint16_t *ad, float *y, int64_t m, int64_t n, int64_t k,

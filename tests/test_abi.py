@@ -184,6 +184,18 @@ def test_argument_errors_return_before_any_launch(lib):
     tab[3].k = 32
     tab[2].aq = 0x10004
     assert lib.qmm_linear_q4_0_grouped(ctypes.addressof(tab), 5, 1, 0, None) == QMM_ERR_ALIGN
+    tab[2].aq = 0x10000
+    # the host-buffer variant: the same table checks, then its copy arguments
+    host = lib.qmm_linear_q4_0_grouped_host
+    assert host(None, 1, 1, 0, 0x10000, 0x10000, 64, 0x10000, 0x10000, 64, None) == QMM_ERR_NULL
+    assert host(ctypes.addressof(tab), 17, 1, 0, 0x10000, 0x10000, 64, 0x10000, 0x10000, 64,
+                None) == QMM_ERR_ARG
+    assert host(ctypes.addressof(tab), 5, 1, 2, 0x10000, 0x10000, 64, 0x10000, 0x10000, 64,
+                None) == QMM_ERR_ARG
+    assert host(ctypes.addressof(tab), 5, 1, 0, None, 0x10000, 64, 0x10000, 0x10000, 64,
+                None) == QMM_ERR_NULL
+    assert host(ctypes.addressof(tab), 5, 1, 0, 0x10000, 0x10000, 64, 0x10000, None, 64,
+                None) == QMM_ERR_NULL
     # debug entry: unknown path
     assert lib.qmm_debug_block_sums_q4_0_q8_0(5, A16, A16, A16, 1, 1, 32, None, 0, None) == QMM_ERR_ARG
 

@@ -7,6 +7,8 @@ f32 outputs must pass the gate of conftest.rel_gate: each output within
 Shapes straddle the kernels' tiles (32-block lanes, 16-row CTAs, 128-row and
 16..128-token tensor-core tiles) with ragged tails, plus the degenerate cases
 (one row, one block, all-zero blocks, large outliers)."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -528,6 +530,56 @@ def test_prepared_grouped_linear_matches_the_one_shot_call(qmm, orc):
     again = qmm.linear_q4_0_grouped([(x, wq, wd) for x, wq, wd in probs], pdl=False)
     for (y1, _, _), (y2, _, _) in zip(again, call()):
         assert torch.equal(y1, y2)
+
+
+def test_grouped_linear_with_host_buffers(qmm, orc):
+    """GroupedLinear(host_io=...): one call copies the activations in from
+    page-locked host memory, runs the layers and copies the outputs back.
+    The host outputs equal, bit for bit, the device outputs of the plain
+    call, and a new host input is picked up by the next call."""
+    import torch
+    shapes = [(300, 4096), (77, 1024), (129, 11008)]
+    xs, mats = [], []
+    for j, (n, k) in enumerate(shapes):
+        w, x = synthetic.q4_0_case(950 + j, n, k, 1)
+        wq, wd = orc.quantize_q4_0(w)
+        xs.append(x.ravel())
+        mats.append((n, k, to_dev(wq), to_dev(wd.view(np.float16))))
+    k_off = np.cumsum([0] + [k for _, k in shapes])
+    n_off = np.cumsum([0] + [n for n, _ in shapes])
+    x_host = torch.from_numpy(np.concatenate(xs)).pin_memory()
+    y_host = torch.full((int(n_off[-1]),), np.nan, dtype=torch.float32).pin_memory()
+    x_dev = torch.zeros_like(x_host, device="cuda")
+    y_dev = torch.zeros((int(n_off[-1]),), dtype=torch.float32, device="cuda")
+    probs = [(x_dev[k_off[j]:k_off[j + 1]].view(1, -1), wq, wd,
+              y_dev[n_off[j]:n_off[j + 1]].view(1, -1))
+             for j, (_, _, wq, wd) in enumerate(mats)]
+    assert qmm.host_addressable(x_host) and qmm.host_addressable(y_host)
+    for direct in (False, True):
+        call = qmm.GroupedLinear(probs, pdl=True, host_io=(x_host, x_dev, y_dev, y_host),
+                                 host_direct=direct)
+        for scale in (1.0, -0.5):
+            if scale != 1.0:
+                x_host.mul_(scale)
+            y_host.fill_(np.nan)
+            call()
+            torch.cuda.synchronize()
+            plain = qmm.linear_q4_0_grouped(
+                [(x_host[k_off[j]:k_off[j + 1]].view(1, -1).cuda(), wq, wd)
+                 for j, (_, _, wq, wd) in enumerate(mats)])
+            for j, (y, _, _) in enumerate(plain):
+                assert torch.equal(y.cpu().ravel(), y_host[n_off[j]:n_off[j + 1]]), (direct, j)
+    # direct mode checks that every x and y lies in the mirrored device buffers
+    lib = qmm.load()
+    outside = torch.zeros((1, shapes[0][1]), dtype=torch.float32, device="cuda")
+    tab, m, _ = qmm._grouped_table(probs + [(outside, *mats[0][2:])])
+    st = lib.qmm_linear_q4_0_grouped_host(
+        ctypes.addressof(tab), len(probs) + 1, m, qmm.LINEAR_HOST_DIRECT, x_host.data_ptr(),
+        x_dev.data_ptr(), x_dev.numel() * 4, y_dev.data_ptr(), y_host.data_ptr(),
+        y_dev.numel() * 4, None)
+    assert st == 8  # QMM_ERR_ARG
+    with pytest.raises(ValueError, match="differ in size"):
+        qmm.GroupedLinear(probs, host_io=(x_host[:-1], x_dev, y_dev, y_host))
 
 
 def test_linear_grouped_full_table(qmm, orc):
