@@ -266,11 +266,28 @@ bitnet_gemm_kernel(const __grid_constant__ CUtensorMap tm_codes,
                 tmem_ld16(col0 + 16 * g, v);
                 tmem_wait_ld();
                 if (row < n) {
+                    // the chunk's 16 activation scales: four 16-byte loads
+                    // where the whole chunk exists and is aligned
+                    const int tc = t0 + grp * kCols + 16 * g;
+                    float sc[16];
+                    if (tc + 16 <= m && (reinterpret_cast<uintptr_t>(act_scale + tc) & 15) == 0) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 f = __ldg(reinterpret_cast<const float4 *>(act_scale + tc) + i);
+                            sc[4 * i] = f.x;
+                            sc[4 * i + 1] = f.y;
+                            sc[4 * i + 2] = f.z;
+                            sc[4 * i + 3] = f.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) sc[c] = tc + c < m ? __ldg(act_scale + tc + c) : 0.0f;
+                    }
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const int t = t0 + grp * kCols + 16 * g + c;
+                        const int t = tc + c;
                         if (t < m) {
-                            const float s = __ldg(act_scale + t);
+                            const float s = sc[c];
                             // dot is the exact integer the accumulator holds; a
                             // zero dot gives the integer's +0, whatever sign the
                             // accumulator's zero carries

@@ -323,6 +323,19 @@ def test_bitnet_gemm_bit_exact(qmm, orc, m, n, k):
         assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
+def test_bitnet_gemm_scales_at_any_alignment(qmm, orc):
+    """act_scale 4-byte but not 16-byte aligned (a view one element into a
+    buffer): the epilogue then reads the scales one by one; same bits."""
+    import torch
+    m, n, k = 48, 130, 128
+    tw, absmean, aq, scale, asum = _bitnet_operands(orc, 8300, m, n, k)
+    buf = torch.zeros(m + 1, dtype=torch.float32, device="cuda")
+    buf[1:] = to_dev(scale)
+    y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), absmean, to_dev(aq), buf[1:]))
+    ref = orc.bitnet_gemv(tw, absmean, aq, scale, asum)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
 def test_bitnet_gemm_division_over_wide_scales(qmm, orc):
     """The epilogue's scaling against the oracle's IEEE operations, bit for
     bit: activation rows scaled across 40 decades (act_scale from ~1e-19 to
