@@ -31,7 +31,7 @@
 namespace qmm {
 namespace {
 
-constexpr int kWarps = 8;        // warps per CTA
+constexpr int kWarps = 4;        // warps per CTA (4: 1.5% faster layer set, 4.7% faster vocabulary GEMV than 8)
 constexpr int kUnroll = 4;       // blocks (per lane, per row) loaded before use
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
