@@ -354,11 +354,11 @@ def run_layer_set(q, args, dist, peaks):
     # 0.3% of the bytes); with PDL the two launches overlap, so its time is
     # bounded by the step time, which is what is measured
     achieved = step_bytes * args.steps / (ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "gemv_grouped_kernel<1,2,true>",
+    roofline = {"bound": "hbm", "kernel": "gemv_grouped_kernel<1,4,true>",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": peaks["source"],
-                "traffic": recorded_traffic("gemv_grouped_kernel<1,2,1>"),
+                "traffic": recorded_traffic("gemv_grouped_kernel<1,4,1>"),
                 "traffic_source": "profiles/traffic.txt (ncu dram__bytes_read.sum + "
                                   "dram__bytes_write.sum of one launch; null once the kernel's "
                                   "source changed since that capture)",
