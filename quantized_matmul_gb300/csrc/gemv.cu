@@ -465,7 +465,8 @@ cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count,
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s) {
-    if (m == 1) return launch_bitnet<1, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    // m = 1: four rows per warp (3.53 against 3.60 us for two at N=6912, K=2560)
+    if (m == 1) return launch_bitnet<1, 4>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     if (m == 2) return launch_bitnet<2, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
     if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
