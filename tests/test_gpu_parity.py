@@ -148,6 +148,25 @@ def test_gemm_is_bit_identical_to_serial_order(qmm, orc, m, n, k):
     assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
 
 
+# More tiles than CTAs fit on the GPU at once (152 SMs; one CTA per SM at
+# BN >= 64, two at BN <= 32), odd block counts, ragged row and token tiles.
+@pytest.mark.parametrize("m,n,k", [(40, 128 * 310 + 5, 32 * 33), (16, 128 * 330 + 77, 32 * 5),
+                                   (130, 128 * 80 + 3, 32 * 9)])
+def test_gemm_more_tiles_than_resident_ctas(qmm, orc, m, n, k):
+    """y on sampled weight rows (tile edges and the last rows) and, where
+    small enough, every block sum, bit for bit."""
+    wq, wd, aq, ad = q4_case(orc, 5600 + m, m, n, k)
+    dwq, dwd = to_dev(wq), to_dev(wd.view(np.float16))
+    y = to_np(qmm.gemm_q4_0_q8_0(dwq, dwd, to_dev(aq), to_dev(ad.view(np.float16))))
+    rows = np.unique(np.r_[0:3, 125:131, 128 * 152 - 2:128 * 152 + 2, 128 * 305:128 * 305 + 3,
+                           n - 4:n].clip(0, n - 1))
+    ref = orc.gemm_q4_0_q8_0(np.ascontiguousarray(wq[rows]), np.ascontiguousarray(wd[rows]), aq, ad)
+    assert np.array_equal(y[:, rows].view(np.uint32), ref.view(np.uint32))
+    if m * n * (k // 32) <= 64 * 1024 * 1024:
+        sumi = to_np(qmm.debug_block_sums(1, dwq, to_dev(aq)))
+        assert np.array_equal(sumi, orc.block_sums(wq, aq))
+
+
 def test_gemm_and_gemv_agree_with_adversarial_activations(qmm, orc):
     m, n, k = 9, 200, 4096
     w, _ = synthetic.q4_0_case(61, n, k, 1)
