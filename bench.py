@@ -337,8 +337,17 @@ def run_layer_set(q, args, dist, peaks):
         return round(nbytes * args.steps / (ms_ * 1e-3) / 1e9, 1)
 
     sampler = ClockSampler(torch.cuda.current_device())
-    ms, clocks = GraphTimer(grouped_step(True), rot).time(args.steps, args.warmup, dist, sampler)
+    timer = GraphTimer(grouped_step(True), rot)
+    ms, clocks = timer.time(args.steps, args.warmup, dist, sampler)
     value = dist.world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    # run-to-run spread: five more timed regions of a fifth of the steps each
+    # (outside the headline's region; they only describe its noise)
+    rep_steps = max(args.steps // 5, 1)
+    reps = [timer.time(rep_steps, 1, dist)[0] for _ in range(5)]
+    rep_mean = sum(reps) / len(reps)
+    rep_cv = (sum((r - rep_mean) ** 2 for r in reps) / len(reps)) ** 0.5 / rep_mean
+    noise = {"repeats": len(reps), "steps_each": rep_steps, "cv": round(rep_cv, 5),
+             "noisy": rep_cv > 0.08}
     variants = {}
     for name, fn, what in (
             ("grouped_no_pdl", grouped_step(False), "the same two launches without PDL"),
@@ -416,7 +425,7 @@ def run_layer_set(q, args, dist, peaks):
            "h2d_bytes_per_step": sum(4 * k for _, k in LAYER_SET),
            "d2h_bytes_per_step": sum(4 * n for n, _ in LAYER_SET),
            "steps": e2e_steps, "path": e2e_path}
-    return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e,
+    return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e, noise=noise,
                 launches=2 * args.steps, rot=rot, set_bytes=set_bytes,
                 step_bytes=step_bytes, variants=variants)
 
@@ -799,6 +808,7 @@ def main():
                 "cpu_baseline": cpu,
                 "e2e": main_res["e2e"],
                 "gpu_launches": main_res["launches"],
+                "noise": main_res["noise"],
                 "frac_hbm_step": round(main_res["value"] / dist.world / peaks["hbm_gbs"], 4),
                 "configs": configs,
             }
