@@ -170,7 +170,7 @@ qmm_status build_group(const qmm_linear_problem *problems, int count, int64_t m,
         const qmm_linear_problem &P = problems[p];
         if (qmm_status st = check_linear(P.wq, P.wd, P.x, P.ldx, P.aq, P.ad, P.y, m, P.n, P.k))
             return st;
-        ctas += (P.n + 7) / 8;  // at most 8 rows per CTA
+        ctas += (P.n + 1) / 2;  // at least 2 rows per CTA of the grouped GEMV
         blocks += m * (P.k / kQK);
         tab.p[p] = {P.wq, P.wd, P.x, P.ldx, P.aq, P.ad, P.y, P.n, P.k};
     }
