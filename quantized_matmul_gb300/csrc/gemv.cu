@@ -31,8 +31,13 @@
 namespace qmm {
 namespace {
 
-constexpr int kWarps = 4;        // warps per CTA (4: 1.5% faster layer set, 4.7% faster vocabulary GEMV than 8)
-constexpr int kGroupedWarps = 2; // warps per CTA of the grouped GEMV (2 at 4 rows: 5178 against 5124 GB/s for 4)
+// Warps per CTA.  Small CTAs start and finish in finer steps: against 4
+// warps, 2 measured 1% faster for the single 4096x4096 GEMV, 2% for the BitNet
+// GEMV and the same for the vocabulary GEMV; against 8, 4 was 4.7% faster at
+// vocabulary size.
+constexpr int kWarps = 2;
+// warps per CTA of the grouped GEMV (2 at 4 rows: 5178 against 5124 GB/s for 4)
+constexpr int kGroupedWarps = 2;
 constexpr int kUnroll = 4;       // blocks (per lane, per row) loaded before use
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
