@@ -128,11 +128,15 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
  * array owned by the library, QMM_NOALLOC_SCRATCH_FLOATS floats (4 MiB)
  * reserved on every GPU that loads the library and held until the process
  * exits.  The call itself allocates nothing.
- *   - An explicit split_k > 1 with split_k * m * n > QMM_NOALLOC_SCRATCH_FLOATS
- *     returns QMM_ERR_WORKSPACE and launches nothing; split_k = 0 picks the
- *     automatic split, lowered until the partials fit.
+ *   - A split_k > 1 with split_k * m * n > QMM_NOALLOC_SCRATCH_FLOATS
+ *     returns QMM_ERR_WORKSPACE and launches nothing.  The automatic split
+ *     (split_k = 0) always fits: it exceeds 1 only for short grids (n below
+ *     ~1200 rows) and never passes 32.
  *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current and keeps it for the life of the process; make
+ *     that first call before any stream capture.  Calls after
+ *     cudaDeviceReset (or any teardown of the device's primary context) are
+ *     not supported: the kept address would no longer be valid.
  *   - Every call on a device shares the one array (it keeps the last call's
  *     partials; each call overwrites all it reads, so nothing needs
  *     clearing): calls whose executions overlap on the GPU, e.g. on two

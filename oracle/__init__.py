@@ -139,6 +139,18 @@ def quantize_q8_0(x) -> tuple[np.ndarray, np.ndarray]:
     return aq, ad
 
 
+def quantize_q8_0_strided(xbuf, k) -> tuple[np.ndarray, np.ndarray]:
+    """The first k columns of f32 [m, ldx] rows (row stride ldx >= k)
+    -> (aq int8 [m, k], ad fp16-bits uint16 [m, k/32])."""
+    xbuf = _c(xbuf, np.float32)
+    m, ldx = xbuf.shape
+    assert k % QK == 0 and ldx >= k
+    aq = np.empty((m, k), np.int8)
+    ad = np.empty((m, k // QK), np.uint16)
+    _load().orc_quantize_q8_0(_p(xbuf), m, k, ldx, _p(aq), _p(ad))
+    return aq, ad
+
+
 def quantize_q4_0(w) -> tuple[np.ndarray, np.ndarray]:
     """f32 [n, k] -> (wq uint8 [n, k/2], wd fp16-bits uint16 [n, k/32])."""
     w = _c(w, np.float32)

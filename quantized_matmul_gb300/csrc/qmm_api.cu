@@ -132,12 +132,13 @@ qmm_status qmm_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, con
     if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
     int split = 1;
     if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
-    const int64_t cap = qmm::kGemvNoAllocScratchFloats;
-    if (split > 1 && (int64_t)split * m * n > cap) {
-        if (split_k != 0) return QMM_ERR_WORKSPACE;  // the built-in scratch is too small
-        split = (int)(cap / (m * n));                // automatic choice: largest that fits
-        if (split < 2) split = 1;
-    }
+    // The automatic split only exceeds 1 when the grid is short of two CTAs
+    // per SM, i.e. for n below ~1200 rows, and it never passes 32: its
+    // partials stay below 20 Ki floats for every m <= QMM_GEMV_MAX_M (a CPU
+    // test sweeps the bound).  Only an explicit split_k can overflow the
+    // array, and the same check rejects both.
+    if (split > 1 && (int64_t)split * m * n > qmm::kGemvNoAllocScratchFloats)
+        return QMM_ERR_WORKSPACE;
     if (qmm_status st = check_device()) return st;
     return launch_status(qmm::launch_gemv_q4_0_q8_0_noalloc(wq, wd, aq, ad, y, m, n, k, split,
                                                             as_stream(stream)));

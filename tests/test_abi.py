@@ -129,6 +129,21 @@ def test_auto_split_policy(lib):
     assert lib.qmm_gemv_auto_split(1, 4096, 4096) >= 1
 
 
+def test_auto_split_always_fits_the_noalloc_array(lib):
+    # qmm_gemv_q4_0_q8_0_noalloc rejects any split whose partials exceed its
+    # built-in array; the automatic split must never be rejected, at any
+    # m <= 16, any n and any k
+    cap = 1 << 20
+    worst = 0
+    for m in range(1, 17):
+        for n in list(range(1, 1400)) + [2048, 4096, 11008, 128256]:
+            for k in (32, 2048, 4096, 11008, 1 << 17):
+                s = lib.qmm_gemv_auto_split(m, n, k)
+                assert 1 <= s <= max(1, k // 32 // 64) or s == 1
+                worst = max(worst, s * m * n if s > 1 else 0)
+    assert 0 < worst <= cap // 32, worst
+
+
 def _p(v):
     return ctypes.c_void_p(v)
 

@@ -41,6 +41,8 @@ MUTANTS = [
     ("q8_0_quantizes_with_fp16_scale",
      "q = roundf(xb[j] / d);",
      "q = roundf(xb[j] / orc_fp16_to_fp32(orc_fp32_to_fp16(d)));", 1),
+    ("q8_0_row_stride_k",
+     "const float *xb = x + i * ldx + b * ORC_QK;", "const float *xb = x + i * k + b * ORC_QK;", 1),
     ("q4_0_positive_divisor",
      "float d = maxv / -8.0f;", "float d = maxv / 8.0f;", 1),
     ("q4_0_last_index_on_ties",

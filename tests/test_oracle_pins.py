@@ -365,6 +365,28 @@ def test_q8_0_invariants(orc):
     assert np.array_equal(ad, d32.astype(np.float32).astype(np.float16).view(np.uint16))
 
 
+def test_q8_0_strided_rows_invariants(orc):
+    # rows read with a row stride larger than k: the padding holds values far
+    # larger than the rows, so a row read from the wrong place changes the
+    # block maxima and breaks the invariants below
+    rng = np.random.default_rng(21)
+    m, k, ldx = 5, 96, 160
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    buf = np.full((m, ldx), 1.0e4, np.float32)
+    buf[:, :k] = x
+    aq, ad = orc.quantize_q8_0_strided(buf, k)
+    q = aq.astype(np.int64).reshape(m, -1, QK)
+    xb = x.astype(np.float64).reshape(m, -1, QK)
+    amax = np.abs(xb).max(axis=2)
+    d32 = (amax.astype(np.float32) / np.float32(127)).astype(np.float64)
+    assert np.array_equal(ad, d32.astype(np.float32).astype(np.float16).view(np.uint16))
+    for i in range(m):
+        for b in range(q.shape[1]):
+            j = int(np.argmax(np.abs(xb[i, b])))
+            assert abs(int(q[i, b, j])) == 127
+            assert (np.abs(xb[i, b] / d32[i, b] - q[i, b]) <= 0.5 + 1e-5).all()
+
+
 def test_q4_0_invariants(orc):
     rng = np.random.default_rng(12)
     k = 256
