@@ -239,6 +239,13 @@ int qmm_host_addressable(const void *host);
  * fma(sumi, dw*da, acc) over blocks in ascending order; the exact products
  * dw*da come from the tensor core too.  The workspace holds an fp16 copy of
  * the activations and one 16-byte activation-scale row per (block, token).
+ * For a few tokens (m <= 32, k % 256 == 0, wd 16-byte aligned) the call runs
+ * a product on the warp-level tensor-core MMA instead (mma.sync, f16
+ * operands, f32 accumulators in registers), with the same block sums and the
+ * same bits of y; its workspace holds the activations as fp16 in the MMA's
+ * fragment order (1 KB per block and 16-token tile) and their scales as f32
+ * (64 bytes per block and tile).  The workspace query covers whichever
+ * product the shape can take.
  *   wq 16-byte aligned; aq 16-byte aligned; wd, ad 2-byte aligned; y 4-byte;
  *   workspace 256-byte aligned, at least
  *   qmm_workspace_bytes(QMM_OP_GEMM_Q4_0_Q8_0, m, n, k, 0) bytes.

@@ -646,11 +646,19 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
 
 }  // namespace
 
-size_t gemm_workspace_bytes(int64_t m, int64_t /*n*/, int64_t k) { return plan_ws(m, k).total; }
+// Covers both products a Q4_0 GEMM call may launch (the few-token kernel of
+// gemm_small.cu for m <= 32, the tcgen05 kernel otherwise).
+size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+    const size_t t = plan_ws(m, k).total;
+    return gemm_small_m_supported(m, n, k) ? std::max(t, gemm_small_m_workspace_bytes(m, k)) : t;
+}
 
 void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : kDefaultWaitLimit; }
 
-void gemm_set_withhold_loads(int enable) { g_withhold_loads = enable ? 1 : 0; }
+void gemm_set_withhold_loads(int enable) {
+    g_withhold_loads = enable ? 1 : 0;
+    gemm_small_set_withhold_loads(enable);
+}
 
 cudaError_t gemm_read_and_clear_error(unsigned int *word, cudaStream_t s) {
     unsigned int zero = 0;
@@ -725,6 +733,10 @@ cudaError_t launch_gemm(const void *w, const uint16_t *wd, const int8_t *aq, con
 cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    // the few-token kernel copies dw with a tensor map, whose base must be
+    // 16-byte aligned (the entry point only asks for 2)
+    if (gemm_small_m_supported(m, n, k) && (reinterpret_cast<uintptr_t>(wd) & 15) == 0)
+        return launch_gemm_small_m(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
     return launch_gemm<32, false>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }
 

@@ -1,0 +1,560 @@
+// Q4_0 x Q8_0 product for a few tokens (m <= 32): the decode-batch and
+// small-prefill shape, where the weights stream once and the product should
+// run at the speed of the weight read.
+//
+// What it computes is the GEMM's definition (llama.cpp visual guide, lesson
+// 31 "The CPU backend", section "How the quantized dot product works"): for
+// every output y[t, n] = sum over blocks b, in ascending order, of
+// fma(sumi[t, n, b], dw[n, b] * da[t, b], acc), where sumi is the exact
+// integer dot of the 32 nibbles (minus 8) with the 32 int8 activations of
+// block b.  y is bit for bit the serial definition.
+//
+// Why not the tcgen05 GEMM here.  With 16 tokens a tcgen05 tile is
+// 128 rows x 16 columns per block, and each block needs its own TMEM
+// accumulator round trip (MMA, commit, drain, release): that chain, not the
+// weight read, sets the time.  The warp-level tensor-core MMA
+// (mma.sync m16n8k16, f16 operands, f32 accumulators) keeps the accumulators
+// in registers, so a block's sums are scaled and added the moment the two
+// MMAs return, with no hand-off at all.  Its rate (1024 MAC/clk/SM on
+// GB300) covers a 16-token product at the weight-streaming speed.
+//
+// Exactness: weights (as 1024 + nibble, see the decode) and activations
+// (-127..127, or that over 16) are exact in fp16, and every partial sum of a
+// block's MMAs, which start from an exact integer correction, is an integer
+// of magnitude below 2^23, so the f32 accumulators hold each block sum
+// exactly (tests compare the block sums bit for bit).  The scale
+// product dw * da of two fp16 values is exact in f32; it comes from one more
+// MMA per 8-token tile whose only nonzero k-slot carries dw (A) and da (B),
+// so it arrives in the same register layout as the block sums.
+//
+// Layout.  One MMA covers 16 weight rows (A, row-major) by 8 tokens (B) over
+// 16 k-slots.  Lane (g = lane / 4, c = lane % 4) holds A at rows g and g + 8,
+// k-slots 2c, 2c+1, 2c+8, 2c+9.  The k-slots of a block's first MMA are
+// mapped to its elements so that a row's four values are the low nibbles of
+// the lane's own four nibble bytes 4c..4c+3 of that row (elements 4c..4c+3),
+// and the same slots of the second MMA to their high nibbles (elements
+// 16+4c..16+4c+3).  The sum over a block does not depend on the order of its
+// elements, so this only fixes how the activations are arranged: a prepass
+// writes them as fp16 in exactly the B-fragment order of that mapping (16
+// bytes per lane, block and 8-token tile), together with the activation
+// scales as fp16 and per-token block corrections as f32.  With the weights
+// as the 16-row operand, each activation
+// fragment a warp loads from shared memory serves 16 weight rows.  Shared
+// memory delivers 128 bytes per cycle to the lanes whatever the sharing, so
+// every register a lane loads per block counts; the layouts keep that to
+// two words of weights, four words of activations per 8-token tile, one
+// word of scales and four of corrections.
+//
+// Roles: warp 8 is the producer; per stage of 8 blocks it copies a tile of
+// 128 weight rows x 128 nibble bytes (tensor copy, 128-byte swizzle, so the
+// 8 rows a lane group reads fall in 8 different bank groups), the 128 x 8 dw
+// scales (tensor copy), and the stage's activation fragments and scales
+// (bulk copies).  Warps 0..7 each own 16 weight rows for every token tile and
+// keep their accumulators in registers across the whole reduction.  CTAs
+// are persistent and walk 128-row sets (sets of 128 rows keep the last round
+// of a large product short: 1002 sets over 152 SMs is 6.6 per SM).  Every
+// mbarrier wait is bounded, as in the other kernels.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "qmm_internal.h"
+#include "tcgen05.cuh"
+
+namespace qmm {
+namespace {
+
+constexpr int kSmRows = 128;    // weight rows per row set (one stage's tile)
+constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
+constexpr int kSmWarps = 8;     // consumer warps, 16 weight rows each
+// stages of the ring: two CTAs share an SM, each within half its shared memory
+template <int MT>
+constexpr int sm_stages() { return MT == 1 ? 4 : 3; }
+constexpr int kSmThreads = 32 * (kSmWarps + 1);
+
+__device__ unsigned int g_small_error = 0;
+
+template <int MT>
+struct SmPlan {
+    static constexpr int kW = kSmRows * 128;           // nibble tile (128-byte swizzle)
+    static constexpr int kDw = kSmRows * 16;           // dw tile: 8 fp16 per row
+    static constexpr int kA = kSmBlocks * MT * 1024;   // activation fragments
+    static constexpr int kDa = kSmBlocks * MT * 128;   // block corrections and scales (f32)
+    static constexpr int kStages = sm_stages<MT>();
+    static constexpr int kOffW = 0;                    // 1024-aligned swizzled tiles
+    static constexpr int kOffDw = kOffW + kStages * kW;
+    static constexpr int kOffA = kOffDw + kStages * kDw;
+    static constexpr int kOffDa = kOffA + kStages * kA;
+    static constexpr int kOffBar = kOffDa + kStages * kDa;
+    static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;       // slack for the 1024-byte round-up
+    static_assert(kW % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+    static_assert(2 * kAlloc <= 227 * 1024, "two CTAs fit one SM's shared memory");
+};
+
+__device__ __forceinline__ bool sm_wait(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                        volatile int *abort_flag) {
+    return wait_bounded_warp_err(bar, parity, limit, abort_flag, &g_small_error, 8);
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint4 &a, uint32_t b0, uint32_t b1,
+                                          const float (&c)[4]) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+          "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+// The lane's 4 nibble bytes 4c..4c+3 of one block of one row (little-endian
+// in w) -> the row's A values of the block's two MMAs, as fp16 pairs.  A
+// nibble v becomes the fp16 pattern 0x6400 | v = 1024 + v (one mask-or, no
+// arithmetic); the 1024 + 8 offset is taken out exactly by the accumulator's
+// starting value (see the kernel).  Low nibbles (first MMA):
+//   lo_a = elements (4c, 4c+2)   (bytes 0 and 2: bits 0-3 and 16-19)
+//   lo_b = elements (4c+1, 4c+3) (bytes 1 and 3, after one 8-bit shift)
+// High nibbles (second MMA), left at bits 4-7 of their 16-bit half, i.e.
+// 1024 + 16 v: hi_a = elements (16+4c, 16+4c+2), hi_b = (16+4c+1, 16+4c+3).
+__device__ __forceinline__ void decode_lane_bytes(uint32_t w, uint32_t &lo_a, uint32_t &lo_b,
+                                                  uint32_t &hi_a, uint32_t &hi_b) {
+    const uint32_t w8 = w >> 8;
+    lo_a = (w & 0x000F000Fu) | 0x64006400u;
+    lo_b = (w8 & 0x000F000Fu) | 0x64006400u;
+    hi_a = (w & 0x00F000F0u) | 0x64006400u;
+    hi_b = (w8 & 0x00F000F0u) | 0x64006400u;
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                            int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// MT: 16-token tiles (m <= 16 MT); EMIT: write the block sums instead of y.
+template <int MT, bool EMIT>
+__global__ void __launch_bounds__(kSmThreads, 2)
+gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_dw,
+                    const uint8_t *__restrict__ afrag, const uint8_t *__restrict__ dafrag,
+                    float *__restrict__ y, int32_t *__restrict__ sumi, int m, int n, int kb_total,
+                    uint32_t wait_limit, int withhold_loads) {
+    using P = SmPlan<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + P::kOffBar);
+    uint64_t *bar_empty = bar_full + P::kStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kOffMisc);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nst = kb_total / kSmBlocks;                 // stages per row set
+    const int nsets = (n + kSmRows - 1) / kSmRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::kStages; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], kSmWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        tmap_prefetch(&tm_w);
+        if (!EMIT) tmap_prefetch(&tm_dw);
+    }
+    __syncthreads();
+
+    if (warp == kSmWarps) {
+        // ---------------------------------------------------------------- producer
+        constexpr uint32_t kTx = (uint32_t)(P::kW + P::kA + P::kDa + (EMIT ? 0 : P::kDw));
+        int it = 0;
+        bool ok = true;
+        // withhold_loads (test hook): issue nothing, so every consumer wait
+        // can only run out its poll limit
+        for (int rs = blockIdx.x; rs < (withhold_loads ? 0 : nsets) && ok; rs += gridDim.x) {
+            for (int j = 0; j < nst; ++j, ++it) {
+                const int s = it % P::kStages;
+                const uint32_t ph = (uint32_t)(it / P::kStages) & 1u;
+                if (!sm_wait(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar_full[s], kTx);
+                    tma_load_3d(smem + P::kOffW + s * P::kW, &tm_w, &bar_full[s], 0, rs * kSmRows,
+                                j * kSmBlocks);
+                    bulk_load(smem + P::kOffA + s * P::kA, afrag + (size_t)j * P::kA, P::kA, &bar_full[s]);
+                    bulk_load(smem + P::kOffDa + s * P::kDa, dafrag + (size_t)j * P::kDa, P::kDa,
+                              &bar_full[s]);
+                    if (!EMIT)
+                        tma_load_2d(smem + P::kOffDw + s * P::kDw, &tm_dw, &bar_full[s], j * kSmBlocks,
+                                    rs * kSmRows);
+                }
+                __syncwarp();
+            }
+        }
+        // Never leave a copy in flight: wait for the stages still pending.
+        for (int i = it > P::kStages ? it - P::kStages : 0; i < it; ++i) {
+            volatile int no_abort = 0;
+            sm_wait(&bar_full[i % P::kStages], (uint32_t)(i / P::kStages) & 1u, kDrainLimit, &no_abort);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    // Warp w owns weight rows 16 w .. 16 w + 15 of every row set: the MMA's A
+    // operand (16 rows), with the tokens as B in tiles of 8 (two per 16-token
+    // tile).  Lane (g, c) holds A at rows g and g + 8 and B at token g of the
+    // 8-token tile; its accumulators are rows g, g + 8 x tokens 2c, 2c + 1.
+    const int g = lane >> 2, c = lane & 3;
+    uint64_t acc[MT][2][2];  // (row g: tokens 2c, 2c+1), (row g + 8: ...)
+    int it = 0;
+    bool ok = true;
+    for (int rs = blockIdx.x; rs < nsets && ok; rs += gridDim.x) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = 0ull;
+        for (int j = 0; j < nst; ++j, ++it) {
+            const int s = it % P::kStages;
+            const uint32_t ph = (uint32_t)(it / P::kStages) & 1u;
+            if (!sm_wait(&bar_full[s], ph, wait_limit, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // weight tile laid out [block][row][16 bytes]: this lane's 4 bytes
+            // of rows g and g + 8 for block b at b * 2048 + row * 16 + 4c
+            const uint8_t *wl = smem + P::kOffW + s * P::kW + (16 * warp + g) * 16 + 4 * c;
+            const uint8_t *at = smem + P::kOffA + s * P::kA;
+            const float4 *rec = reinterpret_cast<const float4 *>(smem + P::kOffDa + s * P::kDa);
+            // dw of rows g and g + 8, the stage's 8 blocks, as f32
+            float dwf0[kSmBlocks], dwf1[kSmBlocks];
+            if (!EMIT) {
+                const uint8_t *dt = smem + P::kOffDw + s * P::kDw;
+                const uint4 r0 = *reinterpret_cast<const uint4 *>(dt + (16 * warp + g) * 16);
+                const uint4 r1 = *reinterpret_cast<const uint4 *>(dt + (16 * warp + g + 8) * 16);
+                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    __half2 h0, h1;
+                    memcpy(&h0, &w0[i], 4);
+                    memcpy(&h1, &w1[i], 4);
+                    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+                    dwf0[2 * i] = f0.x; dwf0[2 * i + 1] = f0.y;
+                    dwf1[2 * i] = f1.x; dwf1[2 * i + 1] = f1.y;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kSmBlocks; ++b) {
+                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(wl + b * 2048);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(wl + b * 2048 + 8 * 16);
+                uint32_t la0, lb0, ha0, hb0, la1, lb1, ha1, hb1;
+                decode_lane_bytes(w0, la0, lb0, ha0, hb0);
+                decode_lane_bytes(w1, la1, lb1, ha1, hb1);
+                // A registers: (row g, slots 2c..), (row g+8, 2c..), (row g, 2c+8..),
+                // (row g+8, 2c+8..); slots 2c, 2c+1, 2c+8, 2c+9 of the first MMA
+                // hold elements 4c, 4c+2, 4c+1, 4c+3, of the second 16 more
+                const uint4 a_lo = make_uint4(la0, la1, lb0, lb1);
+                const uint4 a_hi = make_uint4(ha0, ha1, hb0, hb1);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    // activation fragments of (block b, tile mt): two 512-byte
+                    // pieces (tokens 0..7, 8..15), lane-contiguous 16 bytes
+                    const uint4 *af = reinterpret_cast<const uint4 *>(at + (b * MT + mt) * 1024);
+                    // corrections and scales of tokens 2c, 2c+1 of both 8-token tiles
+                    const float4 cor = rec[(b * MT + mt) * 8 + c];
+                    const float4 da = EMIT ? make_float4(0.f, 0.f, 0.f, 0.f) : rec[(b * MT + mt) * 8 + 4 + c];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const uint4 bf = af[32 * nt + lane];
+                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                        float d[4];
+                        mma_16816(d, a_lo, bf.x, bf.y, zero);
+                        mma_16816(d, a_hi, bf.z, bf.w, d);
+                        // the block sums: add the tokens' corrections (exact, integers)
+                        const uint64_t corp = nt ? f2_pack(cor.z, cor.w) : f2_pack(cor.x, cor.y);
+                        const uint64_t s0 = f2_add(f2_pack(d[0], d[1]), corp);  // row g
+                        const uint64_t s1 = f2_add(f2_pack(d[2], d[3]), corp);  // row g + 8
+                        if constexpr (EMIT) {
+                            const int kbi = j * kSmBlocks + b;
+                            const int t0 = mt * 16 + nt * 8 + 2 * c;
+                            const int n0 = rs * kSmRows + 16 * warp + g;
+                            float v[4];
+                            f2_unpack(s0, v[0], v[1]);
+                            f2_unpack(s1, v[2], v[3]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int t = t0 + (i & 1);
+                                const int nn = n0 + 8 * (i >> 1);
+                                if (t < m && nn < n)
+                                    sumi[((int64_t)t * n + nn) * kb_total + kbi] = __float2int_rn(v[i]);
+                            }
+                        } else {
+                            // S = dw * da (exact); acc = fma(sumi, S, acc), two
+                            // outputs per instruction
+                            const uint64_t dap = nt ? f2_pack(da.z, da.w) : f2_pack(da.x, da.y);
+                            const uint64_t sc0 = f2_mul(f2_pack(dwf0[b], dwf0[b]), dap);
+                            const uint64_t sc1 = f2_mul(f2_pack(dwf1[b], dwf1[b]), dap);
+                            acc[mt][nt][0] = f2_fma(s0, sc0, acc[mt][nt][0]);
+                            acc[mt][nt][1] = f2_fma(s1, sc1, acc[mt][nt][1]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_empty[s]);
+        }
+        if (!EMIT && ok) {
+            const int n0 = rs * kSmRows + 16 * warp + g;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        float v[2];
+                        f2_unpack(acc[mt][nt][r], v[0], v[1]);
+                        const int nn = n0 + 8 * r;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int t = mt * 16 + nt * 8 + 2 * c + i;
+                            if (t < m && nn < n) y[(int64_t)t * n + nn] = v[i];
+                        }
+                    }
+        }
+    }
+}
+
+// Activation prepass, in the B-fragment order of the kernel above.  Per
+// block b and 16-token tile mt, 1 KB in two 512-byte pieces, one per 8-token
+// tile nt; lane l = 4 g + c owns 16 bytes of piece nt at l * 16, for token
+// t = mt * 16 + nt * 8 + g: the first MMA's registers (a[4c], a[4c+2]) and
+// (a[4c+1], a[4c+3]), then the second's (a[16+4c] / 16, a[16+4c+2] / 16) and
+// (a[16+4c+1] / 16, a[16+4c+3] / 16), all exact in fp16 (a = the int8 code
+// of element e of block b).  The first MMA sees the weights as 1024 + v and
+// the second as 1024 + 16 v against activations scaled by 1/16, i.e. 64 + v,
+// so a block's two MMAs sum (v - 8) a exactly once the accumulator starts at
+//   cor[t] = -1032 * (a[0] + .. + a[15]) - 72 * (a[16] + .. + a[31])
+// (every partial sum is an integer below 2^24 in magnitude).  Then a
+// 128-byte record per (b, mt): for c = 0..3 the f32 corrections of tokens
+// (nt0: 2c, 2c+1, nt1: 2c, 2c+1), then for c = 0..3 their scales da as f32.
+// Tokens past m are zeros.
+__global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
+                                       uint4 *__restrict__ afrag, uint8_t *__restrict__ rec,
+                                       int64_t m, int64_t k, int mt_count) {
+    const int64_t kb = k / kQK;
+    const int64_t units = kb * mt_count * 64;  // (block, tile, piece, lane)
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const __half sixteenth = __float2half_rn(0.0625f);
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int lane = (int)(u & 31);
+        const int nt = (int)((u >> 5) & 1);
+        const int64_t bm = u >> 6;                 // b * mt_count + mt
+        const int mt = (int)(bm % mt_count);
+        const int64_t b = bm / mt_count;
+        const int g = lane >> 2, c = lane & 3;
+        const int64_t t = mt * 16 + nt * 8 + g;
+        uint32_t reg[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t q = 0;  // four int8 codes of token t at elements 16 half + 4c ..
+            if (t < m) q = *reinterpret_cast<const uint32_t *>(aq + t * k + b * kQK + 16 * half + 4 * c);
+            __half h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[i] = __int2half_rn((int)(int8_t)((q >> (8 * i)) & 0xff));
+                if (half) h[i] = __hmul(h[i], sixteenth);  // exact: a power of two
+            }
+            reg[2 * half] = h2_bits(__halves2half2(h[0], h[2]));
+            reg[2 * half + 1] = h2_bits(__halves2half2(h[1], h[3]));
+        }
+        afrag[u] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+        uint8_t *r = rec + bm * 128;
+        if (nt == 0 && g == 0) {
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t tt = mt * 16 + (i >> 1) * 8 + 2 * c + (i & 1);
+                int lo = 0, hi = 0;
+                if (tt < m)
+                    for (int e = 0; e < 16; ++e) {
+                        lo += aq[tt * k + b * kQK + e];
+                        hi += aq[tt * k + b * kQK + 16 + e];
+                    }
+                v[i] = (float)(-1032 * lo - 72 * hi);
+            }
+            reinterpret_cast<float4 *>(r)[c] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        if (nt == 1 && g == 0) {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (ad) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t tt = mt * 16 + (i >> 1) * 8 + 2 * c + (i & 1);
+                    if (tt < m) v[i] = __half2float(__ushort_as_half(ad[tt * kb + b]));
+                }
+            }
+            reinterpret_cast<float4 *>(r + 64)[c] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+}
+
+uint32_t g_small_wait_limit = kDefaultWaitLimit;
+int g_small_withhold = 0;
+
+int num_sms() {
+    static int count = 0;
+    if (count == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            count = v;
+        else
+            return 152;
+    }
+    return count;
+}
+
+// The nibble plane u8 [n, k/2] as a 3-D tensor (16 bytes of a block, row,
+// block) with byte strides (1, k/2, 16); box 16 x 128 x 8.
+bool make_map_3d_blocks(CUtensorMap *map, const void *wq, uint64_t n, uint64_t kb, uint64_t row_bytes) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {16, n, kb};
+    const cuuint64_t strides[2] = {row_bytes, 16};
+    const cuuint32_t box[3] = {16, (cuuint32_t)kSmRows, (cuuint32_t)kSmBlocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(wq), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MT, bool EMIT>
+cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, const uint8_t *afrag,
+                              const uint8_t *dafrag, float *y, int32_t *sumi, int64_t m, int64_t n,
+                              int64_t k, cudaStream_t s) {
+    using P = SmPlan<MT>;
+    auto kern = gemm_small_m_kernel<MT, EMIT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
+    if (e != cudaSuccess) return e;
+    const int64_t nsets = (n + kSmRows - 1) / kSmRows;
+    const int grid = (int)std::min<int64_t>(nsets, 2 * num_sms());
+    kern<<<grid, kSmThreads, P::kAlloc, s>>>(tw, tdw, afrag, dafrag, y, sumi, (int)m, (int)n,
+                                             (int)(k / kQK), g_small_wait_limit, g_small_withhold);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+bool gemm_small_m_supported(int64_t m, int64_t /*n*/, int64_t k) {
+    return m >= 1 && m <= 32 && k % (kQK * kSmBlocks) == 0;
+}
+
+size_t gemm_small_m_workspace_bytes(int64_t m, int64_t k) {
+    const int64_t mt = (m + 15) / 16;
+    const int64_t kb = k / kQK;
+    const size_t a = (size_t)(kb * mt * 1024);
+    return (a + 255) / 256 * 256 + (size_t)(kb * mt * 128);
+}
+
+void gemm_small_set_wait_limit(uint32_t iterations) {
+    g_small_wait_limit = iterations ? iterations : kDefaultWaitLimit;
+}
+
+void gemm_small_set_withhold_loads(int enable) { g_small_withhold = enable ? 1 : 0; }
+
+cudaError_t gemm_small_read_and_clear_error(unsigned int *word, cudaStream_t s) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_small_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*word) {
+        e = cudaMemcpyToSymbolAsync(g_small_error, &zero, sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+// wd / ad may be null (block-sum variant, sumi != null).
+cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
+                                int64_t k, void *workspace, cudaStream_t s) {
+    const int mt = (int)((m + 15) / 16);
+    const int64_t kb = k / kQK;
+    auto *ws = static_cast<uint8_t *>(workspace);
+    const size_t a_bytes = (size_t)(kb * mt * 1024);
+    uint8_t *afrag = ws;
+    uint8_t *dafrag = ws + (a_bytes + 255) / 256 * 256;
+    {
+        const int threads = 256;
+        const int64_t units = kb * mt * 64;
+        const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 152 * 8);
+        gemm_small_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(
+            aq, reinterpret_cast<const unsigned short *>(sumi ? nullptr : ad),
+            reinterpret_cast<uint4 *>(afrag), dafrag, m, k, mt);
+        cudaError_t e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap tw, tdw;
+    // nibbles viewed as u8 [blocks][n rows][16 bytes] (strides 16 and k/2
+    // bytes), box 16 x 128 rows x 8 blocks: the tile lands as [block][row][16]
+    if (!make_map_3d_blocks(&tw, wq, (uint64_t)n, (uint64_t)kb, (uint64_t)(k / 2)))
+        return cudaErrorInvalidValue;
+    // dw: fp16 [n rows, k/32], box 8 x 128 (the block-sum variant reads none
+    // and maps the nibbles again as a placeholder)
+    if (sumi) {
+        tdw = tw;
+    } else if (!make_map_2d(&tdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wd, (uint64_t)kb, (uint64_t)n,
+                            (uint64_t)kb * 2, kSmBlocks, kSmRows, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        return cudaErrorInvalidValue;
+    }
+    if (mt == 1)
+        return sumi ? launch_small_tile<1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                    : launch_small_tile<1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+    return sumi ? launch_small_tile<2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                : launch_small_tile<2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+}
+
+}  // namespace qmm

@@ -429,13 +429,15 @@ int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k) {
 }
 
 qmm_status qmm_check_device_error(void *stream) {
-    unsigned int word = 0, word2 = 0, word3 = 0;
+    unsigned int word = 0, word2 = 0, word3 = 0, word4 = 0;
     if (qmm::gemm_read_and_clear_error(&word, as_stream(stream)) != cudaSuccess) return QMM_ERR_CUDA;
+    if (qmm::gemm_small_read_and_clear_error(&word4, as_stream(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
     if (qmm::stream_read_and_clear_error(&word2, as_stream(stream)) != cudaSuccess)
         return QMM_ERR_CUDA;
     if (qmm::bitnet_gemm_read_and_clear_error(&word3, as_stream(stream)) != cudaSuccess)
         return QMM_ERR_CUDA;
-    return (word | word2 | word3) ? QMM_ERR_TIMEOUT : QMM_OK;
+    return (word | word2 | word3 | word4) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 const char *qmm_status_string(qmm_status status) {
@@ -528,6 +530,7 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
 
 void qmm_debug_set_wait_limit(uint32_t iterations) {
     qmm::gemm_set_wait_limit(iterations);
+    qmm::gemm_small_set_wait_limit(iterations);
     qmm::stream_set_wait_limit(iterations);
     qmm::bitnet_gemm_set_wait_limit(iterations);
 }

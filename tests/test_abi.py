@@ -71,7 +71,17 @@ def test_workspace_queries(lib):
     m = 3
     a16 = (m * k * 2 + 255) // 256 * 256
     rows = ((k // 32) * 4 * 16 + 255) // 256 * 256
-    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == a16 + rows
+    # m <= 32 with k a multiple of 256 may run the few-token product: fp16
+    # activation fragments (1 KB per block and 16-token tile) + f32 scale
+    # pairs (64 B per block and tile); the query covers the larger layout
+    frags = (k // 32) * 1024
+    pairs = (k // 32) * 64
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == max(a16 + rows, frags + pairs)
+    assert lib.qmm_workspace_bytes(2, 32, 14336, k, 0) == max(32 * k * 2 + (k // 32) * 32 * 16,
+                                                               2 * (frags + pairs))
+    k = 4064  # not a multiple of 256: the tcgen05 product only
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == (
+        (m * k * 2 + 255) // 256 * 256 + ((k // 32) * 4 * 16 + 255) // 256 * 256)
     bad = ctypes.c_size_t(-1).value
     assert lib.qmm_workspace_bytes(9, 1, 1, 32, 0) == bad        # unknown op
     assert lib.qmm_workspace_bytes(1, 1, 1, 33, 0) == bad        # k not a block multiple

@@ -167,6 +167,57 @@ def test_gemm_more_tiles_than_resident_ctas(qmm, orc, m, n, k):
         assert np.array_equal(sumi, orc.block_sums(wq, aq))
 
 
+# The few-token product (m <= 32, k a multiple of 256: warp-level MMAs with
+# register accumulators, persistent CTAs over 128-row sets): one and two
+# 16-token tiles, ragged row sets, more row sets than SMs, long reductions.
+GEMM_SMALL_SHAPES = [(1, 1, 256), (8, 129, 512), (16, 128, 4096), (16, 257, 2048),
+                     (17, 300, 768), (31, 1000, 1024), (32, 128 * 152 * 2 + 77, 256),
+                     (20, 65, 11008)]
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SMALL_SHAPES)
+def test_gemm_small_m_block_sums_and_y_bit_exact(qmm, orc, m, n, k):
+    wq, wd, aq, ad = q4_case(orc, 8100 + m + n, m, n, k)
+    dwq, daq = to_dev(wq), to_dev(aq)
+    sumi = to_np(qmm.debug_block_sums(1, dwq, daq))
+    assert np.array_equal(sumi, orc.block_sums(wq, aq))
+    y = to_np(qmm.gemm_q4_0_q8_0(dwq, to_dev(wd.view(np.float16)), daq, to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q4_0_q8_0(wq, wd, aq, ad).view(np.uint32))
+
+
+def test_gemm_small_m_adversarial_activations_bit_exact(qmm, orc):
+    m, n, k = 16, 200, 1024
+    wq, wd, _, _ = q4_case(orc, 8200, m, n, k)
+    x = adversarial_x(8201, m, k)
+    aq, ad = orc.quantize_q8_0(x)
+    y = to_np(qmm.gemm_q4_0_q8_0(to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq),
+                                 to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q4_0_q8_0(wq, wd, aq, ad).view(np.uint32))
+
+
+def test_gemm_small_m_wait_timeout_reports_and_device_stays_usable(qmm, orc):
+    """The few-token product with its stages never armed: every bounded wait
+    runs out, QMM_ERR_TIMEOUT is recorded, and the next call is exact."""
+    import torch
+    wq, wd, aq, ad = q4_case(orc, 8300, 16, 300, 1024)
+    args = (to_dev(wq), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    assert qmm.check_device_error() == 0
+    try:
+        qmm.set_wait_limit(2000)
+        qmm.withhold_gemm_loads(True)
+        qmm.gemm_q4_0_q8_0(*args)
+        torch.cuda.synchronize()
+        status = qmm.check_device_error()
+    finally:
+        qmm.withhold_gemm_loads(False)
+        qmm.set_wait_limit(0)
+    assert status == 7
+    y = to_np(qmm.gemm_q4_0_q8_0(*args))
+    torch.cuda.synchronize()
+    assert qmm.check_device_error() == 0
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q4_0_q8_0(wq, wd, aq, ad).view(np.uint32))
+
+
 def test_gemm_and_gemv_agree_with_adversarial_activations(qmm, orc):
     m, n, k = 9, 200, 4096
     w, _ = synthetic.q4_0_case(61, n, k, 1)
