@@ -243,8 +243,8 @@ int qmm_host_addressable(const void *host);
  * a product on the warp-level tensor-core MMA instead (mma.sync, f16
  * operands, f32 accumulators in registers), with the same block sums and the
  * same bits of y; its workspace holds the activations as fp16 in the MMA's
- * fragment order (1 KB per block and 16-token tile) and their scales as f32
- * (64 bytes per block and tile).  The workspace query covers whichever
+ * fragment order (1 KB per block and 16-token tile) and, per block and tile,
+ * a 128-byte record of per-token block corrections and scales (f32).  The workspace query covers whichever
  * product the shape can take.
  *   wq 16-byte aligned; aq 16-byte aligned; wd, ad 2-byte aligned; y 4-byte;
  *   workspace 256-byte aligned, at least
