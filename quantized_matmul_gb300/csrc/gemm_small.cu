@@ -45,12 +45,14 @@
 // two words of weights, four words of activations per 8-token tile, one
 // word of scales and four of corrections.
 //
-// Roles: warp 8 is the producer; per stage of 8 blocks it copies a tile of
+// Roles: warp 4 is the producer; per stage of 8 blocks it copies a tile of
 // 128 weight rows x 128 nibble bytes (tensor copy, 128-byte swizzle, so the
-// 8 rows a lane group reads fall in 8 different bank groups), the 128 x 8 dw
-// scales (tensor copy), and the stage's activation fragments and scales
-// (bulk copies).  Warps 0..7 each own 16 weight rows for every token tile and
-// keep their accumulators in registers across the whole reduction.  CTAs
+// 8 rows a lane group reads fall in 8 different bank groups; a 3-D copy that
+// lands the tile as [block][row][16 bytes] moved 16-byte pieces and streamed
+// a third slower), the 128 x 8 dw scales (tensor copy), and the stage's
+// activation fragments, corrections and scales (bulk copies).  Warps 0..3
+// each own 32 weight rows for every token tile and keep their accumulators in
+// registers across the whole reduction; two CTAs share an SM.  CTAs
 // are persistent and walk 128-row sets (sets of 128 rows keep the last round
 // of a large product short: 1002 sets over 152 SMs is 6.6 per SM).  Every
 // mbarrier wait is bounded, as in the other kernels.
@@ -68,7 +70,7 @@ namespace {
 
 constexpr int kSmRows = 128;    // weight rows per row set (one stage's tile)
 constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
-constexpr int kSmWarps = 8;     // consumer warps, 16 weight rows each
+constexpr int kSmWarps = 4;     // consumer warps, 32 weight rows (two 16-row units) each
 // stages of the ring: two CTAs share an SM, each within half its shared memory
 template <int MT>
 constexpr int sm_stages() { return MT == 1 ? 4 : 3; }
@@ -162,17 +164,10 @@ __device__ __forceinline__ void decode_lane_bytes(uint32_t w, uint32_t &lo_a, ui
     hi_b = (w8 & 0x00F000F0u) | 0x64006400u;
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
-                                            int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// MT: 16-token tiles (m <= 16 MT); EMIT: write the block sums instead of y.
-template <int MT, bool EMIT>
+// MT: 16-token tiles (m <= 16 MT); NT: 8-token tiles used per 16-token tile
+// (1 when m <= 8: the second would hold only padding); EMIT: write the block
+// sums instead of y.
+template <int MT, int NT, bool EMIT>
 __global__ void __launch_bounds__(kSmThreads, 2)
 gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_dw,
                     const uint8_t *__restrict__ afrag, const uint8_t *__restrict__ dafrag,
@@ -220,8 +215,7 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bar_full[s], kTx);
-                    tma_load_3d(smem + P::kOffW + s * P::kW, &tm_w, &bar_full[s], 0, rs * kSmRows,
-                                j * kSmBlocks);
+                    tma_load_2d(smem + P::kOffW + s * P::kW, &tm_w, &bar_full[s], j * 128, rs * kSmRows);
                     bulk_load(smem + P::kOffA + s * P::kA, afrag + (size_t)j * P::kA, P::kA, &bar_full[s]);
                     bulk_load(smem + P::kOffDa + s * P::kDa, dafrag + (size_t)j * P::kDa, P::kDa,
                               &bar_full[s]);
@@ -241,19 +235,23 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
     }
 
     // -------------------------------------------------------------------- consumers
-    // Warp w owns weight rows 16 w .. 16 w + 15 of every row set: the MMA's A
-    // operand (16 rows), with the tokens as B in tiles of 8 (two per 16-token
-    // tile).  Lane (g, c) holds A at rows g and g + 8 and B at token g of the
-    // 8-token tile; its accumulators are rows g, g + 8 x tokens 2c, 2c + 1.
+    // Warp w owns weight rows 32 w .. 32 w + 31 of every row set, as two
+    // units of 16 rows (u = 0, 1).  A unit is the MMA's A operand (16 rows),
+    // with the tokens as B in tiles of 8 (two per 16-token tile); both units
+    // use the same activation fragments, loaded once per block.  Lane (g, c)
+    // holds A at rows g and g + 8 of a unit and B at token g of the 8-token
+    // tile; its accumulators are rows g, g + 8 x tokens 2c, 2c + 1.
     const int g = lane >> 2, c = lane & 3;
-    uint64_t acc[MT][2][2];  // (row g: tokens 2c, 2c+1), (row g + 8: ...)
+    uint64_t acc[2][MT][NT][2];  // [unit][tile][8-token tile][row g | row g + 8], token pairs
     int it = 0;
     bool ok = true;
     for (int rs = blockIdx.x; rs < nsets && ok; rs += gridDim.x) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = 0ull;
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[u][mt][nt][0] = acc[u][mt][nt][1] = 0ull;
         for (int j = 0; j < nst; ++j, ++it) {
             const int s = it % P::kStages;
             const uint32_t ph = (uint32_t)(it / P::kStages) & 1u;
@@ -261,40 +259,55 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                 ok = false;
                 break;
             }
-            // weight tile laid out [block][row][16 bytes]: this lane's 4 bytes
-            // of rows g and g + 8 for block b at b * 2048 + row * 16 + 4c
-            const uint8_t *wl = smem + P::kOffW + s * P::kW + (16 * warp + g) * 16 + 4 * c;
+            // weight tile: 128 rows of 128 bytes under the 128-byte swizzle,
+            // chunk b of row r at chunk b ^ (r % 8).  This lane's rows all have
+            // r % 8 = g, and the offset r * 128 + 4c has bits 4..6 clear, so
+            // the lane's 4 bytes of row r, block b sit at
+            // (r * 128 + 4c + 16 g) ^ (16 b): one XOR per row and block.
+            const uint8_t *wt = smem + P::kOffW + s * P::kW;
+            const uint32_t wl = (32 * warp + g) * 128 + 4 * c + 16 * g;
             const uint8_t *at = smem + P::kOffA + s * P::kA;
             const float4 *rec = reinterpret_cast<const float4 *>(smem + P::kOffDa + s * P::kDa);
-            // dw of rows g and g + 8, the stage's 8 blocks, as f32
-            float dwf0[kSmBlocks], dwf1[kSmBlocks];
+            // dw of rows g and g + 8 of both units, the stage's 8 blocks (fp16 pairs)
+            uint4 dwr[2][2];
             if (!EMIT) {
-                const uint8_t *dt = smem + P::kOffDw + s * P::kDw;
-                const uint4 r0 = *reinterpret_cast<const uint4 *>(dt + (16 * warp + g) * 16);
-                const uint4 r1 = *reinterpret_cast<const uint4 *>(dt + (16 * warp + g + 8) * 16);
-                const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+                const uint8_t *dt = smem + P::kOffDw + s * P::kDw + (32 * warp + g) * 16;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    __half2 h0, h1;
-                    memcpy(&h0, &w0[i], 4);
-                    memcpy(&h1, &w1[i], 4);
-                    const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-                    dwf0[2 * i] = f0.x; dwf0[2 * i + 1] = f0.y;
-                    dwf1[2 * i] = f1.x; dwf1[2 * i + 1] = f1.y;
-                }
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        dwr[u][h] = *reinterpret_cast<const uint4 *>(dt + (16 * u + 8 * h) * 16);
             }
 #pragma unroll
             for (int b = 0; b < kSmBlocks; ++b) {
-                const uint32_t w0 = *reinterpret_cast<const uint32_t *>(wl + b * 2048);
-                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(wl + b * 2048 + 8 * 16);
-                uint32_t la0, lb0, ha0, hb0, la1, lb1, ha1, hb1;
-                decode_lane_bytes(w0, la0, lb0, ha0, hb0);
-                decode_lane_bytes(w1, la1, lb1, ha1, hb1);
-                // A registers: (row g, slots 2c..), (row g+8, 2c..), (row g, 2c+8..),
-                // (row g+8, 2c+8..); slots 2c, 2c+1, 2c+8, 2c+9 of the first MMA
-                // hold elements 4c, 4c+2, 4c+1, 4c+3, of the second 16 more
-                const uint4 a_lo = make_uint4(la0, la1, lb0, lb1);
-                const uint4 a_hi = make_uint4(ha0, ha1, hb0, hb1);
+                uint4 a_lo[2], a_hi[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u) * 128) ^ (16u * b)));
+                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u + 8) * 128) ^ (16u * b)));
+                    uint32_t la0, lb0, ha0, hb0, la1, lb1, ha1, hb1;
+                    decode_lane_bytes(w0, la0, lb0, ha0, hb0);
+                    decode_lane_bytes(w1, la1, lb1, ha1, hb1);
+                    // A registers: (row g, slots 2c..), (row g+8, 2c..), (row g,
+                    // 2c+8..), (row g+8, 2c+8..); slots 2c, 2c+1, 2c+8, 2c+9 of
+                    // the first MMA hold elements 4c, 4c+2, 4c+1, 4c+3, of the
+                    // second 16 more
+                    a_lo[u] = make_uint4(la0, la1, lb0, lb1);
+                    a_hi[u] = make_uint4(ha0, ha1, hb0, hb1);
+                }
+                // dw of the units' rows g, g + 8 for block b, as f32 pairs (dw, dw)
+                uint64_t dwp[2][2];
+                if (!EMIT) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t wv = (&dwr[u][h].x)[b >> 1];
+                            const float f = __half2float(__ushort_as_half(
+                                (unsigned short)((b & 1) ? (wv >> 16) : (wv & 0xFFFFu))));
+                            dwp[u][h] = f2_pack(f, f);
+                        }
+                }
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     // activation fragments of (block b, tile mt): two 512-byte
@@ -304,38 +317,39 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                     const float4 cor = rec[(b * MT + mt) * 8 + c];
                     const float4 da = EMIT ? make_float4(0.f, 0.f, 0.f, 0.f) : rec[(b * MT + mt) * 8 + 4 + c];
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
+                    for (int nt = 0; nt < NT; ++nt) {
                         const uint4 bf = af[32 * nt + lane];
-                        const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-                        float d[4];
-                        mma_16816(d, a_lo, bf.x, bf.y, zero);
-                        mma_16816(d, a_hi, bf.z, bf.w, d);
-                        // the block sums: add the tokens' corrections (exact, integers)
                         const uint64_t corp = nt ? f2_pack(cor.z, cor.w) : f2_pack(cor.x, cor.y);
-                        const uint64_t s0 = f2_add(f2_pack(d[0], d[1]), corp);  // row g
-                        const uint64_t s1 = f2_add(f2_pack(d[2], d[3]), corp);  // row g + 8
-                        if constexpr (EMIT) {
-                            const int kbi = j * kSmBlocks + b;
-                            const int t0 = mt * 16 + nt * 8 + 2 * c;
-                            const int n0 = rs * kSmRows + 16 * warp + g;
-                            float v[4];
-                            f2_unpack(s0, v[0], v[1]);
-                            f2_unpack(s1, v[2], v[3]);
+                        const uint64_t dap = nt ? f2_pack(da.z, da.w) : f2_pack(da.x, da.y);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int t = t0 + (i & 1);
-                                const int nn = n0 + 8 * (i >> 1);
-                                if (t < m && nn < n)
-                                    sumi[((int64_t)t * n + nn) * kb_total + kbi] = __float2int_rn(v[i]);
+                        for (int u = 0; u < 2; ++u) {
+                            const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+                            float d[4];
+                            mma_16816(d, a_lo[u], bf.x, bf.y, zero);
+                            mma_16816(d, a_hi[u], bf.z, bf.w, d);
+                            // the block sums: add the tokens' corrections (exact, integers)
+                            const uint64_t s0 = f2_add(f2_pack(d[0], d[1]), corp);  // row g
+                            const uint64_t s1 = f2_add(f2_pack(d[2], d[3]), corp);  // row g + 8
+                            if constexpr (EMIT) {
+                                const int kbi = j * kSmBlocks + b;
+                                const int t0 = mt * 16 + nt * 8 + 2 * c;
+                                const int n0 = rs * kSmRows + 32 * warp + 16 * u + g;
+                                float v[4];
+                                f2_unpack(s0, v[0], v[1]);
+                                f2_unpack(s1, v[2], v[3]);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int t = t0 + (i & 1);
+                                    const int nn = n0 + 8 * (i >> 1);
+                                    if (t < m && nn < n)
+                                        sumi[((int64_t)t * n + nn) * kb_total + kbi] = __float2int_rn(v[i]);
+                                }
+                            } else {
+                                // S = dw * da (exact); acc = fma(sumi, S, acc), two
+                                // outputs per instruction
+                                acc[u][mt][nt][0] = f2_fma(s0, f2_mul(dwp[u][0], dap), acc[u][mt][nt][0]);
+                                acc[u][mt][nt][1] = f2_fma(s1, f2_mul(dwp[u][1], dap), acc[u][mt][nt][1]);
                             }
-                        } else {
-                            // S = dw * da (exact); acc = fma(sumi, S, acc), two
-                            // outputs per instruction
-                            const uint64_t dap = nt ? f2_pack(da.z, da.w) : f2_pack(da.x, da.y);
-                            const uint64_t sc0 = f2_mul(f2_pack(dwf0[b], dwf0[b]), dap);
-                            const uint64_t sc1 = f2_mul(f2_pack(dwf1[b], dwf1[b]), dap);
-                            acc[mt][nt][0] = f2_fma(s0, sc0, acc[mt][nt][0]);
-                            acc[mt][nt][1] = f2_fma(s1, sc1, acc[mt][nt][1]);
                         }
                     }
                 }
@@ -344,22 +358,25 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
             if (lane == 0) mbar_arrive(&bar_empty[s]);
         }
         if (!EMIT && ok) {
-            const int n0 = rs * kSmRows + 16 * warp + g;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int u = 0; u < 2; ++u) {
+                const int n0 = rs * kSmRows + 32 * warp + 16 * u + g;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        float v[2];
-                        f2_unpack(acc[mt][nt][r], v[0], v[1]);
-                        const int nn = n0 + 8 * r;
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const int t = mt * 16 + nt * 8 + 2 * c + i;
-                            if (t < m && nn < n) y[(int64_t)t * n + nn] = v[i];
+                        for (int r = 0; r < 2; ++r) {
+                            float v[2];
+                            f2_unpack(acc[u][mt][nt][r], v[0], v[1]);
+                            const int nn = n0 + 8 * r;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const int t = mt * 16 + nt * 8 + 2 * c + i;
+                                if (t < m && nn < n) y[(int64_t)t * n + nn] = v[i];
+                            }
                         }
-                    }
+            }
         }
     }
 }
@@ -454,26 +471,12 @@ int num_sms() {
     return count;
 }
 
-// The nibble plane u8 [n, k/2] as a 3-D tensor (16 bytes of a block, row,
-// block) with byte strides (1, k/2, 16); box 16 x 128 x 8.
-bool make_map_3d_blocks(CUtensorMap *map, const void *wq, uint64_t n, uint64_t kb, uint64_t row_bytes) {
-    auto fn = get_encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {16, n, kb};
-    const cuuint64_t strides[2] = {row_bytes, 16};
-    const cuuint32_t box[3] = {16, (cuuint32_t)kSmRows, (cuuint32_t)kSmBlocks};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(wq), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int MT, bool EMIT>
+template <int MT, int NT, bool EMIT>
 cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, const uint8_t *afrag,
                               const uint8_t *dafrag, float *y, int32_t *sumi, int64_t m, int64_t n,
                               int64_t k, cudaStream_t s) {
     using P = SmPlan<MT>;
-    auto kern = gemm_small_m_kernel<MT, EMIT>;
+    auto kern = gemm_small_m_kernel<MT, NT, EMIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
     const int64_t nsets = (n + kSmRows - 1) / kSmRows;
@@ -538,9 +541,9 @@ cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tw, tdw;
-    // nibbles viewed as u8 [blocks][n rows][16 bytes] (strides 16 and k/2
-    // bytes), box 16 x 128 rows x 8 blocks: the tile lands as [block][row][16]
-    if (!make_map_3d_blocks(&tw, wq, (uint64_t)n, (uint64_t)kb, (uint64_t)(k / 2)))
+    // nibbles: u8 [n rows, k/2 bytes], box 128 bytes x 128 rows, 128-byte swizzle
+    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)(k / 2), (uint64_t)n,
+                     (uint64_t)(k / 2), 128, kSmRows, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // dw: fp16 [n rows, k/32], box 8 x 128 (the block-sum variant reads none
     // and maps the nibbles again as a placeholder)
@@ -550,11 +553,16 @@ cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int
                             (uint64_t)kb * 2, kSmBlocks, kSmRows, CU_TENSOR_MAP_SWIZZLE_NONE)) {
         return cudaErrorInvalidValue;
     }
+    // m <= 8 runs one 8-token tile per block (measured 74 against 94 us at
+    // the vocabulary shape)
+    if (m <= 8)
+        return sumi ? launch_small_tile<1, 1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                    : launch_small_tile<1, 1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
     if (mt == 1)
-        return sumi ? launch_small_tile<1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                    : launch_small_tile<1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
-    return sumi ? launch_small_tile<2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                : launch_small_tile<2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+        return sumi ? launch_small_tile<1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                    : launch_small_tile<1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+    return sumi ? launch_small_tile<2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                : launch_small_tile<2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
 }
 
 }  // namespace qmm
