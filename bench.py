@@ -43,6 +43,9 @@ import numpy as np  # noqa: E402
 QK = 32
 L2_BYTES = 129 * 10**6
 METRIC = "decode GEMV achieved HBM GB/s (% of peak); prefill GEMM int8 TOPS (% of peak)"
+# the GB300's nominal HBM3e bandwidth (~8 TB/s); fractions are reported against
+# it beside the measured copy peak
+NOMINAL_HBM_GBS = 8000.0
 LAYER_SET = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]  # (N, K), seeds 1..7
 WORKLOAD_C2 = ("Q4_0xQ8_0 decode GEMV over a 7B-style layer set, m=1: K=4096 -> N in "
                "{4096 x4, 11008 x2}, K=11008 -> N=4096; weights ~N(0,0.02) seeds 1-7, "
@@ -75,7 +78,14 @@ def linear_bytes(m, n, k):
 
 
 def bitnet_bytes(m, n, k):
+    """Ternary GEMV: packed codes + int8 activations, scale and sum + f32 output."""
     return n * k // 4 + m * k + 8 * m + 4 * m * n
+
+
+def bitnet_step_bytes(m, n, k):
+    """BitNet decode layer as a whole: packed codes + f32 activations in +
+    f32 output (the int8 intermediate is not counted)."""
+    return n * k // 4 + 4 * m * k + 4 * m * n
 
 
 def copies_for(bytes_per_copy):
@@ -246,22 +256,39 @@ class GraphTimer:
         if k % self.rot:
             self._tail(k % self.rot).replay()
 
-    def time(self, k: int, warmup: int, dist: Dist, sampler: ClockSampler | None = None):
+    def time(self, k: int, warmup: int, dist: Dist, sampler: ClockSampler | None = None,
+             settle_s: float = 0.6):
+        """Times exactly k steps after `warmup` untimed ones.  With a clock
+        sampler, nvidia-smi samples from just before an untimed block of
+        replays of about settle_s seconds (which runs right before the timed
+        region) until the timed region ends, so a short timed region still
+        has clock samples taken under the same load at the same moment."""
         torch = self.torch
         if k % self.rot:
             self._tail(k % self.rot)
         self.run(max(warmup, 1))
         torch.cuda.synchronize()
+        settle = 0
+        if sampler:
+            t0 = time.perf_counter()
+            self.run(self.rot)
+            torch.cuda.synchronize()
+            per_step = max((time.perf_counter() - t0) / self.rot, 1e-7)
+            settle = int(settle_s / per_step) // self.rot * self.rot
         dist.barrier()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         if sampler:
             sampler.start()
+            self.run(settle)
         start.record()
         self.run(k)
         end.record()
         torch.cuda.synchronize()
         clocks = sampler.stop() if sampler else None
+        if clocks is not None:
+            clocks["window"] = (f"nvidia-smi every 100 ms over {settle} untimed replays of the "
+                                f"same step and the {k} timed ones right after them")
         dist.barrier()
         ms = dist.max(start.elapsed_time(end))
         return ms, clocks
@@ -367,6 +394,8 @@ def run_layer_set(q, args, dist, peaks):
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": peaks["source"],
+                "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                "nominal_peak": NOMINAL_HBM_GBS,
                 "traffic": recorded_traffic("gemv_grouped_kernel<1,4,1>"),
                 "traffic_source": "profiles/traffic.txt (ncu dram__bytes_read.sum + "
                                   "dram__bytes_write.sum of one launch; null once the kernel's "
@@ -421,10 +450,25 @@ def run_layer_set(q, args, dist, peaks):
         e2e_step(i)
     torch.cuda.synchronize()
     e2e_s = dist.max(time.perf_counter() - t0)
+    # the same calls as a token loop must run them: each step's outputs are
+    # in host memory (the stream synchronized) before the next step is issued
+    sync_steps = max(20, min(args.steps, 200))
+    dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(sync_steps):
+        e2e_step(i)
+        torch.cuda.current_stream().synchronize()
+    sync_s = dist.max(time.perf_counter() - t0)
     e2e = {"value": round(dist.world * step_bytes * e2e_steps / e2e_s / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * k for _, k in LAYER_SET),
            "d2h_bytes_per_step": sum(4 * n for n, _ in LAYER_SET),
-           "steps": e2e_steps, "path": e2e_path}
+           "steps": e2e_steps, "path": e2e_path,
+           "timing": "steps issued back to back, one synchronize at the end (pipelined)",
+           "synchronized": {"value": round(dist.world * step_bytes * sync_steps / sync_s / 1e9, 2),
+                            "unit": "GB/s", "us_per_step": round(sync_s * 1e6 / sync_steps, 2),
+                            "steps": sync_steps,
+                            "timing": "each step's outputs in host memory (stream synchronized) "
+                                      "before the next step is issued, as a token loop runs"}}
     return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e, noise=noise,
                 launches=2 * args.steps, rot=rot, set_bytes=set_bytes,
                 step_bytes=step_bytes, variants=variants)
@@ -472,6 +516,7 @@ def run_prefill_repacked(q, steps, warmup, dist, peaks):
                         "(seed 11; weights repacked at load time)",
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
+            **int8_fraction(tops / dist.world, peaks),
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,1>")}
 
@@ -535,11 +580,16 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
                         "(seed 11; Q8_0 weights)",
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
+            **int8_fraction(tops / dist.world, peaks),
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64,0>")}
 
 
 def run_bitnet(q, steps, warmup, dist, peaks):
+    """The BitNet decode step: per-row activation quantizer + ternary GEMV in
+    one call (qmm_linear_bitnet with programmatic dependent launch), from the
+    f32 activation row to the f32 output.  The GEMV alone on pre-quantized
+    activations is reported beside it."""
     import torch
     from quantized_matmul_gb300 import synthetic
     n, k = 6912, 2560
@@ -547,17 +597,34 @@ def run_bitnet(q, steps, warmup, dist, peaks):
     rot = copies_for(n * k // 4)
     tw = q.pack_ternary(_up(t))
     tws = [tw] + [tw.clone() for _ in range(rot - 1)]
-    aq, s, asum = q.quantize_act_bitnet(_up(x))
+    xd = _up(x)
+    aq = torch.empty((1, k), dtype=torch.int8, device="cuda")
+    s = torch.empty((1,), dtype=torch.float32, device="cuda")
+    asum = torch.empty((1,), dtype=torch.int32, device="cuda")
     y = torch.empty((1, n), dtype=torch.float32, device="cuda")
 
     def step(i):
+        q.linear_bitnet(xd, tws[i % rot], absmean, y=y, pdl=True, aq=aq, act_scale=s, act_sum=asum)
+
+    def gemv(i):
         q.bitnet_gemv(tws[i % rot], absmean, aq, s, asum, y=y)
 
     ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
-    gbs = dist.world * bitnet_bytes(1, n, k) * steps / (ms * 1e-3) / 1e9
-    return {"workload": "BitNet ternary GEMV m=1 K=2560 N=6912 (seed 3)", "value": round(gbs, 1),
-            "unit": "GB/s", "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+    ms_g, _ = GraphTimer(gemv, rot).time(steps, warmup, dist)
+    step_bytes = bitnet_step_bytes(1, n, k)
+    gbs = dist.world * step_bytes * steps / (ms * 1e-3) / 1e9
+    gbs_g = dist.world * bitnet_bytes(1, n, k) * steps / (ms_g * 1e-3) / 1e9
+    return {"workload": "BitNet decode step m=1 K=2560 N=6912 (seed 3): per-row activation "
+                        "quantizer + ternary GEMV in one call (qmm_linear_bitnet, PDL)",
+            "value": round(gbs, 1), "unit": "GB/s",
+            "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
+            "frac_hbm_nominal": round(gbs / dist.world / NOMINAL_HBM_GBS, 4),
+            "us_per_step": round(ms * 1e3 / steps, 3), "algorithmic_bytes_per_step": step_bytes,
+            "gpu_launches_per_step": 2, "weight_copies": rot,
+            "gemv_alone": {"value": round(gbs_g, 1), "unit": "GB/s",
+                           "frac_hbm": round(gbs_g / dist.world / peaks["hbm_gbs"], 4),
+                           "us_per_launch": round(ms_g * 1e3 / steps, 3),
+                           "algorithmic_bytes_per_launch": bitnet_bytes(1, n, k)}}
 
 
 def run_bitnet_prefill(q, steps, warmup, dist, peaks):
@@ -614,13 +681,26 @@ def run_prefill(q, steps, warmup, dist, peaks):
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): the block sums run "
-                         "on tcgen05 kind::f16 because sm_103a has no int8 MMA",
+                         "on tcgen05 kind::f16 because sm_103a has no tcgen05 int8 MMA",
+            **int8_fraction(tops / dist.world, peaks),
             "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,0>"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
                             "(profiles/traffic.txt); algorithmic: 33.0 MB weights + 2.1 MB "
                             "activations + 29.4 MB y (y is written back from L2 after the "
                             "kernel)"}
+
+
+def int8_fraction(tops_per_gpu: float, peaks) -> dict:
+    """The product's rate against the GPU's int8 tensor peak: the measured
+    rate of mma.sync m16n8k32 s8, the only int8 tensor-core instruction
+    sm_103a accepts (qmm_debug_mma_probe, timed in this run)."""
+    p = peaks.get("int8_mma_tops")
+    if not p:
+        return {}
+    return {"frac_int8": round(tops_per_gpu / p, 4), "int8_peak": round(p, 1),
+            "int8_peak_note": "measured in this run: mma.sync m16n8k32 s8 x s8 -> s32 on every "
+                              "SM (tcgen05.mma kind::i8 does not assemble for sm_103a)"}
 
 
 def run_vocab(q, steps, warmup, dist, peaks):
@@ -630,7 +710,7 @@ def run_vocab(q, steps, warmup, dist, peaks):
     wq, wd = wts[0]
     out = {"workload": "Q4_0xQ8_0 vocabulary projection K=4096 N=128256 (seed 13), "
                        "weights 295.5 MB > 2x L2", "m": {}}
-    for m in (1, 16, 128):
+    for m in (1, 8, 16, 32, 128):
         aq, ad = q.quantize_act_q8_0(_up(x[:m]))
         y = torch.empty((m, n), dtype=torch.float32, device="cuda")
         ws = torch.empty((q.workspace_bytes(q.OP_GEMM, m, n, k),), dtype=torch.uint8,
@@ -642,8 +722,9 @@ def run_vocab(q, steps, warmup, dist, peaks):
         for name, fn in paths:
             ms, _ = GraphTimer(fn, 1).time(steps, warmup, dist)
             t = ms * 1e-3 / steps
-            res[name] = {"us": round(t * 1e6, 2),
-                         "GB/s": round(dist.world * gemv_bytes(m, n, k) / t / 1e9, 1),
+            gb = dist.world * gemv_bytes(m, n, k) / t / 1e9
+            res[name] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1),
+                         "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
                          "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2)}
         res["faster"] = min((r for r in res if r in ("gemv", "gemm")), key=lambda r: res[r]["us"])
         out["m"][str(m)] = res
@@ -675,19 +756,82 @@ def _oracle_step(mats):
     return moved
 
 
+def host_cores() -> list[int]:
+    try:
+        return sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        return list(range(os.cpu_count() or 1))
+
+
+def _oracle_step_threads(mats, threads: int, ex=None):
+    """One layer-set step of the oracle with each matrix's rows split over
+    `threads` threads of the executor `ex` (the oracle's C calls release the
+    GIL): rows are independent, so the outputs are bit for bit those of one
+    thread."""
+    import oracle
+    if threads <= 1 or ex is None:
+        return _oracle_step(mats)
+    moved = 0
+    for n, k, rows, wq, wd, x in mats:
+        aq, ad = oracle.quantize_q8_0(x)
+        cuts = [rows * t // threads for t in range(threads + 1)]
+        parts = [ex.submit(oracle.gemm_q4_0_q8_0, wq[a:b], wd[a:b], aq, ad)
+                 for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+        for f in parts:
+            f.result()
+        moved += linear_bytes(1, rows, k)
+    return moved
+
+
+def _oracle_rate(mats, threads: int, budget_s: float, pin_core: int | None = None):
+    """GB/s of repeated oracle steps for about budget_s seconds."""
+    from concurrent.futures import ThreadPoolExecutor
+    old = None
+    if pin_core is not None:
+        try:
+            old = os.sched_getaffinity(0)
+            os.sched_setaffinity(0, {pin_core})
+        except (AttributeError, OSError):
+            old = None
+    ex = ThreadPoolExecutor(threads) if threads > 1 else None
+    try:
+        _oracle_step_threads(mats, threads, ex)  # threads started, caches warm
+        steps, moved, t0 = 0, 0, time.perf_counter()
+        while True:
+            moved += _oracle_step_threads(mats, threads, ex)
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    finally:
+        if ex is not None:
+            ex.shutdown()
+        if old is not None:
+            os.sched_setaffinity(0, old)
+    return moved / el / 1e9, steps, el
+
+
 def cpu_baseline(budget_s: float, frac: float = 0.25):
+    """The oracle as it stands on the host cores: one core (pinned) and all
+    host cores (rows split over threads), each the median of three runs of
+    about budget_s / 6 seconds over the same row sample."""
     mats = _oracle_layer_set(frac)
-    steps, moved, t0 = 0, 0, time.perf_counter()
-    while True:
-        moved += _oracle_step(mats)
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return {"value": round(moved / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} layer-set steps, each the Q8_0 quantization of all 7 activation "
-                      f"rows plus the scalar GEMV over the first {frac:.0%} of rows of every "
-                      f"matrix ({el:.1f} s, one thread)"}
+    cores = host_cores()
+    each = max(budget_s / 6.0, 0.5)
+    one = [_oracle_rate(mats, 1, each, pin_core=cores[0]) for _ in range(3)]
+    allc = [_oracle_rate(mats, len(cores), each) for _ in range(3)]
+    med1 = statistics.median(r[0] for r in one)
+    medn = statistics.median(r[0] for r in allc)
+    sample = (f"layer-set steps, each the Q8_0 quantization of all 7 activation rows plus the "
+              f"scalar GEMV over the first {frac:.0%} of rows of every matrix; median of 3 runs "
+              f"of ~{each:.1f} s each")
+    return {"value": round(medn, 4), "unit": "GB/s", "cores": len(cores), "kind": "oracle",
+            "host_cores": len(cores),
+            "sample": sample + f", rows split over {len(cores)} threads",
+            "runs": [round(r[0], 4) for r in allc],
+            "one_core": {"value": round(med1, 4), "unit": "GB/s", "cores": 1,
+                         "runs": [round(r[0], 4) for r in one],
+                         "sample": sample + ", one thread pinned to one core"}}
 
 
 def run_reference(args, dist):
@@ -695,29 +839,36 @@ def run_reference(args, dist):
         return
     # a 1% row sample calibrates the cost of a full step; each timed step then
     # takes a row sample sized so warm-up + steps finish within the budget
+    from concurrent.futures import ThreadPoolExecutor
+    cores = len(host_cores())
+    ex = ThreadPoolExecutor(cores) if cores > 1 else None
     probe_frac = 0.01
     probe = _oracle_layer_set(probe_frac)
+    _oracle_step_threads(probe, cores, ex)
     t0 = time.perf_counter()
-    _oracle_step(probe)
+    _oracle_step_threads(probe, cores, ex)
     full_s = (time.perf_counter() - t0) / probe_frac
     del probe
     frac = min(1.0, args.ref_budget / max(1, args.steps + args.warmup) / max(full_s, 1e-6))
     frac = max(frac, 1e-4)
     mats = _oracle_layer_set(frac)
     for _ in range(args.warmup):
-        _oracle_step(mats)
+        _oracle_step_threads(mats, cores, ex)
     t0 = time.perf_counter()
-    moved = sum(_oracle_step(mats) for _ in range(args.steps))
+    moved = sum(_oracle_step_threads(mats, cores, ex) for _ in range(args.steps))
     el = time.perf_counter() - t0
+    if ex is not None:
+        ex.shutdown()
     value = moved / el / 1e9
     sample = (f"each step: Q8_0 quantization of all 7 activation rows + scalar GEMV over the "
-              f"first {frac:.4%} of rows of every matrix of the layer set, one thread")
+              f"first {frac:.4%} of rows of every matrix of the layer set, rows split over "
+              f"{cores} threads (all host cores)")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el * 1e3 / max(1, args.steps), 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": WORKLOAD_C2, "m": 1, "row_fraction": frac},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -756,6 +907,10 @@ def main():
         import quantized_matmul_gb300 as q
         q.load()  # the CUDA library; raises if it is missing
         peaks = load_peaks()
+        # the int8 tensor peak the prefill products are reported against
+        # (and the warp-level f16 rate beside it), measured now on this GPU
+        peaks["int8_mma_tops"] = q.mma_probe_tops(0)
+        peaks["f16_mma_sync_tflops"] = q.mma_probe_tops(1)
         if args.only:
             run = {"gemv": lambda: run_single_gemv(q, args.steps, args.warmup, dist, peaks),
                    "bitnet": lambda: run_bitnet(q, args.steps, args.warmup, dist, peaks),
@@ -810,6 +965,14 @@ def main():
                 "gpu_launches": main_res["launches"],
                 "noise": main_res["noise"],
                 "frac_hbm_step": round(main_res["value"] / dist.world / peaks["hbm_gbs"], 4),
+                "frac_hbm_step_nominal": round(main_res["value"] / dist.world / NOMINAL_HBM_GBS, 4),
+                "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                          "source": peaks["source"], "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+                          "int8_mma_sync_tops": round(peaks["int8_mma_tops"], 1),
+                          "f16_mma_sync_tflops": round(peaks["f16_mma_sync_tflops"], 1),
+                          "mma_sync_note": "measured in this run with qmm_debug_mma_probe (warp-"
+                                           "level MMA on every SM); int8 is the GPU's only int8 "
+                                           "tensor path on sm_103a"},
                 "configs": configs,
             }
             print(json.dumps(line), flush=True)

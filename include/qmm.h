@@ -342,6 +342,24 @@ qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean,
                            const int8_t *aq, const float *act_scale, const int32_t *act_sum,
                            float *y, int64_t m, int64_t n, int64_t k, void *stream);
 
+/* BitNet decode linear layer (Loom, "BitNet ternary MAD kernel"): the
+ * activation quantization of qmm_quantize_act_bitnet on x, then
+ * qmm_bitnet_gemv, enqueued as one call; aq, act_scale, act_sum and y are bit
+ * for bit those of the two calls.  1 <= m <= QMM_GEMV_MAX_M.
+ *   x f32 [m, ldx] (first k columns, ldx >= k), 4-byte aligned; aq int8
+ *   [m, k] 16-byte aligned; act_scale f32 [m], act_sum int32 [m] 4-byte
+ *   aligned; w, y and the limits on k as for qmm_bitnet_gemv.  Inputs must
+ *   be finite.
+ *   flags: 0, or QMM_LINEAR_PDL: both kernels launch with programmatic
+ *   dependent launch, with the same rules as qmm_linear_q4_0 (the GEMV loads
+ *   its first weight words before the quantizer has finished, so w must not
+ *   be written by work still running on the stream; a chain of such calls
+ *   on one stream stays ordered).
+ * Errors as for the two calls; QMM_ERR_ARG for unknown flags. */
+qmm_status qmm_linear_bitnet(const uint32_t *w, float weight_absmean, const float *x, int64_t ldx,
+                             int8_t *aq, float *act_scale, int32_t *act_sum, float *y,
+                             int64_t m, int64_t n, int64_t k, int flags, void *stream);
+
 /* BitNet ternary matrix product for prefill (any m >= 1), on the tensor
  * cores.  Same result as qmm_bitnet_gemv, bit for bit:
  *   dot[i, r] = sum_j (code[r, j] - 1) * aq[i, j]    (exact; equal to the
@@ -384,6 +402,22 @@ int qmm_version(void);
 /* Test entry points.  They run the same kernels as the product entry points
  * compiled to also emit their intermediate integers, so tests can compare
  * them bit for bit with a reference.  Not for production use. */
+
+/* Test and measurement entry: runs a tensor-pipe throughput loop on every SM
+ * (one CTA of 512 threads per SM, each warp issuing independent warp-level
+ * MMAs back to back) so the caller can time it and obtain the peak rate of
+ * that instruction.  kind 0: mma.sync m16n8k32 s8 x s8 -> s32, the only int8
+ * tensor-core instruction sm_103a accepts (the assembler rejects
+ * tcgen05.mma kind::i8 for this target); kind 1: mma.sync m16n8k16 f16 x f16
+ * -> f32.  *macs receives the multiply-accumulates of the launch.  The pages
+ * have no counterpart; it only supplies the int8 peak that products are
+ * reported against.
+ *   out int32 device buffer of at least (SM count) * 512 * 4 bytes (written
+ *   with values of no meaning); iters > 0.
+ *   QMM_ERR_ARG for another kind or iters <= 0; QMM_ERR_WORKSPACE when out is
+ *   too small. */
+qmm_status qmm_debug_mma_probe(int kind, int iters, int *out, size_t out_bytes, int64_t *macs,
+                               void *stream);
 
 /* Per-block sums sumi int32 [m, n, k/32] = sum_j (nibble_j - 8) * q_j.
  * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the tensor-

@@ -75,6 +75,7 @@ def load() -> ctypes.CDLL:
             "qmm_pack_ternary": (I, [P, I64, I64, P, P]),
             "qmm_bitnet_gemv": (I, [P, F, P, P, P, P, I64, I64, I64, P]),
             "qmm_bitnet_gemm": (I, [P, F, P, P, P, I64, I64, I64, P, SZ, P]),
+            "qmm_linear_bitnet": (I, [P, F, P, I64, P, P, P, P, I64, I64, I64, I, P]),
             "qmm_workspace_bytes": (SZ, [I, I64, I64, I64, I]),
             "qmm_gemv_auto_split": (I, [I64, I64, I64]),
             "qmm_check_device_error": (I, [P]),
@@ -83,6 +84,7 @@ def load() -> ctypes.CDLL:
             "qmm_debug_block_sums_q4_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_debug_block_sums_q8_0_q8_0": (I, [I, P, P, P, I64, I64, I64, P, SZ, P]),
             "qmm_debug_bitnet_dot": (I, [P, P, P, P, I64, I64, I64, P]),
+            "qmm_debug_mma_probe": (I, [I, I, P, SZ, P, P]),
             "qmm_debug_set_wait_limit": (None, [U32]),
             "qmm_debug_withhold_gemm_loads": (None, [I]),
             "qmm_debug_withhold_gemv_loads": (None, [I]),
@@ -499,6 +501,56 @@ def pack_ternary(t):
     st = load().qmm_pack_ternary(_dev(t, torch.int8, "t"), n, k, w.data_ptr(), _stream())
     _check(st, "qmm_pack_ternary")
     return w
+
+
+def linear_bitnet(x, tw, weight_absmean: float, y=None, pdl: bool = False, aq=None,
+                  act_scale=None, act_sum=None, codes: bool = False):
+    """BitNet decode layer in one library call (qmm_linear_bitnet): the
+    per-row activation quantizer then the ternary GEMV, m <= 16.  pdl=True
+    launches both with programmatic dependent launch (see linear_q4_0).
+    codes=True also returns (aq, act_scale, act_sum)."""
+    torch = _torch()
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    m, k = x.shape
+    n = tw.shape[0]
+    _dev(tw, torch.int32, "tw", (n, k // 16))
+    aq = _empty((m, k), torch.int8, x) if aq is None else aq
+    act_scale = _empty((m,), torch.float32, x) if act_scale is None else act_scale
+    act_sum = _empty((m,), torch.int32, x) if act_sum is None else act_sum
+    y = _empty((m, n), torch.float32, x) if y is None else y
+    st = load().qmm_linear_bitnet(tw.data_ptr(), float(weight_absmean), _dev(x, torch.float32, "x"), k,
+                                  _dev(aq, torch.int8, "aq", (m, k)),
+                                  _dev(act_scale, torch.float32, "act_scale", (m,)),
+                                  _dev(act_sum, torch.int32, "act_sum", (m,)),
+                                  _dev(y, torch.float32, "y", (m, n)), m, n, k,
+                                  LINEAR_PDL if pdl else 0, _stream())
+    _check(st, "qmm_linear_bitnet")
+    return (y, aq, act_scale, act_sum) if codes else y
+
+
+def mma_probe_tops(kind: int = 0, iters: int = 4096, repeats: int = 3) -> float:
+    """Measured warp-level tensor-core rate, in tera multiply-accumulates x 2
+    per second (TOPS for kind 0, int8; TFLOPS for kind 1, f16): the best of
+    `repeats` timed launches of qmm_debug_mma_probe after one untimed one."""
+    torch = _torch()
+    dev = torch.cuda.current_device()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty((sms * 512,), dtype=torch.int32, device="cuda")
+    macs = ctypes.c_int64(0)
+    best = 0.0
+    for r in range(repeats + 1):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        st = load().qmm_debug_mma_probe(kind, iters, out.data_ptr(), out.numel() * 4,
+                                        ctypes.byref(macs), _stream())
+        end.record()
+        _check(st, "qmm_debug_mma_probe")
+        end.synchronize()
+        if r:
+            best = max(best, 2.0 * macs.value / (start.elapsed_time(end) * 1e-3) / 1e12)
+    return best
 
 
 def bitnet_gemv(tw, weight_absmean: float, aq, act_scale, act_sum, y=None):

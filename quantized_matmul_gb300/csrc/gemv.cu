@@ -266,7 +266,10 @@ __device__ __forceinline__ int ternary_dot16(uint32_t word, const int act_t[4], 
     return acc;
 }
 
-template <int MT, int ROWS, bool VEC, bool EMIT>
+// PDL: the warp loads its first weight words (model parameters, never
+// written by the preceding kernels), then waits for the predecessor (the
+// activation quantizer) before it reads aq, scale and asum or writes y.
+template <int MT, int ROWS, bool VEC, bool EMIT, bool PDL>
 __global__ void __launch_bounds__(kWarps * 32)
 bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *__restrict__ aq,
                    const float *__restrict__ scale, const int32_t *__restrict__ asum,
@@ -286,8 +289,8 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
     if (VEC) {
         // 4 words (64 weights) per lane per step, 128-bit loads
         const int64_t kv = kw / 4;
-        for (int64_t jj = lane; jj < kv; jj += 32 * kUnroll) {
-            uint4 wv[kUnroll][ROWS];
+        uint4 wv[kUnroll][ROWS];
+        auto load_batch = [&](int64_t jj) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t j = jj + 32 * u;
@@ -297,6 +300,14 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
                                    ? ld_stream_v4(w + (row0 + r) * kw + j * 4)
                                    : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
             }
+        };
+        if (PDL) {
+            load_batch(lane);
+            pdl_wait();
+            pdl_launch_dependents();
+        }
+        for (int64_t jj = lane; jj < kv; jj += 32 * kUnroll) {
+            if (!PDL || jj != lane) load_batch(jj);
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t j = jj + 32 * u;
@@ -323,6 +334,10 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
             }
         }
     } else {
+        if (PDL) {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
         // one word (16 weights) per lane per step
         for (int64_t j = lane; j < kw; j += 32) {
             uint32_t wv[ROWS];
@@ -371,19 +386,32 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
 template <int MT, int ROWS>
 cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, const float *scale,
                           const int32_t *asum, float *y, int32_t *dot, int64_t m, int64_t n,
-                          int64_t k, cudaStream_t s) {
+                          int64_t k, cudaStream_t s, bool pdl) {
     const int64_t rows_per_cta = (int64_t)kWarps * ROWS;
-    const unsigned grid = (unsigned)((n + rows_per_cta - 1) / rows_per_cta);
+    const dim3 grid((unsigned)((n + rows_per_cta - 1) / rows_per_cta));
     const bool vec = (k % 64) == 0;
-#define QMM_BITNET_LAUNCH(V, E)                                                           \
-    bitnet_gemv_kernel<MT, ROWS, V, E><<<grid, kWarps * 32, 0, s>>>(w, absmean, aq, scale, \
-                                                                    asum, y, dot, (int)m, n, k)
-    if (vec) {
-        if (dot) QMM_BITNET_LAUNCH(true, true); else QMM_BITNET_LAUNCH(true, false);
-    } else {
-        if (dot) QMM_BITNET_LAUNCH(false, true); else QMM_BITNET_LAUNCH(false, false);
+    if (dot) {
+        if (vec)
+            bitnet_gemv_kernel<MT, ROWS, true, true, false><<<grid, kWarps * 32, 0, s>>>(
+                w, absmean, aq, scale, asum, y, dot, (int)m, n, k);
+        else
+            bitnet_gemv_kernel<MT, ROWS, false, true, false><<<grid, kWarps * 32, 0, s>>>(
+                w, absmean, aq, scale, asum, y, dot, (int)m, n, k);
+        return cudaPeekAtLastError();
     }
-#undef QMM_BITNET_LAUNCH
+    if (pdl)
+        return vec ? launch_kernel(bitnet_gemv_kernel<MT, ROWS, true, false, true>, grid,
+                                   dim3(kWarps * 32), 0, s, true, w, absmean, aq, scale, asum, y,
+                                   dot, (int)m, n, k)
+                   : launch_kernel(bitnet_gemv_kernel<MT, ROWS, false, false, true>, grid,
+                                   dim3(kWarps * 32), 0, s, true, w, absmean, aq, scale, asum, y,
+                                   dot, (int)m, n, k);
+    if (vec)
+        bitnet_gemv_kernel<MT, ROWS, true, false, false><<<grid, kWarps * 32, 0, s>>>(
+            w, absmean, aq, scale, asum, y, dot, (int)m, n, k);
+    else
+        bitnet_gemv_kernel<MT, ROWS, false, false, false><<<grid, kWarps * 32, 0, s>>>(
+            w, absmean, aq, scale, asum, y, dot, (int)m, n, k);
     return cudaPeekAtLastError();
 }
 
@@ -470,13 +498,13 @@ cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count,
 
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
-                               int64_t m, int64_t n, int64_t k, cudaStream_t s) {
+                               int64_t m, int64_t n, int64_t k, cudaStream_t s, bool pdl) {
     // m = 1: four rows per warp (3.53 against 3.60 us for two at N=6912, K=2560)
-    if (m == 1) return launch_bitnet<1, 4>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
-    if (m == 2) return launch_bitnet<2, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
-    if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
-    if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
-    return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s);
+    if (m == 1) return launch_bitnet<1, 4>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
+    if (m == 2) return launch_bitnet<2, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
+    if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
+    if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
+    return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
 }
 
 cudaError_t launch_linear_grouped(const LinearGroup &tab, bool pdl, cudaStream_t s) {

@@ -346,7 +346,7 @@ qmm_status qmm_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t 
     if (!aligned(x, 4) || !aligned(act_scale, 4) || !aligned(act_sum, 4)) return QMM_ERR_ALIGN;
     if (qmm_status st = check_device()) return st;
     return launch_status(
-        qmm::launch_quantize_act_bitnet(x, m, k, aq, act_scale, act_sum, as_stream(stream)));
+        qmm::launch_quantize_act_bitnet(x, m, k, k, aq, act_scale, act_sum, as_stream(stream)));
 }
 
 qmm_status qmm_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t *w, void *stream) {
@@ -377,6 +377,23 @@ qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean, const int8_t
     if (qmm_status st = check_device()) return st;
     return launch_status(qmm::launch_bitnet_gemv(w, weight_absmean, aq, act_scale, act_sum, y,
                                                  nullptr, m, n, k, as_stream(stream)));
+}
+
+qmm_status qmm_linear_bitnet(const uint32_t *w, float weight_absmean, const float *x, int64_t ldx,
+                             int8_t *aq, float *act_scale, int32_t *act_sum, float *y, int64_t m,
+                             int64_t n, int64_t k, int flags, void *stream) {
+    if (!x) return QMM_ERR_NULL;
+    if (qmm_status st = check_bitnet(w, aq, act_scale, act_sum, y, m, n, k)) return st;
+    if (ldx < k || m * ldx > kMaxElems) return QMM_ERR_SHAPE;
+    if (!aligned(x, 4)) return QMM_ERR_ALIGN;
+    if (flags & ~QMM_LINEAR_PDL) return QMM_ERR_ARG;
+    if (qmm_status st = check_device()) return st;
+    const bool pdl = (flags & QMM_LINEAR_PDL) != 0;
+    const cudaStream_t s = as_stream(stream);
+    cudaError_t e = qmm::launch_quantize_act_bitnet(x, m, k, ldx, aq, act_scale, act_sum, s, pdl);
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    return launch_status(qmm::launch_bitnet_gemv(w, weight_absmean, aq, act_scale, act_sum, y, nullptr,
+                                                 m, n, k, s, pdl));
 }
 
 qmm_status qmm_bitnet_gemm(const uint32_t *w, float weight_absmean, const int8_t *aq,
@@ -526,6 +543,21 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
     if (qmm_status st = check_device()) return st;
     return launch_status(qmm::launch_bitnet_gemv(w, 0.0f, aq, nullptr, act_sum, nullptr, dot, m, n,
                                                  k, as_stream(stream)));
+}
+
+qmm_status qmm_debug_mma_probe(int kind, int iters, int *out, size_t out_bytes, int64_t *macs,
+                               void *stream) {
+    if (!out || !macs) return QMM_ERR_NULL;
+    if ((kind != 0 && kind != 1) || iters <= 0) return QMM_ERR_ARG;
+    if (!aligned(out, 4)) return QMM_ERR_ALIGN;
+    if (qmm_status st = check_device()) return st;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    if (out_bytes < (size_t)sms * 512 * sizeof(int)) return QMM_ERR_WORKSPACE;
+    *macs = qmm::mma_probe_macs_per_iter(kind, sms) * iters;
+    return launch_status(qmm::launch_mma_probe(kind, iters, sms, out, as_stream(stream)));
 }
 
 void qmm_debug_set_wait_limit(uint32_t iterations) {

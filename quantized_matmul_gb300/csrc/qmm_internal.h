@@ -68,8 +68,10 @@ cudaError_t launch_quantize_act_q8_0(const float *x, int64_t m, int64_t k, int64
                                      int8_t *aq, uint16_t *ad, cudaStream_t s, bool pdl = false);
 cudaError_t launch_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
                                         uint8_t *wq, uint16_t *wd, cudaStream_t s);
-cudaError_t launch_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t *aq,
-                                       float *scale, int32_t *sum, cudaStream_t s);
+// x rows ldx floats apart; pdl: launch with programmatic dependent launch
+// (x is read after pdl_wait)
+cudaError_t launch_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int64_t ldx, int8_t *aq,
+                                       float *scale, int32_t *sum, cudaStream_t s, bool pdl = false);
 cudaError_t launch_pack_ternary(const int8_t *t, int64_t n, int64_t k, uint32_t *w,
                                 cudaStream_t s);
 
@@ -90,9 +92,12 @@ constexpr int64_t kGemvNoAllocScratchFloats = int64_t(1) << 20;
 cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                           const uint16_t *ad, float *y, int64_t m, int64_t n,
                                           int64_t k, int split, cudaStream_t s);
+// pdl: launch with programmatic dependent launch; the GEMV then loads its
+// first weight words before pdl_wait and reads aq/scale/sum after it (dot
+// must be null).
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
-                               int64_t m, int64_t n, int64_t k, cudaStream_t s);
+                               int64_t m, int64_t n, int64_t k, cudaStream_t s, bool pdl = false);
 // y[i] = sum over slices s of partials[s * count + i], slices in order.
 cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count, int split,
                                  cudaStream_t s);
@@ -138,6 +143,11 @@ cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int
 void gemm_small_set_wait_limit(uint32_t iterations);
 void gemm_small_set_withhold_loads(int enable);
 cudaError_t gemm_small_read_and_clear_error(unsigned int *word, cudaStream_t s);
+// probe.cu: tensor-pipe peak probes (kind 0: int8 mma.sync m16n8k32; 1: f16
+// mma.sync m16n8k16), one CTA of 512 threads per SM; `out` holds sms * 512
+// ints.
+int64_t mma_probe_macs_per_iter(int kind, int sms);
+cudaError_t launch_mma_probe(int kind, int iters, int sms, int *out, cudaStream_t s);
 // gemm.cu
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 // sumi != nullptr selects the block-sum emitting variant.

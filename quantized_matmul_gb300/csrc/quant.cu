@@ -118,14 +118,22 @@ quantize_weight_q4_0_kernel(const float *__restrict__ w, int64_t n, int64_t k,
 // CTA reductions (max and integer addition do not depend on order).
 constexpr int kBitnetThreads = 256;
 
+// BitNet per-row quantization, one CTA per row.  With PDL the next kernel
+// (the ternary GEMV) may launch at once and stream its weights while this
+// grid waits for x from its own predecessor.
+template <bool PDL>
 __global__ void __launch_bounds__(kBitnetThreads)
-quantize_act_bitnet_kernel(const float *__restrict__ x, int64_t k, int8_t *__restrict__ aq,
+quantize_act_bitnet_kernel(const float *__restrict__ x, int64_t k, int64_t ldx, int8_t *__restrict__ aq,
                            float *__restrict__ scale, int32_t *__restrict__ sum) {
     __shared__ float s_max[kBitnetThreads / 32];
     __shared__ int s_sum[kBitnetThreads / 32];
     __shared__ float s_scale;
+    if (PDL) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
     const int64_t i = blockIdx.x;
-    const float *xr = x + i * k;
+    const float *xr = x + i * ldx;
     float amax = 0.0f;
     for (int64_t j = threadIdx.x; j < k; j += kBitnetThreads) amax = fmaxf(amax, fabsf(xr[j]));
     amax = warp_max(amax);
@@ -209,9 +217,12 @@ cudaError_t launch_quantize_weight_q4_0(const float *w, int64_t n, int64_t k, ui
     return cudaPeekAtLastError();
 }
 
-cudaError_t launch_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int8_t *aq,
-                                       float *scale, int32_t *sum, cudaStream_t s) {
-    quantize_act_bitnet_kernel<<<(unsigned)m, kBitnetThreads, 0, s>>>(x, k, aq, scale, sum);
+cudaError_t launch_quantize_act_bitnet(const float *x, int64_t m, int64_t k, int64_t ldx, int8_t *aq,
+                                       float *scale, int32_t *sum, cudaStream_t s, bool pdl) {
+    if (pdl)
+        return launch_kernel(quantize_act_bitnet_kernel<true>, dim3((unsigned)m), dim3(kBitnetThreads),
+                             0, s, true, x, k, ldx, aq, scale, sum);
+    quantize_act_bitnet_kernel<false><<<(unsigned)m, kBitnetThreads, 0, s>>>(x, k, ldx, aq, scale, sum);
     return cudaPeekAtLastError();
 }
 

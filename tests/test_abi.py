@@ -133,6 +133,23 @@ def test_repack_entry_points(lib):
     assert gemm(A2, 1 << 20, A16, A16, A16, A16, 1, 1, 32, A16, 1 << 20, None) == QMM_ERR_ALIGN
 
 
+def test_linear_bitnet_argument_errors(lib):
+    A16 = _p(0x10000)  # never dereferenced: every call below fails its host checks
+    A2 = _p(0x10002)
+    f = lib.qmm_linear_bitnet
+    f.restype = ctypes.c_int
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    f.argtypes = [P, ctypes.c_float, P, I64, P, P, P, P, I64, I64, I64, I, P]
+    assert f(A16, 1.0, None, 32, A16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_NULL
+    assert f(None, 1.0, A16, 32, A16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_NULL
+    assert f(A16, 1.0, A16, 32, A16, A16, A16, A16, 17, 1, 32, 0, None) == QMM_ERR_SHAPE
+    assert f(A16, 1.0, A16, 32, A16, A16, A16, A16, 1, 1, 24, 0, None) == QMM_ERR_SHAPE
+    assert f(A16, 1.0, A16, 16, A16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_SHAPE  # ldx < k
+    assert f(A2, 1.0, A16, 32, A16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_ALIGN
+    assert f(A16, 1.0, A2, 32, A16, A16, A16, A16, 1, 1, 32, 0, None) == QMM_ERR_ALIGN
+    assert f(A16, 1.0, A16, 32, A16, A16, A16, A16, 1, 1, 32, 4, None) == QMM_ERR_ARG
+
+
 def test_auto_split_policy(lib):
     # a narrow output with a long reduction is split, a wide one is not
     assert lib.qmm_gemv_auto_split(1, 256, 16384) > 1

@@ -260,6 +260,73 @@ def test_bitnet_path_bit_exact(qmm, orc, m, n, k):
     assert np.array_equal(to_np(y).view(np.uint32), y_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 6912, 2560), (1, 33, 48), (3, 65, 160), (16, 31, 1024),
+                                   (2, 129, 2576)])
+@pytest.mark.parametrize("pdl", [False, True])
+def test_linear_bitnet_bit_exact(qmm, orc, m, n, k, pdl):
+    """The decode step in one call: codes, scale, sum and y bit for bit the
+    oracle's, with and without programmatic dependent launch, on rows read
+    with a row stride larger than k."""
+    import torch
+    t, x, absmean = synthetic.bitnet_case(170 + m + n, n, k, m)
+    x = x.copy()
+    if m > 1:
+        x[1] = 0.0  # zero row: scale 0, y 0
+    tw_ref = orc.pack_ternary(t)
+    aq_ref, s_ref, asum_ref = orc.quantize_act_bitnet(x)
+    tw = to_dev(tw_ref.view(np.int32))
+    xbuf = torch.full((m, k + 48), 3.0e3, dtype=torch.float32, device="cuda")
+    xbuf[:, :k] = to_dev(x)
+    aq = torch.empty((m, k), dtype=torch.int8, device="cuda")
+    sc = torch.empty((m,), dtype=torch.float32, device="cuda")
+    asum = torch.empty((m,), dtype=torch.int32, device="cuda")
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    st = qmm.load().qmm_linear_bitnet(tw.data_ptr(), float(absmean), xbuf.data_ptr(), k + 48,
+                                      aq.data_ptr(), sc.data_ptr(), asum.data_ptr(), y.data_ptr(),
+                                      m, n, k, 1 if pdl else 0,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(to_np(sc).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(to_np(asum), asum_ref)
+    y_ref = orc.bitnet_gemv(tw_ref, absmean, aq_ref, s_ref, asum_ref)
+    assert np.array_equal(to_np(y).view(np.uint32), y_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("m", [1, 4])
+def test_linear_bitnet_pdl_chain_reads_the_previous_layer_output(qmm, orc, m):
+    """BitNet layers chained on one stream, each consuming the previous
+    layer's y and sharing one code buffer: with programmatic dependent
+    launch every kernel still reads its inputs after its predecessor, so the
+    chain gives the same bits as without, and each layer's output is the
+    oracle's on that layer's actual input."""
+    import torch
+    dims = [2560, 6912, 2560, 2560]
+    layers = []
+    for j in range(len(dims) - 1):
+        t, _, absmean = synthetic.bitnet_case(6400 + j, dims[j + 1], dims[j], 1)
+        tw_ref = orc.pack_ternary(t)
+        layers.append((tw_ref, absmean, to_dev(tw_ref.view(np.int32))))
+    _, x0, _ = synthetic.bitnet_case(6499, 1, dims[0], m)
+    aq_flat = torch.empty(m * max(dims), dtype=torch.int8, device="cuda")
+    outs = {}
+    for pdl in (False, True):
+        hs = [to_dev(x0)]
+        for j, (_, absmean, tw_d) in enumerate(layers):
+            aq_j = aq_flat[: m * dims[j]].view(m, dims[j])
+            hs.append(qmm.linear_bitnet(hs[-1], tw_d, absmean, pdl=pdl, aq=aq_j))
+        torch.cuda.synchronize()
+        outs[pdl] = [to_np(h) for h in hs]
+    for a, b in zip(outs[False], outs[True]):
+        assert np.isfinite(a).all()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    for j, (tw_ref, absmean, _) in enumerate(layers):
+        aq_r, s_r, asum_r = orc.quantize_act_bitnet(outs[True][j])
+        y_ref = orc.bitnet_gemv(tw_ref, absmean, aq_r, s_r, asum_r)
+        assert np.array_equal(outs[True][j + 1].view(np.uint32), y_ref.view(np.uint32)), j
+
+
 # ---------------------------------------------------------------------------
 # BitNet prefill on the tensor cores
 
