@@ -345,7 +345,10 @@ qmm_status qmm_bitnet_gemv(const uint32_t *w, float weight_absmean,
 /* BitNet decode linear layer (Loom, "BitNet ternary MAD kernel"): the
  * activation quantization of qmm_quantize_act_bitnet on x, then
  * qmm_bitnet_gemv, enqueued as one call; aq, act_scale, act_sum and y are bit
- * for bit those of the two calls.  1 <= m <= QMM_GEMV_MAX_M.
+ * for bit those of the two calls.  1 <= m <= QMM_GEMV_MAX_M.  For m = 1 with
+ * k % 64 == 0, k <= 32768 and x, aq 16-byte aligned this is one kernel in
+ * which every CTA quantizes the row itself (the same operations) and CTA 0
+ * writes aq, act_scale and act_sum; otherwise two kernels.
  *   x f32 [m, ldx] (first k columns, ldx >= k), 4-byte aligned; aq int8
  *   [m, k] 16-byte aligned; act_scale f32 [m], act_sum int32 [m] 4-byte
  *   aligned; w, y and the limits on k as for qmm_bitnet_gemv.  Inputs must

@@ -383,6 +383,149 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
     }
 }
 
+// The BitNet decode step for one token (m = 1, k % 64 == 0) in one kernel.
+// Every CTA quantizes the activation row itself: the per-row scale needs
+// the whole row's maximum, and the row (k floats, read from L2) is small
+// next to the CTA's weights, so this costs each CTA well under a
+// microsecond and takes the separate quantizer launch, and its latency, out
+// of the step.  The operations are the quantizer's (max of |x|, s =
+// 127 / max, q = clamp(round(x * s), -127, 127), sum q), so codes, scale, sum
+// and y are bit for bit those of the two-kernel step; CTA 0 also writes them
+// out.  The codes go to shared memory already transposed for the ternary
+// dot: for 16-element group j, int t_s = bytes of elements 16j + s, s+4, s+8,
+// s+12, stored at [s][j] so that a warp's 16-byte reads are contiguous.
+// PDL: the weight words are loaded before the wait, x after it.
+template <int ROWS, int WARPS, bool PDL>
+__global__ void __launch_bounds__(WARPS * 32)
+bitnet_linear_m1_kernel(const uint32_t *__restrict__ w, float absmean, const float *__restrict__ x,
+                        int8_t *__restrict__ aq, float *__restrict__ scale_out,
+                        int32_t *__restrict__ sum_out, float *__restrict__ y, int64_t n, int64_t k) {
+    extern __shared__ int4 s_act[];  // [4 byte planes][k / 64 vectors], 16 bytes each
+    __shared__ float s_max[WARPS];
+    __shared__ int s_sum[WARPS];
+    constexpr int kThreads = WARPS * 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t row0 = ((int64_t)blockIdx.x * WARPS + warp) * ROWS;
+    const int64_t kw = k / 16, kv = k / 64;
+
+    uint4 wv[kUnroll][ROWS];
+    auto load_batch = [&](int64_t jj) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t j = jj + 32 * u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                wv[u][r] = (j < kv && row0 + r < n)
+                               ? ld_stream_v4(w + (row0 + r) * kw + j * 4)
+                               : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+        }
+    };
+    load_batch(lane);
+    if (PDL) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    // the row's maximum magnitude
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    float amax = 0.0f;
+    for (int64_t i = threadIdx.x; i < k / 4; i += kThreads) {
+        const float4 v = __ldg(x4 + i);
+        amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_max[warp] = amax;
+    __syncthreads();
+    float mx = s_max[0];
+#pragma unroll
+    for (int i = 1; i < WARPS; ++i) mx = fmaxf(mx, s_max[i]);
+    const float sc = (mx != 0.0f) ? __fdiv_rn(127.0f, mx) : 0.0f;
+    // codes of 16-element groups: natural order to aq (CTA 0), transposed to
+    // shared memory
+    int part = 0;
+    for (int64_t gi = threadIdx.x; gi < kw; gi += kThreads) {
+        uint32_t q4[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const float4 v = __ldg(x4 + gi * 4 + h);
+            const float f[4] = {v.x, v.y, v.z, v.w};
+            uint32_t packed = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float q = 0.0f;
+                if (sc != 0.0f) q = fminf(fmaxf(roundf(__fmul_rn(f[e], sc)), -127.0f), 127.0f);
+                const int qi = (int)q;
+                part += qi;
+                packed |= (uint32_t)(qi & 0xff) << (8 * e);
+            }
+            q4[h] = packed;
+        }
+        if (blockIdx.x == 0)
+            reinterpret_cast<int4 *>(aq)[gi] = make_int4((int)q4[0], (int)q4[1], (int)q4[2], (int)q4[3]);
+        int t[4];
+        transpose4x4((int)q4[0], (int)q4[1], (int)q4[2], (int)q4[3], t);
+        // group gi is word (gi % 4) of vector gi / 4; plane s holds t_s
+        int *plane = reinterpret_cast<int *>(s_act);
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) plane[(sp * kv + gi / 4) * 4 + (gi & 3)] = t[sp];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_sum[warp] = part;
+    __syncthreads();
+    int asum = 0;
+#pragma unroll
+    for (int i = 0; i < WARPS; ++i) asum += s_sum[i];
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        scale_out[0] = sc;
+        sum_out[0] = asum;
+    }
+    if (row0 >= n) return;
+    int acc[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) acc[r] = 0;
+    for (int64_t jj = lane; jj < kv; jj += 32 * kUnroll) {
+        if (jj != lane) load_batch(jj);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t j = jj + 32 * u;
+            if (j >= kv) break;
+            // the activations of vector j: planes s = 0..3, word q = 0..3
+            int4 ta[4];
+#pragma unroll
+            for (int sp = 0; sp < 4; ++sp) ta[sp] = s_act[sp * kv + j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int at[4] = {(&ta[0].x)[q], (&ta[1].x)[q], (&ta[2].x)[q], (&ta[3].x)[q]};
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const uint32_t word = q == 0 ? wv[u][r].x
+                                        : q == 1 ? wv[u][r].y
+                                        : q == 2 ? wv[u][r].z
+                                                 : wv[u][r].w;
+                    acc[r] = ternary_dot16(word, at, acc[r]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        int v = acc[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[r] = v;
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            if (row0 + r >= n) break;
+            const int d = acc[r] - asum;
+            y[row0 + r] = sc != 0.0f ? __fdiv_rn(__fmul_rn((float)d, absmean), sc) : 0.0f;
+        }
+    }
+}
+
 template <int MT, int ROWS>
 cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, const float *scale,
                           const int32_t *asum, float *y, int32_t *dot, int64_t m, int64_t n,
@@ -505,6 +648,29 @@ cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *a
     if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
     if (m <= 8) return launch_bitnet<8, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
     return launch_bitnet<16, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
+}
+
+bool bitnet_linear_fused_supported(int64_t m, int64_t k, int64_t ldx, const void *x, const void *aq) {
+    return m == 1 && k % 64 == 0 && k <= 32768 && ldx >= k &&
+           (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(aq) & 15) == 0;
+}
+
+cudaError_t launch_bitnet_linear_fused(const uint32_t *w, float absmean, const float *x, int8_t *aq,
+                                       float *scale, int32_t *sum, float *y, int64_t n, int64_t k,
+                                       cudaStream_t s, bool pdl) {
+    // 3 rows per warp, 8 warps: 3.96 us per step at N=6912, K=2560 (rows x
+    // warps 2x8: 4.01, 4x16: 4.12, 4x8: 4.36, 2x6: 4.48, 4x4: 4.63, 8x8: 4.63,
+    // 2x4: 5.39, 4x2: 5.87, 1x16: 6.05, 1x8: 6.47, 16x4: 8.57; two launches,
+    // quantizer then GEMV: 5.03)
+    constexpr int kRows = 3, kW = 8;
+    const dim3 grid((unsigned)((n + kW * kRows - 1) / (kW * kRows)));
+    const size_t smem = (size_t)k;  // one byte per code
+    if (pdl)
+        return launch_kernel(bitnet_linear_m1_kernel<kRows, kW, true>, grid, dim3(kW * 32), smem, s,
+                             true, w, absmean, x, aq, scale, sum, y, n, k);
+    bitnet_linear_m1_kernel<kRows, kW, false><<<grid, kW * 32, smem, s>>>(w, absmean, x, aq, scale,
+                                                                          sum, y, n, k);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_linear_grouped(const LinearGroup &tab, bool pdl, cudaStream_t s) {

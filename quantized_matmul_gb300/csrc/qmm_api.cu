@@ -390,6 +390,9 @@ qmm_status qmm_linear_bitnet(const uint32_t *w, float weight_absmean, const floa
     if (qmm_status st = check_device()) return st;
     const bool pdl = (flags & QMM_LINEAR_PDL) != 0;
     const cudaStream_t s = as_stream(stream);
+    if (qmm::bitnet_linear_fused_supported(m, k, ldx, x, aq))
+        return launch_status(qmm::launch_bitnet_linear_fused(w, weight_absmean, x, aq, act_scale,
+                                                             act_sum, y, n, k, s, pdl));
     cudaError_t e = qmm::launch_quantize_act_bitnet(x, m, k, ldx, aq, act_scale, act_sum, s, pdl);
     if (e != cudaSuccess) return QMM_ERR_CUDA;
     return launch_status(qmm::launch_bitnet_gemv(w, weight_absmean, aq, act_scale, act_sum, y, nullptr,

@@ -98,6 +98,14 @@ cudaError_t launch_gemv_q4_0_q8_0_noalloc(const uint8_t *wq, const uint16_t *wd,
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s, bool pdl = false);
+// The BitNet decode step for m = 1 in one kernel (every CTA quantizes the
+// row itself; CTA 0 writes aq, scale and sum): when m == 1, k % 64 == 0,
+// k <= 32768 and x, aq are 16-byte aligned (x's row stride does not matter
+// at m = 1).
+bool bitnet_linear_fused_supported(int64_t m, int64_t k, int64_t ldx, const void *x, const void *aq);
+cudaError_t launch_bitnet_linear_fused(const uint32_t *w, float absmean, const float *x, int8_t *aq,
+                                       float *scale, int32_t *sum, float *y, int64_t n, int64_t k,
+                                       cudaStream_t s, bool pdl);
 // y[i] = sum over slices s of partials[s * count + i], slices in order.
 cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count, int split,
                                  cudaStream_t s);
