@@ -623,6 +623,9 @@ def run_bitnet(q, steps, warmup, dist, peaks):
             "frac_hbm_nominal": round(gbs / dist.world / NOMINAL_HBM_GBS, 4),
             "us_per_step": round(ms * 1e3 / steps, 3), "algorithmic_bytes_per_step": step_bytes,
             "gpu_launches_per_step": 1, "weight_copies": rot,
+            "traffic": recorded_traffic("bitnet_linear_m1_kernel<3,8,1>"),
+            "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
+                            "(profiles/traffic.txt)",
             "gemv_alone": {"value": round(gbs_g, 1), "unit": "GB/s",
                            "frac_hbm": round(gbs_g / dist.world / peaks["hbm_gbs"], 4),
                            "us_per_launch": round(ms_g * 1e3 / steps, 3),
@@ -705,14 +708,14 @@ def int8_fraction(tops_per_gpu: float, peaks) -> dict:
                               "SM (tcgen05.mma kind::i8 does not assemble for sm_103a)"}
 
 
-def run_vocab(q, steps, warmup, dist, peaks):
+def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
     import torch
     n, k = 128256, 4096
     wts, x = _quantized_weights(q, 13, n, k, 128, 1)
     wq, wd = wts[0]
     out = {"workload": "Q4_0xQ8_0 vocabulary projection K=4096 N=128256 (seed 13), "
                        "weights 295.5 MB > 2x L2", "m": {}}
-    for m in (1, 8, 16, 32, 128):
+    for m in ms_list:
         aq, ad = q.quantize_act_q8_0(_up(x[:m]))
         y = torch.empty((m, n), dtype=torch.float32, device="cuda")
         ws = torch.empty((q.workspace_bytes(q.OP_GEMM, m, n, k),), dtype=torch.uint8,
@@ -728,6 +731,8 @@ def run_vocab(q, steps, warmup, dist, peaks):
             res[name] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1),
                          "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
                          "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2)}
+        if m == 16:
+            res["gemm"]["traffic"] = recorded_traffic("gemm_small_m_kernel<1,2,0>")
         res["faster"] = min((r for r in res if r in ("gemv", "gemm")), key=lambda r: res[r]["us"])
         out["m"][str(m)] = res
     return out
@@ -896,9 +901,14 @@ def main():
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
+    ap.add_argument("--vocab-m", default="1,8,16,32,128",
+                    help="token counts of the vocabulary sweep (comma-separated, each <= 128)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    vocab_m = tuple(int(v) for v in args.vocab_m.split(","))
+    if not vocab_m or any(not 1 <= v <= 128 for v in vocab_m):
+        ap.error("--vocab-m takes token counts from 1 to 128")
     dist = Dist()
     try:
         if args.impl == "reference":
@@ -917,7 +927,7 @@ def main():
             run = {"gemv": lambda: run_single_gemv(q, args.steps, args.warmup, dist, peaks),
                    "bitnet": lambda: run_bitnet(q, args.steps, args.warmup, dist, peaks),
                    "prefill": lambda: run_prefill(q, args.steps, args.warmup, dist, peaks),
-                   "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks),
+                   "vocab": lambda: run_vocab(q, args.steps, args.warmup, dist, peaks, vocab_m),
                    "bitnet_prefill": lambda: run_bitnet_prefill(q, args.steps, args.warmup, dist,
                                                                 peaks),
                    "q8_gemv": lambda: run_q8_gemv(q, args.steps, args.warmup, dist, peaks),
@@ -937,7 +947,8 @@ def main():
             configs["prefill_512x14336x4096"] = run_prefill(q, max(50, short // 20), 10, dist, peaks)
             configs["bitnet_prefill_2048x6912x2560"] = run_bitnet_prefill(q, max(50, short // 20),
                                                                           10, dist, peaks)
-            configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks)
+            configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks,
+                                                     vocab_m)
             configs["prefill_repacked_512x14336x4096"] = run_prefill_repacked(
                 q, max(50, short // 20), 10, dist, peaks)
             configs["q8_0_gemv_4096x4096"] = run_q8_gemv(q, short * 5, args.warmup, dist, peaks)
