@@ -150,6 +150,19 @@ def test_linear_bitnet_argument_errors(lib):
     assert f(A16, 1.0, A16, 32, A16, A16, A16, A16, 1, 1, 32, 4, None) == QMM_ERR_ARG
 
 
+def test_mma_probe_argument_errors(lib):
+    A16 = _p(0x10000)  # never dereferenced: every call below fails its host checks
+    f = lib.qmm_debug_mma_probe
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                  ctypes.c_void_p]
+    macs = ctypes.c_int64(0)
+    assert f(0, 10, None, 1 << 20, ctypes.byref(macs), None) == QMM_ERR_NULL
+    assert f(0, 10, A16, 1 << 20, None, None) == QMM_ERR_NULL
+    assert f(2, 10, A16, 1 << 20, ctypes.byref(macs), None) == QMM_ERR_ARG
+    assert f(0, 0, A16, 1 << 20, ctypes.byref(macs), None) == QMM_ERR_ARG
+
+
 def test_auto_split_policy(lib):
     # a narrow output with a long reduction is split, a wide one is not
     assert lib.qmm_gemv_auto_split(1, 256, 16384) > 1

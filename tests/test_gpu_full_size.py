@@ -92,6 +92,23 @@ def test_bitnet_6912x2560_full(qmm, orc):
     assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
 
 
+def test_bitnet_decode_step_6912x2560_full(qmm, orc):
+    """The BitNet decode step as the benchmark times it (qmm_linear_bitnet with
+    PDL, one kernel at m = 1), seed 3: codes, scale and sum, and every output,
+    bit for bit."""
+    n, k = 6912, 2560
+    t, x, absmean = synthetic.bitnet_case(3, n, k, 1)
+    tw = orc.pack_ternary(t)
+    aq_ref, s_ref, asum_ref = orc.quantize_act_bitnet(x)
+    y, aq, s, asum = qmm.linear_bitnet(to_dev(x), to_dev(tw.view(np.int32)), absmean, pdl=True,
+                                       codes=True)
+    assert np.array_equal(to_np(aq), aq_ref)
+    assert np.array_equal(to_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(to_np(asum), asum_ref)
+    ref = orc.bitnet_gemv(tw, absmean, aq_ref, s_ref, asum_ref)
+    assert np.array_equal(to_np(y).view(np.uint32), ref.view(np.uint32))
+
+
 # token rows of the prefill outputs the oracle recomputes (first, tile edges, last)
 PREFILL_ROWS = np.r_[0, 1, 127, 128, 255, 300, 383, 384, 510, 511]
 
@@ -139,10 +156,11 @@ def test_prefill_q8_0_weights_sampled_rows(qmm, orc):
 
 
 def test_vocab_128256x4096(qmm, orc):
-    """Vocabulary projection K=4096, N=128256, seed 13, for m = 1, 16, 128 as
-    the benchmark runs them: the m=1 GEMV on every output; for m=16 the GEMV
-    and the GEMM, and for m=128 the GEMM, on sampled weight rows (ends of the
-    range and of 128-row tiles)."""
+    """Vocabulary projection K=4096, N=128256, seed 13, for m = 1, 8, 16, 32,
+    128 as the benchmark runs them: the m=1 GEMV on every output; for m=8 and
+    16 the GEMV and the GEMM (the few-token product), for m=32 the few-token
+    product and for m=128 the tcgen05 GEMM, on sampled weight rows (ends of
+    the range and of 128-row tiles)."""
     n, k = 128256, 4096
     w, x = synthetic.q4_0_case(13, n, k, 128)
     wq, wd = orc.quantize_q4_0(w)
@@ -154,7 +172,7 @@ def test_vocab_128256x4096(qmm, orc):
     _check_decode(y1, orc, wq, wd, np.ascontiguousarray(aq[:1]), np.ascontiguousarray(ad[:1]))
     cols = np.r_[0:130, 64000:64130, n - 130:n]
     wqs, wds = np.ascontiguousarray(wq[cols]), np.ascontiguousarray(wd[cols])
-    for m in (16, 128):
+    for m in (8, 16, 32, 128):
         a, d = np.ascontiguousarray(aq[:m]), np.ascontiguousarray(ad[:m])
         ref = orc.gemm_q4_0_q8_0(wqs, wds, a, d)
         y_gemm = to_np(qmm.gemm_q4_0_q8_0(dwq, dwd, to_dev(a), f16(d)))
