@@ -585,6 +585,34 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64,0>")}
 
 
+def run_q8_vocab(q, steps, warmup, dist, peaks, ms_list=(8, 16)):
+    """Q8_0 weights x Q8_0 at the vocabulary shape (K=4096, N=128256, seed
+    13) for a few tokens: the GEMM call, which takes the few-token product."""
+    import torch
+    n, k = 128256, 4096
+    wts, x = _q8_weights(q, 13, n, k, max(ms_list), 1)
+    w8, wd = wts[0]
+    out = {"workload": "Q8_0xQ8_0 vocabulary projection K=4096 N=128256 (seed 13; Q8_0 "
+                       "weights, 558.4 MB > 2x L2)", "m": {}}
+    for m in ms_list:
+        aq, ad = q.quantize_act_q8_0(_up(x[:m]))
+        y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        ws = torch.empty((q.workspace_bytes(q.OP_GEMM_Q8, m, n, k),), dtype=torch.uint8,
+                         device="cuda")
+        ms, _ = GraphTimer(lambda i: q.gemm_q8_0_q8_0(w8, wd, aq, ad, y=y, workspace=ws),
+                           1).time(steps, warmup, dist)
+        t = ms * 1e-3 / steps
+        nbytes = q8_weight_bytes(n, k) + m * k + 2 * m * (k // QK) + 4 * m * n
+        gb = dist.world * nbytes / t / 1e9
+        out["m"][str(m)] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1),
+                            "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
+                            "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2),
+                            "algorithmic_bytes_per_launch": nbytes}
+        if m == 16:
+            out["m"][str(m)]["traffic"] = recorded_traffic("gemm_small_m_kernel<32,1,2,0>")
+    return out
+
+
 def run_bitnet(q, steps, warmup, dist, peaks):
     """The BitNet decode step: per-row activation quantization + ternary
     GEMV in one call (qmm_linear_bitnet with programmatic dependent launch;
@@ -732,7 +760,7 @@ def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
                          "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
                          "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2)}
         if m == 16:
-            res["gemm"]["traffic"] = recorded_traffic("gemm_small_m_kernel<1,2,0>")
+            res["gemm"]["traffic"] = recorded_traffic("gemm_small_m_kernel<16,1,2,0>")
         res["faster"] = min((r for r in res if r in ("gemv", "gemm")), key=lambda r: res[r]["us"])
         out["m"][str(m)] = res
     return out
@@ -897,7 +925,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
     ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill",
-                                       "q8_gemv", "q8_prefill", "prefill_repacked"],
+                                       "q8_gemv", "q8_prefill", "q8_vocab", "prefill_repacked"],
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
@@ -932,6 +960,7 @@ def main():
                                                                 peaks),
                    "q8_gemv": lambda: run_q8_gemv(q, args.steps, args.warmup, dist, peaks),
                    "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks),
+                   "q8_vocab": lambda: run_q8_vocab(q, args.steps, args.warmup, dist, peaks),
                    "prefill_repacked": lambda: run_prefill_repacked(q, args.steps, args.warmup,
                                                                     dist, peaks)}
             res = run[args.only]()
@@ -954,6 +983,8 @@ def main():
             configs["q8_0_gemv_4096x4096"] = run_q8_gemv(q, short * 5, args.warmup, dist, peaks)
             configs["q8_0_prefill_512x14336x4096"] = run_q8_prefill(q, max(50, short // 20), 10,
                                                                     dist, peaks)
+            configs["q8_0_vocab_4096x128256"] = run_q8_vocab(q, max(50, short // 20), 10, dist,
+                                                             peaks)
         cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
         if dist.rank == 0:
             line = {

@@ -307,8 +307,13 @@ qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
  * qmm_gemm_q4_0_q8_0: the int8 codes are exact in fp16, the block sums exact
  * in the f32 TMEM accumulators, and each f32 output accumulates
  * fma(sumi, dw*da, acc) over blocks in ascending order, bit for bit the
- * serial definition.  Workspace: qmm_workspace_bytes(QMM_OP_GEMM_Q8_0_Q8_0,
- * m, n, k, 0) bytes, 256-byte aligned; w8 16-byte aligned; the rest as for
+ * serial definition.  For a few tokens (m <= 32, k % 256 == 0, wd 16-byte
+ * aligned) the call runs the warp-level product described at
+ * qmm_gemm_q4_0_q8_0, reading each int8 code as the fp16 value 1152 + code
+ * (one logic instruction) and taking 1152 times the activations' block sum
+ * out exactly; same block sums, same bits of y.  Workspace:
+ * qmm_workspace_bytes(QMM_OP_GEMM_Q8_0_Q8_0, m, n, k, 0) bytes (it covers
+ * either product), 256-byte aligned; w8 16-byte aligned; the rest as for
  * qmm_gemm_q4_0_q8_0. */
 qmm_status qmm_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
                               const int8_t *aq, const uint16_t *ad, float *y,
@@ -423,8 +428,9 @@ qmm_status qmm_debug_mma_probe(int kind, int iters, int *out, size_t out_bytes, 
                                void *stream);
 
 /* Per-block sums sumi int32 [m, n, k/32] = sum_j (nibble_j - 8) * q_j.
- * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the tensor-
- * core GEMM kernel (needs the GEMM workspace); path 2: the GEMM on repacked
+ * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the GEMM
+ * call (the few-token product for m <= 32 and k % 256 == 0, else the tensor-
+ * core GEMM kernel; needs the GEMM workspace); path 2: the GEMM on repacked
  * weights (wq then points at the repacked tiles, see qmm_repack_q4_0_gemm).  Same alignment rules as the
  * product entry points; sumi 4-byte aligned. */
 qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int8_t *aq,
@@ -433,7 +439,8 @@ qmm_status qmm_debug_block_sums_q4_0_q8_0(int path, const uint8_t *wq, const int
                                           void *stream);
 
 /* Per-block sums sumi int32 [m, n, k/32] = sum_j q_w * q_a of the Q8_0-weight
- * kernels: path 0 the decode GEMV, path 1 the tensor-core GEMM (needs its
+ * kernels: path 0 the decode GEMV, path 1 the GEMM call (the few-token
+ * product for m <= 32 and k % 256 == 0, else the tcgen05 kernel; needs its
  * workspace).  Rules as for qmm_debug_block_sums_q4_0_q8_0. */
 qmm_status qmm_debug_block_sums_q8_0_q8_0(int path, const int8_t *w8, const int8_t *aq,
                                           int32_t *sumi, int64_t m, int64_t n, int64_t k,

@@ -646,8 +646,9 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
 
 }  // namespace
 
-// Covers both products a Q4_0 GEMM call may launch (the few-token kernel of
-// gemm_small.cu for m <= 32, the tcgen05 kernel otherwise).
+// Covers both products a GEMM call may launch (the few-token kernel of
+// gemm_small.cu for m <= 32, the tcgen05 kernel otherwise), either weight
+// format.
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
     const size_t t = plan_ws(m, k).total;
     return gemm_small_m_supported(m, n, k) ? std::max(t, gemm_small_m_workspace_bytes(m, k)) : t;
@@ -743,6 +744,8 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
 cudaError_t launch_gemm_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m,
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s) {
+    if (gemm_small_m_supported(m, n, k) && (reinterpret_cast<uintptr_t>(wd) & 15) == 0)
+        return launch_gemm_small_m_q8(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
     return launch_gemm<64, false>(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }
 

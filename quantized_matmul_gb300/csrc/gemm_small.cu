@@ -1,13 +1,14 @@
-// Q4_0 x Q8_0 product for a few tokens (m <= 32): the decode-batch and
-// small-prefill shape, where the weights stream once and the product should
-// run at the speed of the weight read.
+// Q4_0 x Q8_0 and Q8_0 x Q8_0 products for a few tokens (m <= 32): the
+// decode-batch and small-prefill shape, where the weights stream once and the
+// product should run at the speed of the weight read.
 //
 // What it computes is the GEMM's definition (llama.cpp visual guide, lesson
 // 31 "The CPU backend", section "How the quantized dot product works"): for
 // every output y[t, n] = sum over blocks b, in ascending order, of
 // fma(sumi[t, n, b], dw[n, b] * da[t, b], acc), where sumi is the exact
-// integer dot of the 32 nibbles (minus 8) with the 32 int8 activations of
-// block b.  y is bit for bit the serial definition.
+// integer dot of the 32 weight values (nibbles minus 8, or int8 codes) with
+// the 32 int8 activations of block b.  y is bit for bit the serial
+// definition.
 //
 // Why not the tcgen05 GEMM here.  With 16 tokens a tcgen05 tile is
 // 128 rows x 16 columns per block, and each block needs its own TMEM
@@ -18,14 +19,13 @@
 // MMAs return, with no hand-off at all.  Its rate (1024 MAC/clk/SM on
 // GB300) covers a 16-token product at the weight-streaming speed.
 //
-// Exactness: weights (as 1024 + nibble, see the decode) and activations
-// (-127..127, or that over 16) are exact in fp16, and every partial sum of a
-// block's MMAs, which start from an exact integer correction, is an integer
-// of magnitude below 2^23, so the f32 accumulators hold each block sum
-// exactly (tests compare the block sums bit for bit).  The scale
-// product dw * da of two fp16 values is exact in f32; it comes from one more
-// MMA per 8-token tile whose only nonzero k-slot carries dw (A) and da (B),
-// so it arrives in the same register layout as the block sums.
+// Exactness: weights (as 1024 + nibble or 1152 + code, see the decodes) and
+// activations (-127..127, or that over 16) are exact in fp16, and every
+// partial sum of a block's two MMAs is an integer of magnitude below 2^23
+// (at most 32 x 1279 x 127 = 5.2e6), so the f32 accumulators hold it
+// exactly; adding the integer correction that takes the 1024 / 1152 offsets
+// out is exact too (tests compare the block sums bit for bit).  The scale
+// product dw * da of two fp16 values is exact in f32.
 //
 // Layout.  One MMA covers 16 weight rows (A, row-major) by 8 tokens (B) over
 // 16 k-slots.  Lane (g = lane / 4, c = lane % 4) holds A at rows g and g + 8,
@@ -33,7 +33,9 @@
 // mapped to its elements so that a row's four values are the low nibbles of
 // the lane's own four nibble bytes 4c..4c+3 of that row (elements 4c..4c+3),
 // and the same slots of the second MMA to their high nibbles (elements
-// 16+4c..16+4c+3).  The sum over a block does not depend on the order of its
+// 16+4c..16+4c+3).  With Q8_0 weights the lane's 8 code bytes 8c..8c+7 of a
+// row fill the same slots (8c, 8c+2, 8c+1, 8c+3 in the first MMA, the next
+// four in the second).  The sum over a block does not depend on the order of its
 // elements, so this only fixes how the activations are arranged: a prepass
 // writes them as fp16 in exactly the B-fragment order of that mapping (16
 // bytes per lane, block and 8-token tile), together with the activation
@@ -46,7 +48,8 @@
 // word of scales and four of corrections.
 //
 // Roles: warp 4 is the producer; per stage of 8 blocks it copies a tile of
-// 128 weight rows x 128 nibble bytes (tensor copy, 128-byte swizzle, so the
+// 128 weight rows x 128 nibble bytes (two such tiles of code bytes for Q8_0;
+// tensor copy, 128-byte swizzle, so the
 // 8 rows a lane group reads fall in 8 different bank groups; a 3-D copy that
 // lands the tile as [block][row][16 bytes] moved 16-byte pieces and streamed
 // a third slower), the 128 x 8 dw scales (tensor copy), and the stage's
@@ -72,19 +75,20 @@ constexpr int kSmRows = 128;    // weight rows per row set (one stage's tile)
 constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
 constexpr int kSmWarps = 4;     // consumer warps, 32 weight rows (two 16-row units) each
 // stages of the ring: two CTAs share an SM, each within half its shared memory
-template <int MT>
-constexpr int sm_stages() { return MT == 1 ? 4 : 3; }
+// WB: weight bytes per row and block (16: Q4_0 nibbles, 32: Q8_0 codes)
+template <int MT, int WB>
+constexpr int sm_stages() { return WB == 16 ? (MT == 1 ? 4 : 3) : 2; }
 constexpr int kSmThreads = 32 * (kSmWarps + 1);
 
 __device__ unsigned int g_small_error = 0;
 
-template <int MT>
+template <int MT, int WB>
 struct SmPlan {
-    static constexpr int kW = kSmRows * 128;           // nibble tile (128-byte swizzle)
+    static constexpr int kW = kSmRows * kSmBlocks * WB;  // weight tile(s), 128-byte swizzle
     static constexpr int kDw = kSmRows * 16;           // dw tile: 8 fp16 per row
     static constexpr int kA = kSmBlocks * MT * 1024;   // activation fragments
     static constexpr int kDa = kSmBlocks * MT * 128;   // block corrections and scales (f32)
-    static constexpr int kStages = sm_stages<MT>();
+    static constexpr int kStages = sm_stages<MT, WB>();
     static constexpr int kOffW = 0;                    // 1024-aligned swizzled tiles
     static constexpr int kOffDw = kOffW + kStages * kW;
     static constexpr int kOffA = kOffDw + kStages * kDw;
@@ -149,8 +153,8 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) {
 // The lane's 4 nibble bytes 4c..4c+3 of one block of one row (little-endian
 // in w) -> the row's A values of the block's two MMAs, as fp16 pairs.  A
 // nibble v becomes the fp16 pattern 0x6400 | v = 1024 + v (one mask-or, no
-// arithmetic); the 1024 + 8 offset is taken out exactly by the accumulator's
-// starting value (see the kernel).  Low nibbles (first MMA):
+// arithmetic); the 1024 + 8 offset is taken out exactly by the block's
+// correction (see the kernel).  Low nibbles (first MMA):
 //   lo_a = elements (4c, 4c+2)   (bytes 0 and 2: bits 0-3 and 16-19)
 //   lo_b = elements (4c+1, 4c+3) (bytes 1 and 3, after one 8-bit shift)
 // High nibbles (second MMA), left at bits 4-7 of their 16-bit half, i.e.
@@ -164,16 +168,35 @@ __device__ __forceinline__ void decode_lane_bytes(uint32_t w, uint32_t &lo_a, ui
     hi_b = (w8 & 0x00F000F0u) | 0x64006400u;
 }
 
+// The lane's 8 Q8_0 code bytes 8c..8c+7 of one block of one row (lo: bytes
+// 0-3, hi: bytes 4-7) -> the row's A values of the block's two MMAs.  A
+// signed byte b becomes the fp16 pattern 0x6400 | (b ^ 0x80) = 1152 + b (one
+// logic instruction); the 1152 offset is taken out exactly by the
+// accumulator's correction.  First MMA: lo_a = elements (8c, 8c+2),
+// lo_b = (8c+1, 8c+3); second: hi_a = (8c+4, 8c+6), hi_b = (8c+5, 8c+7).
+__device__ __forceinline__ uint32_t q8_pair(uint32_t w) {
+    return ((w ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u;
+}
+
+__device__ __forceinline__ void decode_lane_codes(uint2 w, uint32_t &lo_a, uint32_t &lo_b,
+                                                  uint32_t &hi_a, uint32_t &hi_b) {
+    lo_a = q8_pair(w.x);
+    lo_b = q8_pair(w.x >> 8);
+    hi_a = q8_pair(w.y);
+    hi_b = q8_pair(w.y >> 8);
+}
+
+// WB: weight bytes per row and block (16: Q4_0, 32: Q8_0);
 // MT: 16-token tiles (m <= 16 MT); NT: 8-token tiles used per 16-token tile
 // (1 when m <= 8: the second would hold only padding); EMIT: write the block
 // sums instead of y.
-template <int MT, int NT, bool EMIT>
+template <int WB, int MT, int NT, bool EMIT>
 __global__ void __launch_bounds__(kSmThreads, 2)
 gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_dw,
                     const uint8_t *__restrict__ afrag, const uint8_t *__restrict__ dafrag,
                     float *__restrict__ y, int32_t *__restrict__ sumi, int m, int n, int kb_total,
                     uint32_t wait_limit, int withhold_loads) {
-    using P = SmPlan<MT>;
+    using P = SmPlan<MT, WB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,7 +238,11 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bar_full[s], kTx);
-                    tma_load_2d(smem + P::kOffW + s * P::kW, &tm_w, &bar_full[s], j * 128, rs * kSmRows);
+                    // the stage's weights: one 128-byte box per 128 bytes of row
+#pragma unroll
+                    for (int h = 0; h < WB / 16; ++h)
+                        tma_load_2d(smem + P::kOffW + s * P::kW + h * kSmRows * 128, &tm_w, &bar_full[s],
+                                    (j * (WB / 16) + h) * 128, rs * kSmRows);
                     bulk_load(smem + P::kOffA + s * P::kA, afrag + (size_t)j * P::kA, P::kA, &bar_full[s]);
                     bulk_load(smem + P::kOffDa + s * P::kDa, dafrag + (size_t)j * P::kDa, P::kDa,
                               &bar_full[s]);
@@ -259,13 +286,17 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                 ok = false;
                 break;
             }
-            // weight tile: 128 rows of 128 bytes under the 128-byte swizzle,
-            // chunk b of row r at chunk b ^ (r % 8).  This lane's rows all have
-            // r % 8 = g, and the offset r * 128 + 4c has bits 4..6 clear, so
-            // the lane's 4 bytes of row r, block b sit at
-            // (r * 128 + 4c + 16 g) ^ (16 b): one XOR per row and block.
+            // weight tile(s): 128 rows of 128 bytes each under the 128-byte
+            // swizzle, 16-byte chunk q of row r at chunk q ^ (r % 8).  This
+            // lane's rows all have r % 8 = g, and its offsets have bits 4..6
+            // clear before the chunk is set, so one XOR per row and block
+            // places each read:
+            //   Q4_0: 4 bytes of block b (chunk b) at (r*128 + 4c + 16g) ^ 16b;
+            //   Q8_0: 8 bytes of block b (chunk 2(b%4) + c/2 of tile b/4) at
+            //         16384 (b/4) + ((r*128 + 8(c%2) + 16(c/2 ^ g)) ^ 32(b%4)).
             const uint8_t *wt = smem + P::kOffW + s * P::kW;
-            const uint32_t wl = (32 * warp + g) * 128 + 4 * c + 16 * g;
+            const uint32_t wl = WB == 16 ? (32 * warp + g) * 128 + 4 * c + 16 * g
+                                         : (32 * warp + g) * 128 + 8 * (c & 1) + 16 * ((c >> 1) ^ g);
             const uint8_t *at = smem + P::kOffA + s * P::kA;
             const float4 *rec = reinterpret_cast<const float4 *>(smem + P::kOffDa + s * P::kDa);
             // dw of rows g and g + 8 of both units, the stage's 8 blocks (fp16 pairs)
@@ -283,15 +314,24 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
                 uint4 a_lo[2], a_hi[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint32_t w0 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u) * 128) ^ (16u * b)));
-                    const uint32_t w1 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u + 8) * 128) ^ (16u * b)));
                     uint32_t la0, lb0, ha0, hb0, la1, lb1, ha1, hb1;
-                    decode_lane_bytes(w0, la0, lb0, ha0, hb0);
-                    decode_lane_bytes(w1, la1, lb1, ha1, hb1);
+                    if constexpr (WB == 16) {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u) * 128) ^ (16u * b)));
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(wt + ((wl + (16 * u + 8) * 128) ^ (16u * b)));
+                        decode_lane_bytes(w0, la0, lb0, ha0, hb0);
+                        decode_lane_bytes(w1, la1, lb1, ha1, hb1);
+                    } else {
+                        const uint8_t *wb = wt + (b >> 2) * (kSmRows * 128);
+                        const uint2 w0 = *reinterpret_cast<const uint2 *>(wb + ((wl + (16 * u) * 128) ^ (32u * (b & 3))));
+                        const uint2 w1 = *reinterpret_cast<const uint2 *>(wb + ((wl + (16 * u + 8) * 128) ^ (32u * (b & 3))));
+                        decode_lane_codes(w0, la0, lb0, ha0, hb0);
+                        decode_lane_codes(w1, la1, lb1, ha1, hb1);
+                    }
                     // A registers: (row g, slots 2c..), (row g+8, 2c..), (row g,
                     // 2c+8..), (row g+8, 2c+8..); slots 2c, 2c+1, 2c+8, 2c+9 of
                     // the first MMA hold elements 4c, 4c+2, 4c+1, 4c+3, of the
-                    // second 16 more
+                    // second 16 more (Q4_0), or 8c, 8c+2, 8c+1, 8c+3 and 4 more
+                    // (Q8_0)
                     a_lo[u] = make_uint4(la0, la1, lb0, lb1);
                     a_hi[u] = make_uint4(ha0, ha1, hb0, hb1);
                 }
@@ -395,9 +435,14 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
 // 128-byte record per (b, mt): for c = 0..3 the f32 corrections of tokens
 // (nt0: 2c, 2c+1, nt1: 2c, 2c+1), then for c = 0..3 their scales da as f32.
 // Tokens past m are zeros.
+//
+// With Q8_0 weights (q8) the element order follows that kernel's Q8_0
+// mapping: registers (a[8c], a[8c+2]), (a[8c+1], a[8c+3]), then
+// (a[8c+4], a[8c+6]), (a[8c+5], a[8c+7]), nothing scaled, and the weights
+// seen as 1152 + code, so cor[t] = -1152 * (a[0] + .. + a[31]).
 __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
                                        uint4 *__restrict__ afrag, uint8_t *__restrict__ rec,
-                                       int64_t m, int64_t k, int mt_count) {
+                                       int64_t m, int64_t k, int mt_count, int q8) {
     const int64_t kb = k / kQK;
     const int64_t units = kb * mt_count * 64;  // (block, tile, piece, lane)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -413,13 +458,16 @@ __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsi
         uint32_t reg[4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            uint32_t q = 0;  // four int8 codes of token t at elements 16 half + 4c ..
-            if (t < m) q = *reinterpret_cast<const uint32_t *>(aq + t * k + b * kQK + 16 * half + 4 * c);
+            // four int8 codes of token t: elements 16 half + 4c .. (Q4_0) or
+            // 8c + 4 half .. (Q8_0)
+            const int64_t e = q8 ? 8 * c + 4 * half : 16 * half + 4 * c;
+            uint32_t q = 0;
+            if (t < m) q = *reinterpret_cast<const uint32_t *>(aq + t * k + b * kQK + e);
             __half h[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 h[i] = __int2half_rn((int)(int8_t)((q >> (8 * i)) & 0xff));
-                if (half) h[i] = __hmul(h[i], sixteenth);  // exact: a power of two
+                if (half && !q8) h[i] = __hmul(h[i], sixteenth);  // exact: a power of two
             }
             reg[2 * half] = h2_bits(__halves2half2(h[0], h[2]));
             reg[2 * half + 1] = h2_bits(__halves2half2(h[1], h[3]));
@@ -437,7 +485,7 @@ __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsi
                         lo += aq[tt * k + b * kQK + e];
                         hi += aq[tt * k + b * kQK + 16 + e];
                     }
-                v[i] = (float)(-1032 * lo - 72 * hi);
+                v[i] = q8 ? (float)(-1152 * (lo + hi)) : (float)(-1032 * lo - 72 * hi);
             }
             reinterpret_cast<float4 *>(r)[c] = make_float4(v[0], v[1], v[2], v[3]);
         }
@@ -471,12 +519,12 @@ int num_sms() {
     return count;
 }
 
-template <int MT, int NT, bool EMIT>
+template <int WB, int MT, int NT, bool EMIT>
 cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, const uint8_t *afrag,
                               const uint8_t *dafrag, float *y, int32_t *sumi, int64_t m, int64_t n,
                               int64_t k, cudaStream_t s) {
-    using P = SmPlan<MT>;
-    auto kern = gemm_small_m_kernel<MT, NT, EMIT>;
+    using P = SmPlan<MT, WB>;
+    auto kern = gemm_small_m_kernel<WB, MT, NT, EMIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
     const int64_t nsets = (n + kSmRows - 1) / kSmRows;
@@ -520,10 +568,13 @@ cudaError_t gemm_small_read_and_clear_error(unsigned int *word, cudaStream_t s) 
     return e;
 }
 
-// wd / ad may be null (block-sum variant, sumi != null).
-cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
-                                const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
-                                int64_t k, void *workspace, cudaStream_t s) {
+namespace {
+
+// WB = 16: Q4_0 nibbles [n, k/2]; WB = 32: Q8_0 codes [n, k].
+template <int WB>
+cudaError_t launch_small(const void *w, const uint16_t *wd, const int8_t *aq, const uint16_t *ad,
+                         float *y, int32_t *sumi, int64_t m, int64_t n, int64_t k, void *workspace,
+                         cudaStream_t s) {
     const int mt = (int)((m + 15) / 16);
     const int64_t kb = k / kQK;
     auto *ws = static_cast<uint8_t *>(workspace);
@@ -536,17 +587,19 @@ cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int
         const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 152 * 8);
         gemm_small_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(
             aq, reinterpret_cast<const unsigned short *>(sumi ? nullptr : ad),
-            reinterpret_cast<uint4 *>(afrag), dafrag, m, k, mt);
+            reinterpret_cast<uint4 *>(afrag), dafrag, m, k, mt, WB == 32 ? 1 : 0);
         cudaError_t e = cudaPeekAtLastError();
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tw, tdw;
-    // nibbles: u8 [n rows, k/2 bytes], box 128 bytes x 128 rows, 128-byte swizzle
-    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)(k / 2), (uint64_t)n,
-                     (uint64_t)(k / 2), 128, kSmRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    // weights: u8 [n rows, k WB / 32 bytes], box 128 bytes x 128 rows,
+    // 128-byte swizzle (a Q8_0 stage takes two boxes)
+    const uint64_t row_bytes = (uint64_t)(kb * WB);
+    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, (uint64_t)n, row_bytes, 128,
+                     kSmRows, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // dw: fp16 [n rows, k/32], box 8 x 128 (the block-sum variant reads none
-    // and maps the nibbles again as a placeholder)
+    // and maps the weights again as a placeholder)
     if (sumi) {
         tdw = tw;
     } else if (!make_map_2d(&tdw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wd, (uint64_t)kb, (uint64_t)n,
@@ -554,15 +607,30 @@ cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int
         return cudaErrorInvalidValue;
     }
     // m <= 8 runs one 8-token tile per block (measured 74 against 94 us at
-    // the vocabulary shape)
+    // the vocabulary shape with Q4_0 weights)
     if (m <= 8)
-        return sumi ? launch_small_tile<1, 1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                    : launch_small_tile<1, 1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+        return sumi ? launch_small_tile<WB, 1, 1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                    : launch_small_tile<WB, 1, 1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
     if (mt == 1)
-        return sumi ? launch_small_tile<1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                    : launch_small_tile<1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
-    return sumi ? launch_small_tile<2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                : launch_small_tile<2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+        return sumi ? launch_small_tile<WB, 1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                    : launch_small_tile<WB, 1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+    return sumi ? launch_small_tile<WB, 2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
+                : launch_small_tile<WB, 2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+}
+
+}  // namespace
+
+// wd / ad may be null (block-sum variant, sumi != null).
+cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                                const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
+                                int64_t k, void *workspace, cudaStream_t s) {
+    return launch_small<16>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
+}
+
+cudaError_t launch_gemm_small_m_q8(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
+                                   int64_t k, void *workspace, cudaStream_t s) {
+    return launch_small<32>(w8, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }
 
 }  // namespace qmm

@@ -148,6 +148,9 @@ size_t gemm_small_m_workspace_bytes(int64_t m, int64_t k);
 cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                 const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
                                 int64_t k, void *workspace, cudaStream_t s);
+cudaError_t launch_gemm_small_m_q8(const int8_t *w8, const uint16_t *wd, const int8_t *aq,
+                                   const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,
+                                   int64_t k, void *workspace, cudaStream_t s);
 void gemm_small_set_wait_limit(uint32_t iterations);
 void gemm_small_set_withhold_loads(int enable);
 cudaError_t gemm_small_read_and_clear_error(unsigned int *word, cudaStream_t s);

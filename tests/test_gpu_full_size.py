@@ -182,3 +182,22 @@ def test_vocab_128256x4096(qmm, orc):
             absterms = orc.gemm_q4_0_q8_0_absterms(wqs, wds, a, d)
             ok, worst, maxrel = rel_gate(y_gemv[:, cols], ref, absterms)
             assert ok, (m, worst, maxrel)
+
+
+def test_vocab_q8_0_weights_few_tokens(qmm, orc):
+    """The vocabulary projection with Q8_0 weights (K=4096, N=128256, seed
+    13) for m = 8 and 16, the few-token product as timed, on sampled weight
+    rows (ends of the range and of 128-row sets), bit for bit."""
+    n, k = 128256, 4096
+    w, x = synthetic.q4_0_case(13, n, k, 16)
+    w8, wd = orc.quantize_q8_0(w)
+    del w
+    aq, ad = orc.quantize_q8_0(x)
+    dw8, dwd = to_dev(w8), f16(wd)
+    cols = np.r_[0:130, 64000:64130, n - 130:n]
+    w8s, wds = np.ascontiguousarray(w8[cols]), np.ascontiguousarray(wd[cols])
+    for m in (8, 16):
+        a, d = np.ascontiguousarray(aq[:m]), np.ascontiguousarray(ad[:m])
+        y = to_np(qmm.gemm_q8_0_q8_0(dw8, dwd, to_dev(a), f16(d)))
+        ref = orc.gemm_q8_0_q8_0(w8s, wds, a, d)
+        assert np.array_equal(y[:, cols].view(np.uint32), ref.view(np.uint32))

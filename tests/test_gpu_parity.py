@@ -417,6 +417,63 @@ def test_gemm_q8_0_is_bit_identical_to_serial_order(qmm, orc, m, n, k):
     assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
 
 
+# The few-token product with Q8_0 weights (m <= 32, k % 256 == 0): each code
+# read as the fp16 value 1152 + code, two 128-byte swizzled boxes per stage.
+@pytest.mark.parametrize("m,n,k", GEMM_SMALL_SHAPES)
+def test_gemm_small_m_q8_0_block_sums_and_y_bit_exact(qmm, orc, m, n, k):
+    w8, wd, aq, ad = q8_case(orc, 8400 + m + n, m, n, k)
+    dw8, daq = to_dev(w8), to_dev(aq)
+    sumi = to_np(qmm.debug_block_sums_q8(1, dw8, daq))
+    assert np.array_equal(sumi, orc.block_sums_q8_0(w8, aq))
+    y = to_np(qmm.gemm_q8_0_q8_0(dw8, to_dev(wd.view(np.float16)), daq, to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q8_0_q8_0(w8, wd, aq, ad).view(np.uint32))
+
+
+def test_gemm_small_m_q8_0_extreme_codes_bit_exact(qmm, orc):
+    """Codes at the ends of the int8 range, whole blocks of them, so that a
+    block's MMA partial sums reach their largest magnitude (32 x (1152 + 127)
+    x 127 = 5.2e6, still an integer an f32 holds): block sums and y bit for
+    bit."""
+    m, n, k = 16, 136, 2048
+    rng = np.random.default_rng(8500)
+    w8 = rng.choice(np.array([-128, -127, 127], dtype=np.int8), size=(n, k))
+    aq = rng.choice(np.array([-127, 127], dtype=np.int8), size=(m, k))
+    w8[:8, :] = 127                   # whole rows of the largest code ...
+    aq[:4, :] = 127                   # ... against whole tokens of +127
+    w8[8:16, :] = -128                # and of the smallest code
+    aq[4:8, :] = -127
+    wd = (rng.random((n, k // QK)) * 0.01).astype(np.float16).view(np.uint16)
+    ad = (rng.random((m, k // QK)) * 0.05).astype(np.float16).view(np.uint16)
+    dw8, daq = to_dev(w8), to_dev(aq)
+    sumi = to_np(qmm.debug_block_sums_q8(1, dw8, daq))
+    ref = orc.block_sums_q8_0(w8, aq)
+    assert ref.max() == 32 * 128 * 127 and ref.min() == -32 * 128 * 127
+    assert np.array_equal(sumi, ref)
+    y = to_np(qmm.gemm_q8_0_q8_0(dw8, to_dev(wd.view(np.float16)), daq, to_dev(ad.view(np.float16))))
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q8_0_q8_0(w8, wd, aq, ad).view(np.uint32))
+
+
+def test_gemm_small_m_q8_0_wait_timeout_reports_and_device_stays_usable(qmm, orc):
+    import torch
+    w8, wd, aq, ad = q8_case(orc, 8600, 16, 300, 1024)
+    args = (to_dev(w8), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+    assert qmm.check_device_error() == 0
+    try:
+        qmm.set_wait_limit(2000)
+        qmm.withhold_gemm_loads(True)
+        qmm.gemm_q8_0_q8_0(*args)
+        torch.cuda.synchronize()
+        status = qmm.check_device_error()
+    finally:
+        qmm.withhold_gemm_loads(False)
+        qmm.set_wait_limit(0)
+    assert status == 7
+    y = to_np(qmm.gemm_q8_0_q8_0(*args))
+    torch.cuda.synchronize()
+    assert qmm.check_device_error() == 0
+    assert np.array_equal(y.view(np.uint32), orc.gemm_q8_0_q8_0(w8, wd, aq, ad).view(np.uint32))
+
+
 def test_gemm_and_gemv_q8_0_agree_with_adversarial_activations(qmm, orc):
     m, n, k = 9, 200, 4096
     w, _ = synthetic.q4_0_case(63, n, k, 1)
