@@ -55,10 +55,15 @@
 // a third slower), the 128 x 8 dw scales (tensor copy), and the stage's
 // activation fragments, corrections and scales (bulk copies).  Warps 0..3
 // each own 32 weight rows for every token tile and keep their accumulators in
-// registers across the whole reduction; two CTAs share an SM.  CTAs
-// are persistent and walk 128-row sets (sets of 128 rows keep the last round
-// of a large product short: 1002 sets over 152 SMs is 6.6 per SM).  Every
-// mbarrier wait is bounded, as in the other kernels.
+// registers across the whole reduction; two or three CTAs share an SM.
+// CTAs are persistent over 128-row sets (sets of 128 rows keep the last
+// round of a large product short: 1002 sets over 152 SMs is 6.6 per SM);
+// after its first set (its block index) a CTA takes the next free one from a
+// counter, so the sets spread evenly over the SMs however the CTAs were
+// placed (a fixed stride put two 4-set CTAs on some SMs: 8 sets there against
+// 6.6 on average).  The product is a programmatic dependent launch after the
+// prepass: its first weight copies overlap the prepass.  Every mbarrier wait
+// is bounded, as in the other kernels.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -74,31 +79,40 @@ namespace {
 constexpr int kSmRows = 128;    // weight rows per row set (one stage's tile)
 constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
 constexpr int kSmWarps = 4;     // consumer warps, 32 weight rows (two 16-row units) each
-// stages of the ring: two CTAs share an SM, each within half its shared memory
-// WB: weight bytes per row and block (16: Q4_0 nibbles, 32: Q8_0 codes)
-template <int MT, int WB>
-constexpr int sm_stages() { return WB == 16 ? (MT == 1 ? 4 : 3) : 2; }
+// CTAs per SM and stages of each CTA's ring, per shape (WB: weight bytes per
+// row and block, 16 for Q4_0 nibbles, 32 for Q8_0 codes; MT, NT as for the
+// kernel).  Q4_0 at 9..16 tokens runs three CTAs of two stages (measured
+// 92.4 against 95.9 us for two CTAs of four at the vocabulary shape; with one
+// 8-token tile, and for 17..32 tokens, three CTAs gain nothing); the rest two
+// CTAs, each within half the SM's shared memory.
+template <int WB, int MT, int NT>
+constexpr int sm_ctas() { return WB == 16 && MT == 1 && NT == 2 ? 3 : 2; }
+template <int WB, int MT, int NT>
+constexpr int sm_stages() {
+    return WB == 32 ? 2 : MT == 2 ? 3 : NT == 2 ? 2 : 4;
+}
 constexpr int kSmThreads = 32 * (kSmWarps + 1);
 
 __device__ unsigned int g_small_error = 0;
 
-template <int MT, int WB>
+template <int WB, int MT, int NT>
 struct SmPlan {
     static constexpr int kW = kSmRows * kSmBlocks * WB;  // weight tile(s), 128-byte swizzle
     static constexpr int kDw = kSmRows * 16;           // dw tile: 8 fp16 per row
     static constexpr int kA = kSmBlocks * MT * 1024;   // activation fragments
     static constexpr int kDa = kSmBlocks * MT * 128;   // block corrections and scales (f32)
-    static constexpr int kStages = sm_stages<MT, WB>();
+    static constexpr int kStages = sm_stages<WB, MT, NT>();
     static constexpr int kOffW = 0;                    // 1024-aligned swizzled tiles
     static constexpr int kOffDw = kOffW + kStages * kW;
     static constexpr int kOffA = kOffDw + kStages * kDw;
     static constexpr int kOffDa = kOffA + kStages * kA;
     static constexpr int kOffBar = kOffDa + kStages * kDa;
     static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kBytes = kOffMisc + 16 + 4 * kStages;  // abort flag, stage row sets
     static constexpr int kAlloc = kBytes + 1024;       // slack for the 1024-byte round-up
     static_assert(kW % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
-    static_assert(2 * kAlloc <= 227 * 1024, "two CTAs fit one SM's shared memory");
+    // the SM's 228 KB hold the CTAs' allocations and 1 KB reserved per CTA
+    static_assert(sm_ctas<WB, MT, NT>() * (kAlloc + 1024) <= 228 * 1024, "the CTAs fit one SM");
 };
 
 __device__ __forceinline__ bool sm_wait(uint64_t *bar, uint32_t parity, uint32_t limit,
@@ -191,18 +205,21 @@ __device__ __forceinline__ void decode_lane_codes(uint2 w, uint32_t &lo_a, uint3
 // (1 when m <= 8: the second would hold only padding); EMIT: write the block
 // sums instead of y.
 template <int WB, int MT, int NT, bool EMIT>
-__global__ void __launch_bounds__(kSmThreads, 2)
+__global__ void __launch_bounds__(kSmThreads, sm_ctas<WB, MT, NT>())
 gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_dw,
                     const uint8_t *__restrict__ afrag, const uint8_t *__restrict__ dafrag,
-                    float *__restrict__ y, int32_t *__restrict__ sumi, int m, int n, int kb_total,
-                    uint32_t wait_limit, int withhold_loads) {
-    using P = SmPlan<MT, WB>;
+                    float *__restrict__ y, int32_t *__restrict__ sumi, unsigned int *set_counter, int m,
+                    int n, int kb_total, uint32_t wait_limit, int withhold_loads) {
+    using P = SmPlan<WB, MT, NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + P::kOffBar);
     uint64_t *bar_empty = bar_full + P::kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kOffMisc);
+    // the row set each stage of the ring holds (-1: no further set), written
+    // by the producer before it arms the stage
+    int *stage_set = reinterpret_cast<int *>(smem + P::kOffMisc + 16);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -224,37 +241,85 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
     if (warp == kSmWarps) {
         // ---------------------------------------------------------------- producer
         constexpr uint32_t kTx = (uint32_t)(P::kW + P::kA + P::kDa + (EMIT ? 0 : P::kDw));
+        auto issue_weights = [&](int s, int rs, int j) {  // stage s <- weights, dw of (rs, j)
+#pragma unroll
+            for (int h = 0; h < WB / 16; ++h)  // one 128-byte box per 128 bytes of row
+                tma_load_2d(smem + P::kOffW + s * P::kW + h * kSmRows * 128, &tm_w, &bar_full[s],
+                            (j * (WB / 16) + h) * 128, rs * kSmRows);
+            if (!EMIT)
+                tma_load_2d(smem + P::kOffDw + s * P::kDw, &tm_dw, &bar_full[s], j * kSmBlocks,
+                            rs * kSmRows);
+        };
+        auto issue_acts = [&](int s, int j) {  // stage s <- activation fragments, records of j
+            bulk_load(smem + P::kOffA + s * P::kA, afrag + (size_t)j * P::kA, P::kA, &bar_full[s]);
+            bulk_load(smem + P::kOffDa + s * P::kDa, dafrag + (size_t)j * P::kDa, P::kDa, &bar_full[s]);
+        };
+        // Row sets: the first is blockIdx.x, each further one the next free
+        // set from a counter in the workspace (zeroed by the prepass), so the
+        // sets spread over the SMs as they finish, wherever the CTAs were
+        // placed.  withhold_loads (a test hook) issues nothing, so every
+        // consumer wait can only run out its limit.
+        int rs = withhold_loads ? nsets : (int)blockIdx.x;
+        // The weights do not depend on the previous kernel on the stream (the
+        // prepass): the first stage gets its weight copies before the wait
+        // for it (programmatic dependent launch), its activation copies after.
+        // A stage is armed once, for all its bytes.  (More stages ahead of the
+        // wait put more weight traffic in front of the first activation
+        // copies: 0.1-1 us slower per launch at the vocabulary shape.)
+        const int pre = rs < nsets ? 1 : 0;
+        if (lane == 0)
+            for (int i = 0; i < pre; ++i) {
+                stage_set[i] = rs;
+                mbar_arrive_expect_tx(&bar_full[i], kTx);
+                issue_weights(i, rs, i);
+            }
+        pdl_wait();
+        __syncwarp();
         int it = 0;
         bool ok = true;
-        // withhold_loads (test hook): issue nothing, so every consumer wait
-        // can only run out its poll limit
-        for (int rs = blockIdx.x; rs < (withhold_loads ? 0 : nsets) && ok; rs += gridDim.x) {
+        while (ok && rs < nsets) {
             for (int j = 0; j < nst; ++j, ++it) {
                 const int s = it % P::kStages;
-                const uint32_t ph = (uint32_t)(it / P::kStages) & 1u;
-                if (!sm_wait(&bar_empty[s], ph ^ 1u, wait_limit, abort_flag)) {
-                    ok = false;
-                    break;
+                if (it >= pre) {
+                    if (!sm_wait(&bar_empty[s], ((uint32_t)(it / P::kStages) & 1u) ^ 1u, wait_limit,
+                                 abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        stage_set[s] = rs;
+                        mbar_arrive_expect_tx(&bar_full[s], kTx);
+                        issue_weights(s, rs, j);
+                    }
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar_full[s], kTx);
-                    // the stage's weights: one 128-byte box per 128 bytes of row
-#pragma unroll
-                    for (int h = 0; h < WB / 16; ++h)
-                        tma_load_2d(smem + P::kOffW + s * P::kW + h * kSmRows * 128, &tm_w, &bar_full[s],
-                                    (j * (WB / 16) + h) * 128, rs * kSmRows);
-                    bulk_load(smem + P::kOffA + s * P::kA, afrag + (size_t)j * P::kA, P::kA, &bar_full[s]);
-                    bulk_load(smem + P::kOffDa + s * P::kDa, dafrag + (size_t)j * P::kDa, P::kDa,
-                              &bar_full[s]);
-                    if (!EMIT)
-                        tma_load_2d(smem + P::kOffDw + s * P::kDw, &tm_dw, &bar_full[s], j * kSmBlocks,
-                                    rs * kSmRows);
-                }
+                if (lane == 0) issue_acts(s, j);
                 __syncwarp();
             }
+            int next = 0;
+            if (lane == 0) next = (int)gridDim.x + (int)atomicAdd(set_counter, 1u);
+            rs = __shfl_sync(0xffffffffu, next, 0);
         }
-        // Never leave a copy in flight: wait for the stages still pending.
-        for (int i = it > P::kStages ? it - P::kStages : 0; i < it; ++i) {
+        // no further set: one more stage, with no copies, says so (once the
+        // consumers released stage it - kStages, whose copies have landed)
+        bool sent = false;
+        if (ok && !withhold_loads) {
+            const int s = it % P::kStages;
+            if (sm_wait(&bar_empty[s], ((uint32_t)(it / P::kStages) & 1u) ^ 1u, wait_limit, abort_flag)) {
+                if (lane == 0) {
+                    stage_set[s] = -1;
+                    mbar_arrive(&bar_full[s]);
+                }
+                sent = true;
+            }
+            __syncwarp();
+        }
+        // Never leave a copy in flight: wait for the last stages issued (an
+        // abort can only come at it >= pre, so every stage armed before the
+        // wait got its activation copies too).  Stage it - kStages is skipped
+        // once the end stage went out on its slot: its copies landed, and its
+        // barrier has moved on by two phases.
+        const int first_pending = (it > P::kStages ? it - P::kStages : 0) + (sent && it >= P::kStages ? 1 : 0);
+        for (int i = first_pending; i < it; ++i) {
             volatile int no_abort = 0;
             sm_wait(&bar_full[i % P::kStages], (uint32_t)(i / P::kStages) & 1u, kDrainLimit, &no_abort);
         }
@@ -272,7 +337,15 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
     uint64_t acc[2][MT][NT][2];  // [unit][tile][8-token tile][row g | row g + 8], token pairs
     int it = 0;
     bool ok = true;
-    for (int rs = blockIdx.x; rs < nsets && ok; rs += gridDim.x) {
+    for (;;) {
+        // the next set: its first stage says which (or that there is none)
+        if (!sm_wait(&bar_full[it % P::kStages], (uint32_t)(it / P::kStages) & 1u, wait_limit,
+                     abort_flag)) {
+            ok = false;
+            break;
+        }
+        const int rs = stage_set[it % P::kStages];
+        if (rs < 0) break;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -282,7 +355,7 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
         for (int j = 0; j < nst; ++j, ++it) {
             const int s = it % P::kStages;
             const uint32_t ph = (uint32_t)(it / P::kStages) & 1u;
-            if (!sm_wait(&bar_full[s], ph, wait_limit, abort_flag)) {
+            if (j > 0 && !sm_wait(&bar_full[s], ph, wait_limit, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -397,7 +470,8 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_empty[s]);
         }
-        if (!EMIT && ok) {
+        if (!ok) break;
+        if (!EMIT) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int n0 = rs * kSmRows + 32 * warp + 16 * u + g;
@@ -429,12 +503,13 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
 // (a[16+4c+1] / 16, a[16+4c+3] / 16), all exact in fp16 (a = the int8 code
 // of element e of block b).  The first MMA sees the weights as 1024 + v and
 // the second as 1024 + 16 v against activations scaled by 1/16, i.e. 64 + v,
-// so a block's two MMAs sum (v - 8) a exactly once the accumulator starts at
+// so a block's two MMAs sum (v - 8) a exactly once the correction
 //   cor[t] = -1032 * (a[0] + .. + a[15]) - 72 * (a[16] + .. + a[31])
-// (every partial sum is an integer below 2^24 in magnitude).  Then a
-// 128-byte record per (b, mt): for c = 0..3 the f32 corrections of tokens
+// is added (every partial sum is an integer below 2^24 in magnitude).  Then
+// a 128-byte record per (b, mt): for c = 0..3 the f32 corrections of tokens
 // (nt0: 2c, 2c+1, nt1: 2c, 2c+1), then for c = 0..3 their scales da as f32.
-// Tokens past m are zeros.
+// Tokens past m are zeros.  The four lanes of a token hold all its codes of
+// the block, so its sums come from two shuffle steps.
 //
 // With Q8_0 weights (q8) the element order follows that kernel's Q8_0
 // mapping: registers (a[8c], a[8c+2]), (a[8c+1], a[8c+3]), then
@@ -442,7 +517,12 @@ gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_const
 // seen as 1152 + code, so cor[t] = -1152 * (a[0] + .. + a[31]).
 __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
                                        uint4 *__restrict__ afrag, uint8_t *__restrict__ rec,
-                                       int64_t m, int64_t k, int mt_count, int q8) {
+                                       unsigned int *set_counter, int64_t m, int64_t k, int mt_count,
+                                       int q8) {
+    // the product (launched with programmatic dependent launch) may start its
+    // weight copies now; it reads what this kernel writes only after its wait
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *set_counter = 0;  // the product's row-set counter
     const int64_t kb = k / kQK;
     const int64_t units = kb * mt_count * 64;  // (block, tile, piece, lane)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -456,6 +536,7 @@ __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsi
         const int g = lane >> 2, c = lane & 3;
         const int64_t t = mt * 16 + nt * 8 + g;
         uint32_t reg[4];
+        int part[2] = {0, 0};  // sums of the two groups of four codes
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             // four int8 codes of token t: elements 16 half + 4c .. (Q4_0) or
@@ -466,40 +547,28 @@ __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsi
             __half h[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                h[i] = __int2half_rn((int)(int8_t)((q >> (8 * i)) & 0xff));
+                const int v = (int)(int8_t)((q >> (8 * i)) & 0xff);
+                part[half] += v;
+                h[i] = __int2half_rn(v);
                 if (half && !q8) h[i] = __hmul(h[i], sixteenth);  // exact: a power of two
             }
             reg[2 * half] = h2_bits(__halves2half2(h[0], h[2]));
             reg[2 * half + 1] = h2_bits(__halves2half2(h[1], h[3]));
         }
         afrag[u] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
-        uint8_t *r = rec + bm * 128;
-        if (nt == 0 && g == 0) {
-            float v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t tt = mt * 16 + (i >> 1) * 8 + 2 * c + (i & 1);
-                int lo = 0, hi = 0;
-                if (tt < m)
-                    for (int e = 0; e < 16; ++e) {
-                        lo += aq[tt * k + b * kQK + e];
-                        hi += aq[tt * k + b * kQK + 16 + e];
-                    }
-                v[i] = q8 ? (float)(-1152 * (lo + hi)) : (float)(-1032 * lo - 72 * hi);
-            }
-            reinterpret_cast<float4 *>(r)[c] = make_float4(v[0], v[1], v[2], v[3]);
-        }
-        if (nt == 1 && g == 0) {
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (ad) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int64_t tt = mt * 16 + (i >> 1) * 8 + 2 * c + (i & 1);
-                    if (tt < m) v[i] = __half2float(__ushort_as_half(ad[tt * kb + b]));
-                }
-            }
-            reinterpret_cast<float4 *>(r + 64)[c] = make_float4(v[0], v[1], v[2], v[3]);
-        }
+        // the four lanes of token t hold all 32 of its codes in the block:
+        // lo = a[0] + .. + a[15], hi = a[16] + .. + a[31] for Q4_0 (for Q8_0
+        // only their total is used)
+        int lo = part[0], hi = part[1];
+        lo += __shfl_xor_sync(0xffffffffu, lo, 1);
+        hi += __shfl_xor_sync(0xffffffffu, hi, 1);
+        lo += __shfl_xor_sync(0xffffffffu, lo, 2);
+        hi += __shfl_xor_sync(0xffffffffu, hi, 2);
+        // token g of 8-token tile nt sits at float 4 (g / 2) + 2 nt + g % 2 of
+        // the record's correction half (and 16 floats on, its scale)
+        float *r = reinterpret_cast<float *>(rec + bm * 128) + 4 * (g >> 1) + 2 * nt + (g & 1);
+        if (c == 0) r[0] = q8 ? (float)(-1152 * (lo + hi)) : (float)(-1032 * lo - 72 * hi);
+        if (c == 1) r[16] = ad && t < m ? __half2float(__ushort_as_half(ad[t * kb + b])) : 0.0f;
     }
 }
 
@@ -521,17 +590,19 @@ int num_sms() {
 
 template <int WB, int MT, int NT, bool EMIT>
 cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, const uint8_t *afrag,
-                              const uint8_t *dafrag, float *y, int32_t *sumi, int64_t m, int64_t n,
-                              int64_t k, cudaStream_t s) {
-    using P = SmPlan<MT, WB>;
+                              const uint8_t *dafrag, float *y, int32_t *sumi, unsigned int *counter,
+                              int64_t m, int64_t n, int64_t k, cudaStream_t s) {
+    using P = SmPlan<WB, MT, NT>;
     auto kern = gemm_small_m_kernel<WB, MT, NT, EMIT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
     const int64_t nsets = (n + kSmRows - 1) / kSmRows;
-    const int grid = (int)std::min<int64_t>(nsets, 2 * num_sms());
-    kern<<<grid, kSmThreads, P::kAlloc, s>>>(tw, tdw, afrag, dafrag, y, sumi, (int)m, (int)n,
-                                             (int)(k / kQK), g_small_wait_limit, g_small_withhold);
-    return cudaPeekAtLastError();
+    const int grid = (int)std::min<int64_t>(nsets, sm_ctas<WB, MT, NT>() * num_sms());
+    // programmatic dependent launch: the CTAs start their weight copies
+    // while the prepass before them still runs
+    return launch_kernel(kern, dim3(grid), dim3(kSmThreads), P::kAlloc, s, true, tw, tdw, afrag,
+                         dafrag, y, sumi, counter, (int)m, (int)n, (int)(k / kQK), g_small_wait_limit,
+                         g_small_withhold);
 }
 
 }  // namespace
@@ -540,11 +611,13 @@ bool gemm_small_m_supported(int64_t m, int64_t /*n*/, int64_t k) {
     return m >= 1 && m <= 32 && k % (kQK * kSmBlocks) == 0;
 }
 
+// activation fragments, then the records, then the row-set counter, each
+// 256-byte aligned
 size_t gemm_small_m_workspace_bytes(int64_t m, int64_t k) {
     const int64_t mt = (m + 15) / 16;
     const int64_t kb = k / kQK;
-    const size_t a = (size_t)(kb * mt * 1024);
-    return (a + 255) / 256 * 256 + (size_t)(kb * mt * 128);
+    const size_t a = (size_t)(kb * mt * 1024), r = (size_t)(kb * mt * 128);
+    return (a + 255) / 256 * 256 + (r + 255) / 256 * 256 + 256;
 }
 
 void gemm_small_set_wait_limit(uint32_t iterations) {
@@ -578,16 +651,17 @@ cudaError_t launch_small(const void *w, const uint16_t *wd, const int8_t *aq, co
     const int mt = (int)((m + 15) / 16);
     const int64_t kb = k / kQK;
     auto *ws = static_cast<uint8_t *>(workspace);
-    const size_t a_bytes = (size_t)(kb * mt * 1024);
+    const size_t a_bytes = (size_t)(kb * mt * 1024), r_bytes = (size_t)(kb * mt * 128);
     uint8_t *afrag = ws;
     uint8_t *dafrag = ws + (a_bytes + 255) / 256 * 256;
+    auto *counter = reinterpret_cast<unsigned int *>(dafrag + (r_bytes + 255) / 256 * 256);
     {
         const int threads = 256;
         const int64_t units = kb * mt * 64;
         const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 152 * 8);
         gemm_small_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(
             aq, reinterpret_cast<const unsigned short *>(sumi ? nullptr : ad),
-            reinterpret_cast<uint4 *>(afrag), dafrag, m, k, mt, WB == 32 ? 1 : 0);
+            reinterpret_cast<uint4 *>(afrag), dafrag, counter, m, k, mt, WB == 32 ? 1 : 0);
         cudaError_t e = cudaPeekAtLastError();
         if (e != cudaSuccess) return e;
     }
@@ -609,13 +683,13 @@ cudaError_t launch_small(const void *w, const uint16_t *wd, const int8_t *aq, co
     // m <= 8 runs one 8-token tile per block (measured 74 against 94 us at
     // the vocabulary shape with Q4_0 weights)
     if (m <= 8)
-        return sumi ? launch_small_tile<WB, 1, 1, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                    : launch_small_tile<WB, 1, 1, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+        return sumi ? launch_small_tile<WB, 1, 1, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
+                    : launch_small_tile<WB, 1, 1, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
     if (mt == 1)
-        return sumi ? launch_small_tile<WB, 1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                    : launch_small_tile<WB, 1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
-    return sumi ? launch_small_tile<WB, 2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s)
-                : launch_small_tile<WB, 2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, m, n, k, s);
+        return sumi ? launch_small_tile<WB, 1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
+                    : launch_small_tile<WB, 1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
+    return sumi ? launch_small_tile<WB, 2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
+                : launch_small_tile<WB, 2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
 }
 
 }  // namespace

@@ -73,13 +73,16 @@ def test_workspace_queries(lib):
     rows = ((k // 32) * 4 * 16 + 255) // 256 * 256
     # m <= 32 with k a multiple of 256 may run the few-token product: fp16
     # activation fragments (1 KB per block and 16-token tile) + a 128-byte
-    # record of f32 block corrections and scales per block and tile; the
-    # query covers the larger layout
+    # record of f32 block corrections and scales per block and tile + 256
+    # bytes for its row-set counter, each part 256-byte rounded; the query
+    # covers the larger layout
     frags = (k // 32) * 1024
     pairs = (k // 32) * 128
-    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == max(a16 + rows, frags + pairs)
+    assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == max(a16 + rows, frags + pairs + 256)
     assert lib.qmm_workspace_bytes(2, 32, 14336, k, 0) == max(32 * k * 2 + (k // 32) * 32 * 16,
-                                                               2 * (frags + pairs))
+                                                               2 * (frags + pairs) + 256)
+    assert lib.qmm_workspace_bytes(5, 16, 14336, k, 0) == max(16 * k * 2 + (k // 32) * 16 * 16,
+                                                              frags + pairs + 256)
     k = 4064  # not a multiple of 256: the tcgen05 product only
     assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == (
         (m * k * 2 + 255) // 256 * 256 + ((k // 32) * 4 * 16 + 255) // 256 * 256)
