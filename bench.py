@@ -931,10 +931,15 @@ def main():
                          "its result; the headline contract line is not produced")
     ap.add_argument("--vocab-m", default="1,8,16,32,128",
                     help="token counts of the vocabulary sweep (comma-separated, each <= 128)")
+    ap.add_argument("--q8-vocab-m", default="8,16",
+                    help="token counts of the Q8_0-weight vocabulary sweep (each <= 32)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     vocab_m = tuple(int(v) for v in args.vocab_m.split(","))
+    q8_vocab_m = tuple(int(v) for v in args.q8_vocab_m.split(","))
+    if not q8_vocab_m or any(not 1 <= v <= 32 for v in q8_vocab_m):
+        ap.error("--q8-vocab-m takes token counts from 1 to 32")
     if not vocab_m or any(not 1 <= v <= 128 for v in vocab_m):
         ap.error("--vocab-m takes token counts from 1 to 128")
     dist = Dist()
@@ -960,7 +965,8 @@ def main():
                                                                 peaks),
                    "q8_gemv": lambda: run_q8_gemv(q, args.steps, args.warmup, dist, peaks),
                    "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks),
-                   "q8_vocab": lambda: run_q8_vocab(q, args.steps, args.warmup, dist, peaks),
+                   "q8_vocab": lambda: run_q8_vocab(q, args.steps, args.warmup, dist, peaks,
+                                                    q8_vocab_m),
                    "prefill_repacked": lambda: run_prefill_repacked(q, args.steps, args.warmup,
                                                                     dist, peaks)}
             res = run[args.only]()
@@ -984,7 +990,7 @@ def main():
             configs["q8_0_prefill_512x14336x4096"] = run_q8_prefill(q, max(50, short // 20), 10,
                                                                     dist, peaks)
             configs["q8_0_vocab_4096x128256"] = run_q8_vocab(q, max(50, short // 20), 10, dist,
-                                                             peaks)
+                                                             peaks, q8_vocab_m)
         cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
         if dist.rank == 0:
             line = {

@@ -81,15 +81,16 @@ constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
 constexpr int kSmWarps = 4;     // consumer warps, 32 weight rows (two 16-row units) each
 // CTAs per SM and stages of each CTA's ring, per shape (WB: weight bytes per
 // row and block, 16 for Q4_0 nibbles, 32 for Q8_0 codes; MT, NT as for the
-// kernel).  Q4_0 at 9..16 tokens runs three CTAs of two stages (measured
-// 92.4 against 95.9 us for two CTAs of four at the vocabulary shape; with one
-// 8-token tile, and for 17..32 tokens, three CTAs gain nothing); the rest two
-// CTAs, each within half the SM's shared memory.
+// kernel).  Q4_0 with two 8-token tiles per 16-token tile (9..32 tokens) runs
+// three CTAs of two stages (vocabulary shape: 95.9 -> 92.4 us at 16 tokens,
+// 145.5 -> 138.5 us at 32, registers capped at 128); with one 8-token tile
+// three CTAs gain nothing, and Q8_0's stages are too large for three: those
+// run two CTAs, each within half the SM's shared memory.
 template <int WB, int MT, int NT>
-constexpr int sm_ctas() { return WB == 16 && MT == 1 && NT == 2 ? 3 : 2; }
+constexpr int sm_ctas() { return WB == 16 && NT == 2 ? 3 : 2; }
 template <int WB, int MT, int NT>
 constexpr int sm_stages() {
-    return WB == 32 ? 2 : MT == 2 ? 3 : NT == 2 ? 2 : 4;
+    return WB == 32 ? 2 : NT == 2 ? 2 : 4;
 }
 constexpr int kSmThreads = 32 * (kSmWarps + 1);
 
