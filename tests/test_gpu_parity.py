@@ -169,10 +169,13 @@ def test_gemm_more_tiles_than_resident_ctas(qmm, orc, m, n, k):
 
 # The few-token product (m <= 32, k a multiple of 256: warp-level MMAs with
 # register accumulators, persistent CTAs over 128-row sets): one and two
-# 16-token tiles, ragged row sets, more row sets than SMs, long reductions.
+# 16-token tiles, ragged row sets, more row sets than SMs, long reductions,
+# and more row sets than resident CTAs (two or three per SM), so that CTAs
+# take further sets from the counter, with one stage per set (k = 256).
 GEMM_SMALL_SHAPES = [(1, 1, 256), (8, 129, 512), (16, 128, 4096), (16, 257, 2048),
                      (17, 300, 768), (31, 1000, 1024), (32, 128 * 152 * 2 + 77, 256),
-                     (20, 65, 11008)]
+                     (20, 65, 11008), (8, 128 * 700 + 3, 256), (16, 128 * 1000 + 5, 512),
+                     (29, 128 * 600 + 127, 256)]
 
 
 @pytest.mark.parametrize("m,n,k", GEMM_SMALL_SHAPES)
