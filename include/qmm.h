@@ -108,6 +108,13 @@ qmm_status qmm_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
  *   the shape.  S may not exceed k/32.  workspace: device memory of at least
  *   qmm_workspace_bytes(QMM_OP_GEMV_Q4_0_Q8_0, m, n, k, split_k) bytes,
  *   16-byte aligned (NULL allowed when that size is 0).
+ * With split_k = 0, 3 <= m, k % 256 == 0, wd 16-byte aligned and a 256-byte
+ * aligned workspace of at least the queried size (the query for split_k = 0
+ * covers it), the call runs the few-token product described at
+ * qmm_gemm_q4_0_q8_0 instead, which is faster from three tokens on; its y is
+ * the serial definition bit for bit, within this entry's tolerance.  A
+ * smaller or absent workspace keeps the GEMV kernels.  Explicit split_k >= 1
+ * always runs the GEMV kernels.
  * With one slice and 8 <= m, when k/32 is a multiple of 8, wq, wd, aq and
  * ad are 16-byte aligned and the quantized activations fit in shared memory,
  * a persistent kernel streams the weights through shared memory with tensor
@@ -297,7 +304,8 @@ qmm_status qmm_gemm_q4_0_q8_0_repacked(const uint8_t *wr, size_t wr_bytes, const
  * workspace as for qmm_gemv_q4_0_q8_0 (workspace size from
  * qmm_workspace_bytes(QMM_OP_GEMV_Q8_0_Q8_0, ...)); w8 16-byte aligned.
  * Each warp streams its rows through registers, two 16-byte loads per
- * block. */
+ * block.  With split_k = 0 and the conditions stated at qmm_gemv_q4_0_q8_0
+ * the call runs the few-token product of qmm_gemm_q8_0_q8_0 instead. */
 qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd,
                               const int8_t *aq, const uint16_t *ad, float *y,
                               int64_t m, int64_t n, int64_t k, int split_k,
@@ -386,7 +394,9 @@ qmm_status qmm_bitnet_gemm(const uint32_t *w, float weight_absmean, const int8_t
 
 /* ---------------------------------------------------------------------- */
 /* Workspace size in bytes for `op` (QMM_OP_*) at this shape; 0 when none is
- * needed; SIZE_MAX for an invalid op or shape. */
+ * needed; SIZE_MAX for an invalid op or shape.  For the GEMV ops with
+ * split_k = 0 it covers both products the call may choose (the GEMV's
+ * split-K partials, the few-token product's activation layout). */
 size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k);
 
 /* The split-K factor qmm_gemv_q4_0_q8_0 uses for split_k = 0 at this shape. */

@@ -6,6 +6,7 @@
 // small unchecked kernels, and output buffers come from the caller).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -70,6 +71,28 @@ qmm_status gemv_split(int split_k, int64_t m, int64_t n, int64_t k, int *out) {
     return QMM_OK;
 }
 
+// The decode GEMV entries with split_k = 0 (the library's choice) hand the
+// call to the few-token product of gemm_small.cu where that is faster: from
+// three tokens on (vocabulary shape, K=4096, N=128256: 70 against 117 us at
+// m = 3, 88 against 323 us at m = 16; at m = 2 the GEMV kernel is faster, 57
+// against 70), for k % 256 == 0, when the caller's workspace holds the
+// product's activation layout (qmm_workspace_bytes reports that size for
+// split_k = 0) and wd is 16-byte aligned (the product copies it with a
+// tensor map).  The product's y is the serial definition, bit for bit,
+// which is within the GEMV's tolerance.
+constexpr int64_t kFewTokenMinM = 3;
+
+bool few_token_shape(int64_t m, int64_t n, int64_t k, int split_k) {
+    return split_k == 0 && m >= kFewTokenMinM && m <= QMM_GEMV_MAX_M &&
+           qmm::gemm_small_m_supported(m, n, k);
+}
+
+bool few_token_route(int64_t m, int64_t n, int64_t k, int split_k, const void *wd,
+                     const void *workspace, size_t workspace_bytes) {
+    return few_token_shape(m, n, k, split_k) && aligned(wd, 16) && workspace &&
+           aligned(workspace, 256) && workspace_bytes >= qmm::gemm_small_m_workspace_bytes(m, k);
+}
+
 qmm_status check_linear(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
                         const int8_t *aq, const uint16_t *ad, const float *y, int64_t m,
                         int64_t n, int64_t k) {
@@ -114,6 +137,11 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const int8_
                               int split_k, void *workspace, size_t workspace_bytes, void *stream) {
     if (qmm_status st = check_q4_common(wq, wd, aq, ad, y, m, n, k)) return st;
     if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    if (few_token_route(m, n, k, split_k, wd, workspace, workspace_bytes)) {
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemm_small_m(wq, wd, aq, ad, y, nullptr, m, n, k, workspace,
+                                                      as_stream(stream)));
+    }
     int split = 1;
     if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
     const size_t need = qmm::gemv_workspace_bytes(m, n, k, split);
@@ -312,6 +340,11 @@ qmm_status qmm_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const int8_t
     const auto *wb = reinterpret_cast<const uint8_t *>(w8);
     if (qmm_status st = check_q4_common(wb, wd, aq, ad, y, m, n, k)) return st;
     if (m > QMM_GEMV_MAX_M) return QMM_ERR_SHAPE;
+    if (few_token_route(m, n, k, split_k, wd, workspace, workspace_bytes)) {
+        if (qmm_status st = check_device()) return st;
+        return launch_status(qmm::launch_gemm_small_m_q8(w8, wd, aq, ad, y, nullptr, m, n, k,
+                                                         workspace, as_stream(stream)));
+    }
     int split = 1;
     if (qmm_status st = gemv_split(split_k, m, n, k, &split)) return st;
     const size_t need = qmm::gemv_workspace_bytes(m, n, k, split);
@@ -423,17 +456,16 @@ size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k)
                                                            : qmm::bitnet_gemm_workspace_bytes(m, k);
     if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return SIZE_MAX;
     switch (op) {
-        case QMM_OP_GEMV_Q4_0_Q8_0: {
-            if (m > QMM_GEMV_MAX_M) return SIZE_MAX;
-            int split = 1;
-            if (gemv_split(split_k, m, n, k, &split) != QMM_OK) return SIZE_MAX;
-            return qmm::gemv_workspace_bytes(m, n, k, split);
-        }
+        case QMM_OP_GEMV_Q4_0_Q8_0:
         case QMM_OP_GEMV_Q8_0_Q8_0: {
             if (m > QMM_GEMV_MAX_M) return SIZE_MAX;
             int split = 1;
             if (gemv_split(split_k, m, n, k, &split) != QMM_OK) return SIZE_MAX;
-            return qmm::gemv_workspace_bytes(m, n, k, split);
+            const size_t need = qmm::gemv_workspace_bytes(m, n, k, split);
+            // enough for either product the call may run
+            return few_token_shape(m, n, k, split_k)
+                       ? std::max(need, qmm::gemm_small_m_workspace_bytes(m, k))
+                       : need;
         }
         case QMM_OP_GEMM_Q4_0_Q8_0:
         case QMM_OP_GEMM_Q8_0_Q8_0:

@@ -83,6 +83,14 @@ def test_workspace_queries(lib):
                                                                2 * (frags + pairs) + 256)
     assert lib.qmm_workspace_bytes(5, 16, 14336, k, 0) == max(16 * k * 2 + (k // 32) * 16 * 16,
                                                               frags + pairs + 256)
+    # the decode GEMV with split_k = 0 from three tokens on may run the
+    # few-token product: the query covers its layout (and stays 0 for an
+    # explicit unsplit call, which always runs the GEMV kernels)
+    for op in (1, 4):
+        assert lib.qmm_workspace_bytes(op, 3, 14336, k, 0) == frags + pairs + 256
+        assert lib.qmm_workspace_bytes(op, 16, 14336, k, 0) == frags + pairs + 256
+        assert lib.qmm_workspace_bytes(op, 3, 14336, k, 1) == 0
+        assert lib.qmm_workspace_bytes(op, 2, 14336, k, 0) == 0
     k = 4064  # not a multiple of 256: the tcgen05 product only
     assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == (
         (m * k * 2 + 255) // 256 * 256 + ((k // 32) * 4 * 16 + 255) // 256 * 256)

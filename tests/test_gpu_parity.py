@@ -221,6 +221,44 @@ def test_gemm_small_m_wait_timeout_reports_and_device_stays_usable(qmm, orc):
     assert np.array_equal(y.view(np.uint32), orc.gemm_q4_0_q8_0(wq, wd, aq, ad).view(np.uint32))
 
 
+@pytest.mark.parametrize("fmt", ["q4", "q8"])
+def test_gemv_auto_runs_the_few_token_product_from_three_tokens(qmm, orc, fmt):
+    """split_k = 0 with m >= 3 and k % 256 == 0 hands the GEMV call to the
+    few-token product (the serial definition, bit for bit); m = 2, an
+    explicit split_k = 1, or no workspace keep the GEMV kernels (within the
+    f32 gate)."""
+    import torch
+    n, k = 300, 1024
+    for m in (2, 3, 8, 16):
+        if fmt == "q4":
+            w, wd, aq, ad = q4_case(orc, 8700 + m, m, n, k)
+            ref = orc.gemm_q4_0_q8_0(w, wd, aq, ad)
+            absterms = orc.gemm_q4_0_q8_0_absterms(w, wd, aq, ad)
+            gemv, entry = qmm.gemv_q4_0_q8_0, "qmm_gemv_q4_0_q8_0"
+        else:
+            w, wd, aq, ad = q8_case(orc, 8700 + m, m, n, k)
+            ref = orc.gemm_q8_0_q8_0(w, wd, aq, ad)
+            _, absterms = orc.gemm_q8_0_q8_0_f64(w, wd, aq, ad)
+            gemv, entry = qmm.gemv_q8_0_q8_0, "qmm_gemv_q8_0_q8_0"
+        args = (to_dev(w), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+        y_auto = to_np(gemv(*args))
+        if m >= 3:
+            assert np.array_equal(y_auto.view(np.uint32), ref.view(np.uint32)), m
+        else:
+            ok, worst, maxrel = rel_gate(y_auto, ref, absterms)
+            assert ok, (m, worst, maxrel)
+        ok, worst, maxrel = rel_gate(to_np(gemv(*args, split_k=1)), ref, absterms)
+        assert ok, (m, worst, maxrel)
+        # no workspace at all: the GEMV kernels (this shape needs no split)
+        y = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+        fn = getattr(qmm.load(), entry)
+        st = fn(args[0].data_ptr(), args[1].data_ptr(), args[2].data_ptr(), args[3].data_ptr(),
+                y.data_ptr(), m, n, k, 0, None, 0, torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        ok, worst, maxrel = rel_gate(to_np(y), ref, absterms)
+        assert ok, (m, worst, maxrel)
+
+
 def test_gemm_and_gemv_agree_with_adversarial_activations(qmm, orc):
     m, n, k = 9, 200, 4096
     w, _ = synthetic.q4_0_case(61, n, k, 1)
