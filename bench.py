@@ -742,7 +742,10 @@ def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
     wts, x = _quantized_weights(q, 13, n, k, 128, 1)
     wq, wd = wts[0]
     out = {"workload": "Q4_0xQ8_0 vocabulary projection K=4096 N=128256 (seed 13), "
-                       "weights 295.5 MB > 2x L2", "m": {}}
+                       "weights 295.5 MB > 2x L2", "m": {},
+           "paths": "gemv: qmm_gemv_q4_0_q8_0 with split_k=1 (the dp4a GEMV kernels); gemm: "
+                    "qmm_gemm_q4_0_q8_0 (the few-token product for m <= 32, else tcgen05). "
+                    "qmm_gemv_q4_0_q8_0 with split_k=0 takes the few-token product from m = 3 on"}
     for m in ms_list:
         aq, ad = q.quantize_act_q8_0(_up(x[:m]))
         y = torch.empty((m, n), dtype=torch.float32, device="cuda")
