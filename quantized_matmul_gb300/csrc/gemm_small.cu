@@ -35,25 +35,25 @@
 // and the same slots of the second MMA to their high nibbles (elements
 // 16+4c..16+4c+3).  With Q8_0 weights the lane's 8 code bytes 8c..8c+7 of a
 // row fill the same slots (8c, 8c+2, 8c+1, 8c+3 in the first MMA, the next
-// four in the second).  The sum over a block does not depend on the order of its
-// elements, so this only fixes how the activations are arranged: a prepass
-// writes them as fp16 in exactly the B-fragment order of that mapping (16
-// bytes per lane, block and 8-token tile), together with the activation
-// scales as fp16 and per-token block corrections as f32.  With the weights
-// as the 16-row operand, each activation
-// fragment a warp loads from shared memory serves 16 weight rows.  Shared
-// memory delivers 128 bytes per cycle to the lanes whatever the sharing, so
-// every register a lane loads per block counts; the layouts keep that to
-// two words of weights, four words of activations per 8-token tile, one
-// word of scales and four of corrections.
+// four in the second).  The sum over a block does not depend on the order
+// of its elements, so this only fixes how the activations are arranged: a
+// prepass writes them as fp16 in exactly the B-fragment order of that
+// mapping (16 bytes per lane, block and 8-token tile), together with the
+// per-token block corrections and activation scales as f32.  With the
+// weights as the 16-row operand, each activation fragment a warp loads from
+// shared memory serves 16 weight rows.  Shared memory delivers 128 bytes
+// per cycle to the lanes whatever the sharing, so every register a lane
+// loads per block counts; the layouts keep that to one (Q4_0) or two (Q8_0)
+// words of weights per row, four words of activations per 8-token tile, and
+// one 16-byte load each of corrections and scales per 16-token tile.
 //
 // Roles: warp 4 is the producer; per stage of 8 blocks it copies a tile of
-// 128 weight rows x 128 nibble bytes (two such tiles of code bytes for Q8_0;
-// tensor copy, 128-byte swizzle, so the
-// 8 rows a lane group reads fall in 8 different bank groups; a 3-D copy that
-// lands the tile as [block][row][16 bytes] moved 16-byte pieces and streamed
-// a third slower), the 128 x 8 dw scales (tensor copy), and the stage's
-// activation fragments, corrections and scales (bulk copies).  Warps 0..3
+// 128 weight rows x 128 nibble bytes (two such tiles of code bytes for
+// Q8_0; tensor copies with 128-byte swizzle, so the 8 rows a lane group
+// reads fall in 8 different bank groups; a 3-D copy that lands the tile as
+// [block][row][16 bytes] moved 16-byte pieces and streamed a third slower),
+// the 128 x 8 dw scales (tensor copy), and the stage's activation
+// fragments, corrections and scales (bulk copies).  Warps 0..3
 // each own 32 weight rows for every token tile and keep their accumulators in
 // registers across the whole reduction; two or three CTAs share an SM.
 // CTAs are persistent over 128-row sets (sets of 128 rows keep the last
@@ -186,8 +186,8 @@ __device__ __forceinline__ void decode_lane_bytes(uint32_t w, uint32_t &lo_a, ui
 // The lane's 8 Q8_0 code bytes 8c..8c+7 of one block of one row (lo: bytes
 // 0-3, hi: bytes 4-7) -> the row's A values of the block's two MMAs.  A
 // signed byte b becomes the fp16 pattern 0x6400 | (b ^ 0x80) = 1152 + b (one
-// logic instruction); the 1152 offset is taken out exactly by the
-// accumulator's correction.  First MMA: lo_a = elements (8c, 8c+2),
+// logic instruction); the 1152 offset is taken out exactly by the block's
+// correction.  First MMA: lo_a = elements (8c, 8c+2),
 // lo_b = (8c+1, 8c+3); second: hi_a = (8c+4, 8c+6), hi_b = (8c+5, 8c+7).
 __device__ __forceinline__ uint32_t q8_pair(uint32_t w) {
     return ((w ^ 0x00800080u) & 0x00FF00FFu) | 0x64006400u;
