@@ -907,3 +907,22 @@ def test_linear_pdl_chain_reads_the_previous_layer_output(qmm, orc, m):
         ok, worst, maxrel = rel_gate(outs[True][j + 1], orc.gemm_q4_0_q8_0(wq, wd, aq_r, ad_r),
                                      orc.gemm_q4_0_q8_0_absterms(wq, wd, aq_r, ad_r))
         assert ok, (j, worst, maxrel)
+
+
+@pytest.mark.parametrize("fmt", ["q4", "q8"])
+def test_gemm_few_token_shape_with_unaligned_scales_takes_the_tcgen05_product(qmm, orc, fmt):
+    """The few-token product copies dw with a tensor map (16-byte aligned
+    base); with dw 2 bytes off a 16-byte boundary the GEMM call runs the
+    tcgen05 product instead.  Both are the serial definition, bit for bit."""
+    m, n, k = 16, 300, 1024
+    if fmt == "q4":
+        w, wd, aq, ad = q4_case(orc, 8800, m, n, k)
+        ref, gemm = orc.gemm_q4_0_q8_0(w, wd, aq, ad), qmm.gemm_q4_0_q8_0
+    else:
+        w, wd, aq, ad = q8_case(orc, 8801, m, n, k)
+        ref, gemm = orc.gemm_q8_0_q8_0(w, wd, aq, ad), qmm.gemm_q8_0_q8_0
+    w_d, wd_d = to_dev(w), to_dev(wd.view(np.float16))
+    aq_d, ad_d = to_dev(aq), to_dev(ad.view(np.float16))
+    for scales in (wd_d, _misaligned_copy(wd_d)):
+        y = to_np(gemm(w_d, scales, aq_d, ad_d))
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
