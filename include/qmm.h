@@ -134,7 +134,11 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
  * except that there is no workspace: the split-K partials go to a device
  * array owned by the library, QMM_NOALLOC_SCRATCH_FLOATS floats (4 MiB)
  * reserved on every GPU that loads the library and held until the process
- * exits.  The call itself allocates nothing.
+ * exits.  The call itself allocates nothing.  It always runs the GEMV
+ * kernels, never the few-token product (whose activation layout would need
+ * a workspace), so at m >= 3 with split_k = 0 its bits can differ from
+ * those of qmm_gemv_q4_0_q8_0 given a workspace; both meet the same
+ * tolerance.
  *   - A split_k > 1 with split_k * m * n > QMM_NOALLOC_SCRATCH_FLOATS
  *     returns QMM_ERR_WORKSPACE and launches nothing.  The automatic split
  *     (split_k = 0) always fits: it exceeds 1 only for short grids (n below
