@@ -451,14 +451,29 @@ def run_layer_set(q, args, dist, peaks):
     torch.cuda.synchronize()
     e2e_s = dist.max(time.perf_counter() - t0)
     # the same calls as a token loop must run them: each step's outputs are
-    # in host memory (the stream synchronized) before the next step is issued
+    # in host memory (the stream synchronized) before the next step is issued;
+    # such a loop replays the step as a CUDA graph (GroupedLinear(graph=True):
+    # one launch per step), the eager form is reported beside it
     sync_steps = max(20, min(args.steps, 200))
-    dist.barrier()
-    t0 = time.perf_counter()
-    for i in range(sync_steps):
-        e2e_step(i)
-        torch.cuda.current_stream().synchronize()
-    sync_s = dist.max(time.perf_counter() - t0)
+    gcalls = [q.GroupedLinear([(x_d[k_off[j]:k_off[j + 1]].view(1, -1), *mt["wts"][c],
+                                y_d[n_off[j]:n_off[j + 1]].view(1, -1), mt["aq"], mt["ad"])
+                               for j, mt in enumerate(mats)], pdl=True,
+                              host_io=(x_h, x_d, y_d, y_h), host_direct=True, graph=True)
+              for c in range(rot)]
+    for i in range(max(3, rot)):
+        gcalls[i % rot]()  # first call of each: run and capture
+    torch.cuda.synchronize()
+
+    def sync_loop(fn):
+        dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(sync_steps):
+            fn(i)
+            torch.cuda.current_stream().synchronize()
+        return dist.max(time.perf_counter() - t0)
+
+    sync_s = sync_loop(lambda i: gcalls[i % rot]())
+    sync_eager_s = sync_loop(e2e_step)
     e2e = {"value": round(dist.world * step_bytes * e2e_steps / e2e_s / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": sum(4 * k for _, k in LAYER_SET),
            "d2h_bytes_per_step": sum(4 * n for n, _ in LAYER_SET),
@@ -467,8 +482,14 @@ def run_layer_set(q, args, dist, peaks):
            "synchronized": {"value": round(dist.world * step_bytes * sync_steps / sync_s / 1e9, 2),
                             "unit": "GB/s", "us_per_step": round(sync_s * 1e6 / sync_steps, 2),
                             "steps": sync_steps,
+                            "path": "GroupedLinear(..., host_direct=True, graph=True): the step "
+                                    "captured once and replayed as a CUDA graph",
                             "timing": "each step's outputs in host memory (stream synchronized) "
-                                      "before the next step is issued, as a token loop runs"}}
+                                      "before the next step is issued, as a token loop runs",
+                            "eager": {"value": round(dist.world * step_bytes * sync_steps /
+                                                     sync_eager_s / 1e9, 2),
+                                      "us_per_step": round(sync_eager_s * 1e6 / sync_steps, 2),
+                                      "path": "the same with one eager call per step"}}}
     return dict(value=value, ms=ms / args.steps, clocks=clocks, roofline=roofline, e2e=e2e, noise=noise,
                 launches=2 * args.steps, rot=rot, set_bytes=set_bytes,
                 step_bytes=step_bytes, variants=variants)

@@ -400,9 +400,21 @@ class GroupedLinear:
     the host tensors must then stay unchanged until the stream has passed
     the copies.  host_direct=True lets the kernels read x_host and write
     y_host themselves where the device can address them (page-locked memory
-    over NVLink-C2C), with no copy engine transfer; elsewhere it copies."""
+    over NVLink-C2C), with no copy engine transfer; elsewhere it copies.
 
-    def __init__(self, problems, pdl: bool = False, host_io=None, host_direct: bool = False):
+    graph=True suits a loop that waits for every call's outputs before the
+    next: the first call runs the layers and captures the same C call into a
+    CUDA graph, and every later call replays that graph on the current stream
+    (one launch instead of one per kernel: measured 29.5 against 36.1 us per
+    layer-set step with the outputs awaited each time).  Calls issued back to
+    back are faster without it, since consecutive graph launches do not
+    overlap the way dependent launches do.  The graph keeps the pointers of
+    the first call, which GroupedLinear fixes anyway; with host_io the host
+    tensors must be page-locked (a copy from pageable memory cannot be
+    captured)."""
+
+    def __init__(self, problems, pdl: bool = False, host_io=None, host_direct: bool = False,
+                 graph: bool = False):
         self._table, self._m, self.outputs = _grouped_table(problems)
         self._keep = [tuple(p) for p in problems]  # the tensors the table points at
         self._count = len(problems)
@@ -428,8 +440,26 @@ class GroupedLinear:
                           y_dev.data_ptr(), y_host.data_ptr(), yb)
             self._fn_host = load().qmm_linear_q4_0_grouped_host
             self._host_flags = self._flags | (LINEAR_HOST_DIRECT if host_direct else 0)
+            if graph and not (host_io[0].is_pinned() and host_io[3].is_pinned()):
+                raise ValueError("graph=True with host_io needs page-locked host tensors")
+        self._use_graph = graph
+        self._graph = None
 
     def __call__(self):
+        if not self._use_graph:
+            return self._run()
+        if self._graph is None:
+            torch = _torch()
+            self._run()  # this call's results; also any one-time set-up
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._run()
+            self._graph = g
+            return self.outputs
+        self._graph.replay()
+        return self.outputs
+
+    def _run(self):
         if self._host is not None:
             st = self._fn_host(self._addr, self._count, self._m, self._host_flags, *self._host,
                                _stream())

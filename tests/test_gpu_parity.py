@@ -803,10 +803,12 @@ def test_grouped_linear_with_host_buffers(qmm, orc):
               y_dev[n_off[j]:n_off[j + 1]].view(1, -1))
              for j, (_, _, wq, wd) in enumerate(mats)]
     assert qmm.host_addressable(x_host) and qmm.host_addressable(y_host)
-    for direct in (False, True):
+    # graph=True: the first call runs and captures, later calls replay the
+    # graph; each must pick up the new host input like the eager form
+    for direct, graph in ((False, False), (True, False), (False, True), (True, True)):
         call = qmm.GroupedLinear(probs, pdl=True, host_io=(x_host, x_dev, y_dev, y_host),
-                                 host_direct=direct)
-        for scale in (1.0, -0.5):
+                                 host_direct=direct, graph=graph)
+        for scale in (1.0, -0.5, 3.0):
             if scale != 1.0:
                 x_host.mul_(scale)
             y_host.fill_(np.nan)
@@ -816,7 +818,10 @@ def test_grouped_linear_with_host_buffers(qmm, orc):
                 [(x_host[k_off[j]:k_off[j + 1]].view(1, -1).cuda(), wq, wd)
                  for j, (_, _, wq, wd) in enumerate(mats)])
             for j, (y, _, _) in enumerate(plain):
-                assert torch.equal(y.cpu().ravel(), y_host[n_off[j]:n_off[j + 1]]), (direct, j)
+                assert torch.equal(y.cpu().ravel(), y_host[n_off[j]:n_off[j + 1]]), (direct, graph, j)
+    # a graph cannot capture copies from pageable memory: refused up front
+    with pytest.raises(ValueError):
+        qmm.GroupedLinear(probs, host_io=(x_host.clone(), x_dev, y_dev, y_host.clone()), graph=True)
     # direct mode checks that every x and y lies in the mirrored device buffers
     lib = qmm.load()
     outside = torch.zeros((1, shapes[0][1]), dtype=torch.float32, device="cuda")
