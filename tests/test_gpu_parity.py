@@ -931,3 +931,30 @@ def test_gemm_few_token_shape_with_unaligned_scales_takes_the_tcgen05_product(qm
     for scales in (wd_d, _misaligned_copy(wd_d)):
         y = to_np(gemm(w_d, scales, aq_d, ad_d))
         assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+def test_few_token_product_random_shapes_bit_exact(qmm, orc):
+    """Seeded random shapes for the few-token product (1 <= m <= 32, any n,
+    k a multiple of 256), both weight formats: y bit for bit the serial
+    definition, through the GEMM entries and, for 3 <= m <= 16, the GEMV
+    entries with split_k = 0."""
+    rng = np.random.default_rng(9100)
+    for case in range(12):
+        m = int(rng.integers(1, 33))
+        n = int(rng.integers(1, 3000))
+        k = 256 * int(rng.integers(1, 13))
+        fmt = "q4" if case % 2 == 0 else "q8"
+        if fmt == "q4":
+            w, wd, aq, ad = q4_case(orc, 9100 + case, m, n, k)
+            ref = orc.gemm_q4_0_q8_0(w, wd, aq, ad)
+            gemm, gemv = qmm.gemm_q4_0_q8_0, qmm.gemv_q4_0_q8_0
+        else:
+            w, wd, aq, ad = q8_case(orc, 9100 + case, m, n, k)
+            ref = orc.gemm_q8_0_q8_0(w, wd, aq, ad)
+            gemm, gemv = qmm.gemm_q8_0_q8_0, qmm.gemv_q8_0_q8_0
+        args = (to_dev(w), to_dev(wd.view(np.float16)), to_dev(aq), to_dev(ad.view(np.float16)))
+        y = to_np(gemm(*args))
+        assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), (fmt, m, n, k)
+        if 3 <= m <= 16:
+            y = to_np(gemv(*args))
+            assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), (fmt, m, n, k, "gemv")
