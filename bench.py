@@ -870,6 +870,86 @@ def _oracle_rate(mats, threads: int, budget_s: float, pin_core: int | None = Non
     return moved / el / 1e9, steps, el
 
 
+# ---------------------------------------------------------------------------
+# Result checksums and run identity
+
+FNV64_OFFSET = 0xCBF29CE484222325  # FNV-1a, 64-bit (Fowler, Noll, Vo)
+FNV64_PRIME = 0x100000001B3
+
+
+def fnv1a64(data: bytes) -> str:
+    h = FNV64_OFFSET
+    for byte in data:
+        h = ((h ^ byte) * FNV64_PRIME) & 0xFFFFFFFFFFFFFFFF
+    return f"0x{h:016x}"
+
+
+CHECK_ROWS, CHECK_N, CHECK_K = 512, 4096, 4096  # rows 0..511 of the 4096 x 4096 GEMV (seed 0)
+
+
+def _check_inputs():
+    from quantized_matmul_gb300 import synthetic
+    w, x = synthetic.q4_0_case(0, CHECK_N, CHECK_K, 1)
+    return np.ascontiguousarray(w[:CHECK_ROWS]), x
+
+
+def gpu_checksums(q):
+    """FNV-1a of integer results of the CUDA path on a fixed case: the Q8_0
+    codes of the 4096-element activation row (seed 0) and the GEMV's int32
+    block sums [1, 512, 128] against the first 512 rows of the 4096 x 4096
+    weights, both quantized on the GPU.  Integer results are exact, so any
+    machine (and the oracle) must give the same bytes."""
+    import torch
+    w, x = _check_inputs()
+    wq, _ = q.quantize_weight_q4_0(_up(w))
+    aq, _ = q.quantize_act_q8_0(_up(x))
+    sumi = q.debug_block_sums(0, wq, aq)
+    torch.cuda.synchronize()
+    return {"q8_0_codes": fnv1a64(aq.cpu().numpy().tobytes()),
+            "block_sums": fnv1a64(sumi.cpu().numpy().tobytes())}
+
+
+def oracle_checksums():
+    """The same two checksums from the oracle (CPU), quantizing the same f32
+    inputs itself."""
+    import oracle
+    w, x = _check_inputs()
+    wq, _ = oracle.quantize_q4_0(w)
+    aq, _ = oracle.quantize_q8_0(x)
+    return {"q8_0_codes": fnv1a64(np.ascontiguousarray(aq).tobytes()),
+            "block_sums": fnv1a64(np.ascontiguousarray(oracle.block_sums(wq, aq)).tobytes())}
+
+
+def run_identity():
+    """The source the run was built from: the git commit where the checkout
+    has one, else a SHA-256 over the native and Python sources."""
+    import hashlib
+    import subprocess
+    try:
+        sha = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                             text=True, timeout=10).stdout.strip()
+    except (OSError, subprocess.SubprocessError):
+        sha = ""
+    h = hashlib.sha256()
+    for sub in ("quantized_matmul_gb300/csrc", "quantized_matmul_gb300", "include", "oracle"):
+        d = os.path.join(ROOT, sub)
+        for name in sorted(os.listdir(d)):
+            if name.endswith((".cu", ".cuh", ".h", ".c", ".py")):
+                with open(os.path.join(d, name), "rb") as f:
+                    h.update(name.encode() + b"\0" + f.read())
+    out = {"source_sha256": h.hexdigest()}
+    if len(sha) == 40:
+        out["git_commit"] = sha
+    return out
+
+
+def gpu_identity():
+    import torch
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return {"name": p.name, "compute_capability": f"{p.major}.{p.minor}",
+            "sms": p.multi_processor_count, "memory_gib": round(p.total_memory / 2**30, 1)}
+
+
 def cpu_baseline(budget_s: float, frac: float = 0.25):
     """The oracle as it stands on the host cores: one core (pinned) and all
     host cores (rows split over threads), each the median of three runs of
@@ -885,7 +965,7 @@ def cpu_baseline(budget_s: float, frac: float = 0.25):
               f"scalar GEMV over the first {frac:.0%} of rows of every matrix; median of 3 runs "
               f"of ~{each:.1f} s each")
     return {"value": round(medn, 4), "unit": "GB/s", "cores": len(cores), "kind": "oracle",
-            "host_cores": len(cores),
+            "host_cores": len(cores), "checksums": oracle_checksums(),
             "sample": sample + f", rows split over {len(cores)} threads",
             "runs": [round(r[0], 4) for r in allc],
             "one_core": {"value": round(med1, 4), "unit": "GB/s", "cores": 1,
@@ -1016,6 +1096,15 @@ def main():
             configs["q8_0_vocab_4096x128256"] = run_q8_vocab(q, max(50, short // 20), 10, dist,
                                                              peaks, q8_vocab_m)
         cpu = cpu_baseline(args.cpu_budget) if dist.rank == 0 and args.cpu_budget > 0 else None
+        checks = None
+        if dist.rank == 0:
+            gpu_sums = gpu_checksums(q)
+            checks = {"case": f"Q4_0 GEMV {CHECK_N}x{CHECK_K} (seed 0), weight rows 0..{CHECK_ROWS - 1}, "
+                              f"m = 1: FNV-1a-64 of the Q8_0 codes and of the int32 block sums",
+                      "gpu": gpu_sums}
+            if cpu is not None:  # the oracle's own checksums come with its baseline
+                checks["oracle"] = cpu.pop("checksums")
+                checks["match"] = checks["oracle"] == gpu_sums
         if dist.rank == 0:
             line = {
                 "metric": METRIC, "value": round(main_res["value"], 1), "unit": "GB/s",
@@ -1048,6 +1137,9 @@ def main():
                                            "level MMA on every SM); int8 is the GPU's only int8 "
                                            "tensor path on sm_103a"},
                 "configs": configs,
+                "checks": checks,
+                "gpu": gpu_identity(),
+                "build": run_identity(),
             }
             print(json.dumps(line), flush=True)
     finally:

@@ -38,3 +38,7 @@ def test_bench_prints_one_contract_line():
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 2 * 40
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    # integer results of the CUDA path and of the oracle, checksummed alike
+    ck = d["checks"]
+    assert ck["match"] is True and ck["gpu"] == ck["oracle"], ck
+    assert d["gpu"]["sms"] > 0 and d["build"]["source_sha256"]

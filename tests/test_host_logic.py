@@ -70,3 +70,27 @@ def test_rotation_exceeds_twice_the_l2():
     for nbytes in (4_450_000, 9_460_000, 17_850_000, 113_840_000, 295_500_000):
         c = bench.copies_for(nbytes)
         assert (c - 1) * nbytes >= 2 * bench.L2_BYTES or c == 1 and nbytes >= 2 * bench.L2_BYTES
+
+
+def test_fnv1a64_published_vectors():
+    """The bench's result checksum is 64-bit FNV-1a: the published values for
+    the empty string, "a" and "foobar"."""
+    bench = _bench()
+    assert bench.fnv1a64(b"") == "0xcbf29ce484222325"
+    assert bench.fnv1a64(b"a") == "0xaf63dc4c8601ec8c"
+    assert bench.fnv1a64(b"foobar") == "0x85944171f73967e8"
+
+
+def test_oracle_checksums_are_stable():
+    """The oracle side of the bench's checksums is deterministic and covers
+    both integer results."""
+    bench = _bench()
+    a, b = bench.oracle_checksums(), bench.oracle_checksums()
+    assert a == b and set(a) == {"q8_0_codes", "block_sums"}
+    assert all(v.startswith("0x") and len(v) == 18 for v in a.values())
+
+
+def test_run_identity_hashes_the_sources():
+    bench = _bench()
+    ident = bench.run_identity()
+    assert len(ident["source_sha256"]) == 64
