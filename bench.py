@@ -256,6 +256,16 @@ class GraphTimer:
         if k % self.rot:
             self._tail(k % self.rot).replay()
 
+    def median(self, k: int, warmup: int, dist: Dist, repeats: int = 3):
+        """Times k steps `repeats` times (the first after `warmup` untimed
+        steps) and returns the median time with the spread: CV over the
+        repeats and NOISY when it passes 8%."""
+        runs = [self.time(k, warmup if r == 0 else 1, dist)[0] for r in range(repeats)]
+        mean = sum(runs) / len(runs)
+        cv = (sum((v - mean) ** 2 for v in runs) / len(runs)) ** 0.5 / mean
+        return statistics.median(runs), {"repeats": repeats, "cv": round(cv, 5),
+                                         "noisy": cv > 0.08}
+
     def time(self, k: int, warmup: int, dist: Dist, sampler: ClockSampler | None = None,
              settle_s: float = 0.6):
         """Times exactly k steps after `warmup` untimed ones.  With a clock
@@ -383,8 +393,8 @@ def run_layer_set(q, args, dist, peaks):
             ("chain_no_pdl", chain_step(False), "qmm_linear_q4_0 per matrix, no PDL"),
             ("quantize_then_gemv", two_kernel_step, "qmm_quantize_act_q8_0 + "
              "qmm_gemv_q4_0_q8_0 per matrix, plain launches")):
-        ms_v, _ = GraphTimer(fn, rot).time(args.steps, args.warmup, dist)
-        variants[name] = {"value": gbs(ms_v, step_bytes), "unit": "GB/s",
+        ms_v, noise_v = GraphTimer(fn, rot).median(args.steps, args.warmup, dist)
+        variants[name] = {"value": gbs(ms_v, step_bytes), "unit": "GB/s", "noise": noise_v,
                           "ms_per_step": round(ms_v / args.steps, 6), "path": what}
     # the step's dominant kernel is gemv_grouped_kernel (the quantizer moves
     # 0.3% of the bytes); with PDL the two launches overlap, so its time is
@@ -406,8 +416,8 @@ def run_layer_set(q, args, dist, peaks):
                             "launch, overlapped by PDL) per launch of the GEMV, CUDA events on "
                             "the replay stream"}
     # the GEMV kernel alone on pre-quantized activations, same 7 matrices
-    ms_g, _ = GraphTimer(gemv_only, rot).time(args.steps, args.warmup, dist)
-    variants["gemv_only_prequantized"] = {
+    ms_g, noise_g = GraphTimer(gemv_only, rot).median(args.steps, args.warmup, dist)
+    variants["gemv_only_prequantized"] = {"noise": noise_g,
         "value": gbs(ms_g, gemv_step_bytes), "unit": "GB/s",
         "bytes": "weights + Q8_0 activations + f32 y", "ms_per_step": round(ms_g / args.steps, 6)}
 
@@ -507,11 +517,11 @@ def run_single_gemv(q, steps, warmup, dist, peaks):
         wq, wd = wts[i % rot]
         q.gemv_q4_0_q8_0(wq, wd, aq, ad, y=y, split_k=1)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     gbs = dist.world * gemv_bytes(1, n, k) * steps / (ms * 1e-3) / 1e9
     return {"workload": "Q4_0xQ8_0 GEMV m=1 K=4096 N=4096 (seed 0)", "value": round(gbs, 1),
             "unit": "GB/s", "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot}
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise}
 
 
 def run_prefill_repacked(q, steps, warmup, dist, peaks):
@@ -530,7 +540,7 @@ def run_prefill_repacked(q, steps, warmup, dist, peaks):
         wr, wd = reps[i % rot]
         q.gemm_q4_0_q8_0_repacked(wr, wd, aq, ad, y=y, workspace=ws)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": "Q4_0xQ8_0 prefill GEMM m=512 K=4096 N=14336, 1% outliers x20 "
@@ -538,7 +548,7 @@ def run_prefill_repacked(q, steps, warmup, dist, peaks):
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             **int8_fraction(tops / dist.world, peaks),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,1>")}
 
 
@@ -569,13 +579,13 @@ def run_q8_gemv(q, steps, warmup, dist, peaks):
         w8, wd = wts[i % rot]
         q.gemv_q8_0_q8_0(w8, wd, aq, ad, y=y, split_k=1)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     nbytes = q8_weight_bytes(n, k) + k + 2 * (k // QK) + 4 * n
     gbs = dist.world * nbytes * steps / (ms * 1e-3) / 1e9
     return {"workload": "Q8_0xQ8_0 GEMV m=1 K=4096 N=4096 (seed 0; Q8_0 weights)",
             "value": round(gbs, 1), "unit": "GB/s",
             "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise,
             "traffic": recorded_traffic("gemv_q8_0_q8_0_kernel<1,2,0>"),
             "algorithmic_bytes_per_launch": nbytes}
 
@@ -594,7 +604,7 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
         w8, wd = wts[i % rot]
         q.gemm_q8_0_q8_0(w8, wd, aq, ad, y=y, workspace=ws)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": "Q8_0xQ8_0 prefill GEMM m=512 K=4096 N=14336, 1% outliers x20 "
@@ -602,7 +612,7 @@ def run_q8_prefill(q, steps, warmup, dist, peaks):
             "value": round(tops, 1), "unit": "TOPS (int ops, 2*m*n*k)",
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             **int8_fraction(tops / dist.world, peaks),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,64,0>")}
 
 
@@ -620,12 +630,12 @@ def run_q8_vocab(q, steps, warmup, dist, peaks, ms_list=(8, 16)):
         y = torch.empty((m, n), dtype=torch.float32, device="cuda")
         ws = torch.empty((q.workspace_bytes(q.OP_GEMM_Q8, m, n, k),), dtype=torch.uint8,
                          device="cuda")
-        ms, _ = GraphTimer(lambda i: q.gemm_q8_0_q8_0(w8, wd, aq, ad, y=y, workspace=ws),
-                           1).time(steps, warmup, dist)
+        ms, noise = GraphTimer(lambda i: q.gemm_q8_0_q8_0(w8, wd, aq, ad, y=y, workspace=ws),
+                               1).median(steps, warmup, dist)
         t = ms * 1e-3 / steps
         nbytes = q8_weight_bytes(n, k) + m * k + 2 * m * (k // QK) + 4 * m * n
         gb = dist.world * nbytes / t / 1e9
-        out["m"][str(m)] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1),
+        out["m"][str(m)] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1), "noise": noise,
                             "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
                             "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2),
                             "algorithmic_bytes_per_launch": nbytes}
@@ -659,8 +669,8 @@ def run_bitnet(q, steps, warmup, dist, peaks):
     def gemv(i):
         q.bitnet_gemv(tws[i % rot], absmean, aq, s, asum, y=y)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
-    ms_g, _ = GraphTimer(gemv, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
+    ms_g, _ = GraphTimer(gemv, rot).median(steps, warmup, dist)
     step_bytes = bitnet_step_bytes(1, n, k)
     gbs = dist.world * step_bytes * steps / (ms * 1e-3) / 1e9
     gbs_g = dist.world * bitnet_bytes(1, n, k) * steps / (ms_g * 1e-3) / 1e9
@@ -671,6 +681,7 @@ def run_bitnet(q, steps, warmup, dist, peaks):
             "frac_hbm": round(gbs / dist.world / peaks["hbm_gbs"], 4),
             "frac_hbm_nominal": round(gbs / dist.world / NOMINAL_HBM_GBS, 4),
             "us_per_step": round(ms * 1e3 / steps, 3), "algorithmic_bytes_per_step": step_bytes,
+            "noise": noise,
             "gpu_launches_per_step": 1, "weight_copies": rot,
             "traffic": recorded_traffic("bitnet_linear_m1_kernel<3,8,1>"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
@@ -697,7 +708,7 @@ def run_bitnet_prefill(q, steps, warmup, dist, peaks):
     def step(i):
         q.bitnet_gemm(tws[i % rot], absmean, aq, s, y=y, workspace=ws)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": "BitNet ternary prefill m=2048 K=2560 N=6912 (seed 3), tensor cores",
@@ -705,7 +716,7 @@ def run_bitnet_prefill(q, steps, warmup, dist, peaks):
             "frac_tensor": round(tops / dist.world / peak, 4), "peak": peak,
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): codes - 1 and "
                          "int8 activations run exactly on tcgen05 kind::f16",
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise,
             "traffic": recorded_traffic("bitnet_gemm_kernel"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
                             "(profiles/traffic.txt); algorithmic: 4.4 MB codes + 10.5 MB fp16 "
@@ -728,7 +739,7 @@ def run_prefill(q, steps, warmup, dist, peaks):
         a, d = acts[i % rot]
         q.gemm_q4_0_q8_0(wq, wd, a, d, y=y, workspace=ws)
 
-    ms, _ = GraphTimer(step, rot).time(steps, warmup, dist)
+    ms, noise = GraphTimer(step, rot).median(steps, warmup, dist)
     tops = dist.world * 2.0 * m * n * k * steps / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"workload": "Q4_0xQ8_0 prefill GEMM m=512 K=4096 N=14336, 1% outliers x20 (seed 11)",
@@ -737,7 +748,7 @@ def run_prefill(q, steps, warmup, dist, peaks):
             "peak_note": "dense fp16/bf16 tensor peak (measured bf16 burst): the block sums run "
                          "on tcgen05 kind::f16 because sm_103a has no tcgen05 int8 MMA",
             **int8_fraction(tops / dist.world, peaks),
-            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot,
+            "us_per_launch": round(ms * 1e3 / steps, 3), "weight_copies": rot, "noise": noise,
             "traffic": recorded_traffic("gemm_blocks_kernel<128,0,32,0>"),
             "traffic_note": "DRAM bytes of one launch from the recorded ncu capture "
                             "(profiles/traffic.txt); algorithmic: 33.0 MB weights + 2.1 MB "
@@ -777,10 +788,10 @@ def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
         if m <= 16:
             paths.insert(0, ("gemv", lambda i: q.gemv_q4_0_q8_0(wq, wd, aq, ad, y=y, split_k=1)))
         for name, fn in paths:
-            ms, _ = GraphTimer(fn, 1).time(steps, warmup, dist)
+            ms, noise = GraphTimer(fn, 1).median(steps, warmup, dist)
             t = ms * 1e-3 / steps
             gb = dist.world * gemv_bytes(m, n, k) / t / 1e9
-            res[name] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1),
+            res[name] = {"us": round(t * 1e6, 2), "GB/s": round(gb, 1), "noise": noise,
                          "frac_hbm": round(gb / dist.world / peaks["hbm_gbs"], 4),
                          "TOPS": round(dist.world * 2.0 * m * n * k / t / 1e12, 2)}
         if m == 16:
