@@ -768,7 +768,7 @@ def int8_fraction(tops_per_gpu: float, peaks) -> dict:
                               "SM (tcgen05.mma kind::i8 does not assemble for sm_103a)"}
 
 
-def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
+def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 64, 128)):
     import torch
     n, k = 128256, 4096
     wts, x = _quantized_weights(q, 13, n, k, 128, 1)
@@ -776,7 +776,7 @@ def run_vocab(q, steps, warmup, dist, peaks, ms_list=(1, 8, 16, 32, 128)):
     out = {"workload": "Q4_0xQ8_0 vocabulary projection K=4096 N=128256 (seed 13), "
                        "weights 295.5 MB > 2x L2", "m": {},
            "paths": "gemv: qmm_gemv_q4_0_q8_0 with split_k=1 (the dp4a GEMV kernels); gemm: "
-                    "qmm_gemm_q4_0_q8_0 (the few-token product for m <= 32, else tcgen05). "
+                    "qmm_gemm_q4_0_q8_0 (the few-token product for m <= 64, else tcgen05). "
                     "qmm_gemv_q4_0_q8_0 with split_k=0 takes the few-token product from m = 3 on"}
     for m in ms_list:
         aq, ad = q.quantize_act_q8_0(_up(x[:m]))
@@ -1044,7 +1044,7 @@ def main():
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
-    ap.add_argument("--vocab-m", default="1,8,16,32,128",
+    ap.add_argument("--vocab-m", default="1,8,16,32,64,128",
                     help="token counts of the vocabulary sweep (comma-separated, each <= 128)")
     ap.add_argument("--q8-vocab-m", default="8,16",
                     help="token counts of the Q8_0-weight vocabulary sweep (each <= 32)")

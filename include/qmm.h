@@ -250,7 +250,7 @@ int qmm_host_addressable(const void *host);
  * fma(sumi, dw*da, acc) over blocks in ascending order; the exact products
  * dw*da come from the tensor core too.  The workspace holds an fp16 copy of
  * the activations and one 16-byte activation-scale row per (block, token).
- * For a few tokens (m <= 32, k % 256 == 0, wd 16-byte aligned) the call runs
+ * For a few tokens (m <= 64, k % 256 == 0, wd 16-byte aligned) the call runs
  * a product on the warp-level tensor-core MMA instead (mma.sync, f16
  * operands, f32 accumulators in registers), with the same block sums and the
  * same bits of y; its workspace holds the activations as fp16 in the MMA's
@@ -443,7 +443,7 @@ qmm_status qmm_debug_mma_probe(int kind, int iters, int *out, size_t out_bytes, 
 
 /* Per-block sums sumi int32 [m, n, k/32] = sum_j (nibble_j - 8) * q_j.
  * path 0: the decode GEMV kernel (m <= QMM_GEMV_MAX_M); path 1: the GEMM
- * call (the few-token product for m <= 32 and k % 256 == 0, else the tensor-
+ * call (the few-token product for m <= 64 and k % 256 == 0, else the tensor-
  * core GEMM kernel; needs the GEMM workspace); path 2: the GEMM on repacked
  * weights (wq then points at the repacked tiles, see qmm_repack_q4_0_gemm).  Same alignment rules as the
  * product entry points; sumi 4-byte aligned. */

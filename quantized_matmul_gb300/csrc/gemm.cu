@@ -647,11 +647,11 @@ cudaError_t launch_tile(const CUtensorMap &nib, const CUtensorMap &act, const CU
 }  // namespace
 
 // Covers both products a GEMM call may launch (the few-token kernel of
-// gemm_small.cu for m <= 32, the tcgen05 kernel otherwise), either weight
-// format.
+// gemm_small.cu for m <= 64 with Q4_0 weights, m <= 32 with Q8_0, the
+// tcgen05 kernel otherwise), either weight format.
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
     const size_t t = plan_ws(m, k).total;
-    return gemm_small_m_supported(m, n, k) ? std::max(t, gemm_small_m_workspace_bytes(m, k)) : t;
+    return gemm_small_m_supported_q4(m, n, k) ? std::max(t, gemm_small_m_workspace_bytes(m, k)) : t;
 }
 
 void gemm_set_wait_limit(uint32_t iterations) { g_wait_limit = iterations ? iterations : kDefaultWaitLimit; }
@@ -736,7 +736,7 @@ cudaError_t launch_gemm_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
                                   int64_t n, int64_t k, void *workspace, cudaStream_t s) {
     // the few-token kernel copies dw with a tensor map, whose base must be
     // 16-byte aligned (the entry point only asks for 2)
-    if (gemm_small_m_supported(m, n, k) && (reinterpret_cast<uintptr_t>(wd) & 15) == 0)
+    if (gemm_small_m_supported_q4(m, n, k) && (reinterpret_cast<uintptr_t>(wd) & 15) == 0)
         return launch_gemm_small_m(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
     return launch_gemm<32, false>(wq, wd, aq, ad, y, sumi, m, n, k, workspace, s);
 }

@@ -1,6 +1,7 @@
-// Q4_0 x Q8_0 and Q8_0 x Q8_0 products for a few tokens (m <= 32): the
-// decode-batch and small-prefill shape, where the weights stream once and the
-// product should run at the speed of the weight read.
+// Q4_0 x Q8_0 and Q8_0 x Q8_0 products for a few tokens (m <= 64 with Q4_0
+// weights, m <= 32 with Q8_0): the decode-batch and small-prefill shape,
+// where the weights stream once and the product should run at the speed of
+// the weight read.
 //
 // What it computes is the GEMM's definition (llama.cpp visual guide, lesson
 // 31 "The CPU backend", section "How the quantized dot product works"): for
@@ -81,13 +82,14 @@ constexpr int kSmBlocks = 8;    // blocks per stage (256 k-elements)
 constexpr int kSmWarps = 4;     // consumer warps, 32 weight rows (two 16-row units) each
 // CTAs per SM and stages of each CTA's ring, per shape (WB: weight bytes per
 // row and block, 16 for Q4_0 nibbles, 32 for Q8_0 codes; MT, NT as for the
-// kernel).  Q4_0 with two 8-token tiles per 16-token tile (9..32 tokens) runs
-// three CTAs of two stages (vocabulary shape: 95.9 -> 92.4 us at 16 tokens,
-// 145.5 -> 138.5 us at 32, registers capped at 128); with one 8-token tile
-// three CTAs gain nothing, and Q8_0's stages are too large for three: those
-// run two CTAs, each within half the SM's shared memory.
+// kernel).  Q4_0 with two 8-token tiles per 16-token tile up to 32 tokens
+// runs three CTAs of two stages (vocabulary shape: 95.9 -> 92.4 us at 16
+// tokens, 145.5 -> 138.5 us at 32, registers capped at 128); with one
+// 8-token tile three CTAs gain nothing, and Q8_0's stages, and those of 33..64
+// tokens, are too large for three: those run two CTAs, each within half the
+// SM's shared memory.
 template <int WB, int MT, int NT>
-constexpr int sm_ctas() { return WB == 16 && NT == 2 ? 3 : 2; }
+constexpr int sm_ctas() { return WB == 16 && NT == 2 && MT <= 2 ? 3 : 2; }
 template <int WB, int MT, int NT>
 constexpr int sm_stages() {
     return WB == 32 ? 2 : NT == 2 ? 2 : 4;
@@ -612,6 +614,10 @@ bool gemm_small_m_supported(int64_t m, int64_t /*n*/, int64_t k) {
     return m >= 1 && m <= 32 && k % (kQK * kSmBlocks) == 0;
 }
 
+bool gemm_small_m_supported_q4(int64_t m, int64_t n, int64_t k) {
+    return gemm_small_m_supported(std::min<int64_t>(m, 32), n, k) && m <= 64;
+}
+
 // activation fragments, then the records, then the row-set counter, each
 // 256-byte aligned
 size_t gemm_small_m_workspace_bytes(int64_t m, int64_t k) {
@@ -689,6 +695,16 @@ cudaError_t launch_small(const void *w, const uint16_t *wd, const int8_t *aq, co
     if (mt == 1)
         return sumi ? launch_small_tile<WB, 1, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
                     : launch_small_tile<WB, 1, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
+    if constexpr (WB == 16) {
+        // 33..64 tokens, Q4_0 only (Q8_0 stages of that width would not fit
+        // two CTAs per SM)
+        if (mt == 3)
+            return sumi ? launch_small_tile<WB, 3, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
+                        : launch_small_tile<WB, 3, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
+        if (mt == 4)
+            return sumi ? launch_small_tile<WB, 4, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
+                        : launch_small_tile<WB, 4, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
+    }
     return sumi ? launch_small_tile<WB, 2, 2, true>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s)
                 : launch_small_tile<WB, 2, 2, false>(tw, tdw, afrag, dafrag, y, sumi, counter, m, n, k, s);
 }

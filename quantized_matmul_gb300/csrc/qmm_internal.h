@@ -139,11 +139,14 @@ cudaError_t launch_gemv_q8_0_q8_0(const int8_t *w8, const uint16_t *wd, const in
                                   int64_t n, int64_t k, int split, float *partials,
                                   cudaStream_t s);
 
-// gemm_small.cu: Q4_0 x Q8_0 product for m <= 32 and k % 256 == 0 on the
-// warp-level tensor-core MMA (accumulators in registers); launched by the
-// GEMM launcher for those shapes.  wd / ad may be null when sumi is given
-// (block-sum variant).
+// gemm_small.cu: Q4_0 x Q8_0 (m <= 64) and Q8_0 x Q8_0 (m <= 32) products
+// for k % 256 == 0 on the warp-level tensor-core MMA (accumulators in
+// registers); launched by the GEMM launchers for those shapes and by the
+// decode GEMV entries from three tokens on.  wd / ad may be null when sumi is
+// given (block-sum variant).
 bool gemm_small_m_supported(int64_t m, int64_t n, int64_t k);
+// Q4_0 weights also from 33 to 64 tokens
+bool gemm_small_m_supported_q4(int64_t m, int64_t n, int64_t k);
 size_t gemm_small_m_workspace_bytes(int64_t m, int64_t k);
 cudaError_t launch_gemm_small_m(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
                                 const uint16_t *ad, float *y, int32_t *sumi, int64_t m, int64_t n,

@@ -91,6 +91,12 @@ def test_workspace_queries(lib):
         assert lib.qmm_workspace_bytes(op, 16, 14336, k, 0) == frags + pairs + 256
         assert lib.qmm_workspace_bytes(op, 3, 14336, k, 1) == 0
         assert lib.qmm_workspace_bytes(op, 2, 14336, k, 0) == 0
+    # Q4_0 weights take the few-token product up to 64 tokens: the query
+    # covers its layout there too (three and four 16-token tiles)
+    for mm in (33, 48, 64):
+        mt = (mm + 15) // 16
+        small = (k // 32) * mt * 1024 + (k // 32) * mt * 128 + 256
+        assert lib.qmm_workspace_bytes(2, mm, 14336, k, 0) >= small
     k = 4064  # not a multiple of 256: the tcgen05 product only
     assert lib.qmm_workspace_bytes(2, m, 14336, k, 0) == (
         (m * k * 2 + 255) // 256 * 256 + ((k // 32) * 4 * 16 + 255) // 256 * 256)

@@ -157,10 +157,10 @@ def test_prefill_q8_0_weights_sampled_rows(qmm, orc):
 
 def test_vocab_128256x4096(qmm, orc):
     """Vocabulary projection K=4096, N=128256, seed 13, for m = 1, 8, 16, 32,
-    128 as the benchmark runs them: the m=1 GEMV on every output; for m=8 and
-    16 the GEMV and the GEMM (the few-token product), for m=32 the few-token
-    product and for m=128 the tcgen05 GEMM, on sampled weight rows (ends of
-    the range and of 128-row tiles)."""
+    64, 128 as the benchmark runs them: the m=1 GEMV on every output; for m=8
+    and 16 the GEMV and the GEMM (the few-token product), for m=32 and 64 the
+    few-token product and for m=128 the tcgen05 GEMM, on sampled weight rows
+    (ends of the range and of 128-row tiles)."""
     n, k = 128256, 4096
     w, x = synthetic.q4_0_case(13, n, k, 128)
     wq, wd = orc.quantize_q4_0(w)
@@ -172,7 +172,7 @@ def test_vocab_128256x4096(qmm, orc):
     _check_decode(y1, orc, wq, wd, np.ascontiguousarray(aq[:1]), np.ascontiguousarray(ad[:1]))
     cols = np.r_[0:130, 64000:64130, n - 130:n]
     wqs, wds = np.ascontiguousarray(wq[cols]), np.ascontiguousarray(wd[cols])
-    for m in (8, 16, 32, 128):
+    for m in (8, 16, 32, 64, 128):
         a, d = np.ascontiguousarray(aq[:m]), np.ascontiguousarray(ad[:m])
         ref = orc.gemm_q4_0_q8_0(wqs, wds, a, d)
         y_gemm = to_np(qmm.gemm_q4_0_q8_0(dwq, dwd, to_dev(a), f16(d)))

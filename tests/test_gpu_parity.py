@@ -175,7 +175,11 @@ def test_gemm_more_tiles_than_resident_ctas(qmm, orc, m, n, k):
 GEMM_SMALL_SHAPES = [(1, 1, 256), (8, 129, 512), (16, 128, 4096), (16, 257, 2048),
                      (17, 300, 768), (31, 1000, 1024), (32, 128 * 152 * 2 + 77, 256),
                      (20, 65, 11008), (8, 128 * 700 + 3, 256), (16, 128 * 1000 + 5, 512),
-                     (29, 128 * 600 + 127, 256)]
+                     (29, 128 * 600 + 127, 256),
+                     # three and four 16-token tiles (Q4_0 weights; Q8_0 takes the
+                     # tcgen05 product from 33 tokens on)
+                     (33, 300, 1024), (48, 1000, 512), (64, 257, 4096), (40, 129, 11008),
+                     (64, 128 * 600 + 5, 256)]
 
 
 @pytest.mark.parametrize("m,n,k", GEMM_SMALL_SHAPES)
