@@ -648,6 +648,38 @@ def run_q8_vocab(q, steps, warmup, dist, peaks, ms_list=(8, 16)):
     return out
 
 
+def run_bitnet_batch(q, steps, warmup, dist, peaks, ms_list=(4, 8, 16, 32)):
+    """BitNet 2560 -> 6912 (seed 3) for a few tokens on pre-quantized
+    activations: qmm_bitnet_gemm (the warp-level few-token product for
+    m <= 32) beside qmm_bitnet_gemv (m <= 16)."""
+    import torch
+    from quantized_matmul_gb300 import synthetic
+    n, k = 6912, 2560
+    t, x, absmean = synthetic.bitnet_case(3, n, k, max(ms_list))
+    rot = copies_for(n * k // 4)
+    tw = q.pack_ternary(_up(t))
+    tws = [tw] + [tw.clone() for _ in range(rot - 1)]
+    out = {"workload": "BitNet K=2560 N=6912 (seed 3), a few tokens, pre-quantized activations",
+           "weight_copies": rot, "m": {}}
+    for m in ms_list:
+        aq, sc, sm = q.quantize_act_bitnet(_up(x[:m]))
+        y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        ws = torch.empty((q.workspace_bytes(q.OP_BITNET_GEMM, m, n, k),), dtype=torch.uint8,
+                         device="cuda")
+        paths = [("gemm", lambda i: q.bitnet_gemm(tws[i % rot], absmean, aq, sc, y=y,
+                                                   workspace=ws))]
+        if m <= 16:
+            paths.append(("gemv", lambda i: q.bitnet_gemv(tws[i % rot], absmean, aq, sc, sm, y=y)))
+        res = {}
+        for name, fn in paths:
+            ms, noise = GraphTimer(fn, rot).median(steps, warmup, dist)
+            us = ms * 1e3 / steps
+            res[name] = {"us": round(us, 2), "TOPS": round(dist.world * 2.0 * m * n * k / us / 1e6, 2),
+                         "noise": noise}
+        out["m"][str(m)] = res
+    return out
+
+
 def run_bitnet(q, steps, warmup, dist, peaks):
     """The BitNet decode step: per-row activation quantization + ternary
     GEMV in one call (qmm_linear_bitnet with programmatic dependent launch;
@@ -1044,7 +1076,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline leg (0: skip it)")
     ap.add_argument("--only", choices=["gemv", "bitnet", "prefill", "vocab", "bitnet_prefill",
-                                       "q8_gemv", "q8_prefill", "q8_vocab", "prefill_repacked"],
+                                       "q8_gemv", "q8_prefill", "q8_vocab", "prefill_repacked",
+                                       "bitnet_batch"],
                     default=None,
                     help="profiling aid: run only this workload (steps as given) and print "
                          "its result; the headline contract line is not produced")
@@ -1086,6 +1119,7 @@ def main():
                    "q8_prefill": lambda: run_q8_prefill(q, args.steps, args.warmup, dist, peaks),
                    "q8_vocab": lambda: run_q8_vocab(q, args.steps, args.warmup, dist, peaks,
                                                     q8_vocab_m),
+                   "bitnet_batch": lambda: run_bitnet_batch(q, args.steps, args.warmup, dist, peaks),
                    "prefill_repacked": lambda: run_prefill_repacked(q, args.steps, args.warmup,
                                                                     dist, peaks)}
             res = run[args.only]()
@@ -1101,6 +1135,8 @@ def main():
             configs["prefill_512x14336x4096"] = run_prefill(q, max(50, short // 20), 10, dist, peaks)
             configs["bitnet_prefill_2048x6912x2560"] = run_bitnet_prefill(q, max(50, short // 20),
                                                                           10, dist, peaks)
+            configs["bitnet_batch_2560x6912"] = run_bitnet_batch(q, max(200, short // 4), 10, dist,
+                                                                 peaks)
             configs["vocab_4096x128256"] = run_vocab(q, max(50, short // 20), 10, dist, peaks,
                                                      vocab_m)
             configs["prefill_repacked_512x14336x4096"] = run_prefill_repacked(

@@ -386,7 +386,12 @@ qmm_status qmm_linear_bitnet(const uint32_t *w, float weight_absmean, const floa
  *               identity sum(code * q) - sum(q), so no act_sum is needed)
  *   y[i, r]   = act_scale[i] == 0 ? 0 : ((float)dot * weight_absmean) / act_scale[i]
  * Every operand is exact in fp16 and |dot| < 2^24, so the tensor core's f32
- * accumulation over all of k is exact.
+ * accumulation over all of k is exact.  For a few tokens (m <= 32) the call
+ * runs a product on the warp-level tensor-core MMA instead
+ * (mma.sync, codes as the fp16 values 1024 + code, exact per-group
+ * corrections, accumulators in registers, 64-row sets over the SMs): the
+ * same dots and the same bits of y; the workspace query covers its layout
+ * (activations in the MMA's fragment order, the corrections, a counter).
  *   w uint32 [n, k/16] 16-byte aligned; aq int8 [m, k] 16-byte aligned;
  *   act_scale f32 [m]; y f32 [m, n]; k % 64 == 0 and k <= 131072.
  *   workspace 256-byte aligned, at least
@@ -473,8 +478,9 @@ qmm_status qmm_debug_bitnet_dot(const uint32_t *w, const int8_t *aq, const int32
  * call. */
 void qmm_debug_set_wait_limit(uint32_t iterations);
 
-/* Test hook: while enabled, the GEMM kernel's load stage issues no copies,
- * so its pipeline waits can only run out their poll limit.  Tests use it
+/* Test hook: while enabled, the load stages of the GEMM kernel, of the
+ * few-token products (Q4_0, Q8_0 and BitNet) issue no copies, so their
+ * pipeline waits can only run out their poll limit.  Tests use it
  * with a small limit to check that the kernel then records QMM_ERR_TIMEOUT
  * (read by qmm_check_device_error), releases its resources and returns, and
  * that the device stays usable.  Outputs of such a call are unspecified. */

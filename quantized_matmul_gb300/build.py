@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libqmm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["qmm_api.cu", "quant.cu", "gemv.cu", "gemv_q8.cu", "gemv_stream.cu", "gemm.cu",
-           "gemm_small.cu", "bitnet_gemm.cu", "probe.cu"]
+           "gemm_small.cu", "bitnet_gemm.cu", "probe.cu", "bitnet_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", "-I" + INCLUDE]

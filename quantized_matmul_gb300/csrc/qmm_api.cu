@@ -93,6 +93,14 @@ bool few_token_route(int64_t m, int64_t n, int64_t k, int split_k, const void *w
            aligned(workspace, 256) && workspace_bytes >= qmm::gemm_small_m_workspace_bytes(m, k);
 }
 
+// Workspace of qmm_bitnet_gemm: enough for either product it may run.
+size_t bitnet_gemm_need(int64_t m, int64_t n, int64_t k) {
+    const size_t t = qmm::bitnet_gemm_workspace_bytes(m, k);
+    return qmm::bitnet_small_m_supported(m, n, k)
+               ? std::max(t, qmm::bitnet_small_m_workspace_bytes(m, k))
+               : t;
+}
+
 qmm_status check_linear(const uint8_t *wq, const uint16_t *wd, const float *x, int64_t ldx,
                         const int8_t *aq, const uint16_t *ad, const float *y, int64_t m,
                         int64_t n, int64_t k) {
@@ -442,18 +450,22 @@ qmm_status qmm_bitnet_gemm(const uint32_t *w, float weight_absmean, const int8_t
         return QMM_ERR_SHAPE;
     if (!aligned(w, 16) || !aligned(aq, 16) || !aligned(act_scale, 4) || !aligned(y, 4))
         return QMM_ERR_ALIGN;
-    const size_t need = qmm::bitnet_gemm_workspace_bytes(m, k);
+    const size_t need = bitnet_gemm_need(m, n, k);
     if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return QMM_ERR_ALIGN;
     if (qmm_status st = check_device()) return st;
+    // a few tokens: the warp-level MMA product (the tcgen05 tiles of 128 rows
+    // would leave most SMs idle); the same bits
+    if (qmm::bitnet_small_m_supported(m, n, k))
+        return launch_status(qmm::launch_bitnet_small_m(w, weight_absmean, aq, act_scale, y, m, n,
+                                                        k, workspace, as_stream(stream)));
     return launch_status(qmm::launch_bitnet_gemm(w, weight_absmean, aq, act_scale, y, m, n, k,
                                                  workspace, as_stream(stream)));
 }
 
 size_t qmm_workspace_bytes(int op, int64_t m, int64_t n, int64_t k, int split_k) {
     if (op == QMM_OP_BITNET_GEMM)
-        return (m <= 0 || n <= 0 || k <= 0 || k % 64 != 0) ? SIZE_MAX
-                                                           : qmm::bitnet_gemm_workspace_bytes(m, k);
+        return (m <= 0 || n <= 0 || k <= 0 || k % 64 != 0) ? SIZE_MAX : bitnet_gemm_need(m, n, k);
     if (m <= 0 || n <= 0 || k <= 0 || k % kQK != 0) return SIZE_MAX;
     switch (op) {
         case QMM_OP_GEMV_Q4_0_Q8_0:
@@ -481,7 +493,7 @@ int qmm_gemv_auto_split(int64_t m, int64_t n, int64_t k) {
 }
 
 qmm_status qmm_check_device_error(void *stream) {
-    unsigned int word = 0, word2 = 0, word3 = 0, word4 = 0;
+    unsigned int word = 0, word2 = 0, word3 = 0, word4 = 0, word5 = 0;
     if (qmm::gemm_read_and_clear_error(&word, as_stream(stream)) != cudaSuccess) return QMM_ERR_CUDA;
     if (qmm::gemm_small_read_and_clear_error(&word4, as_stream(stream)) != cudaSuccess)
         return QMM_ERR_CUDA;
@@ -489,7 +501,9 @@ qmm_status qmm_check_device_error(void *stream) {
         return QMM_ERR_CUDA;
     if (qmm::bitnet_gemm_read_and_clear_error(&word3, as_stream(stream)) != cudaSuccess)
         return QMM_ERR_CUDA;
-    return (word | word2 | word3 | word4) ? QMM_ERR_TIMEOUT : QMM_OK;
+    if (qmm::bitnet_small_read_and_clear_error(&word5, as_stream(stream)) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return (word | word2 | word3 | word4 | word5) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 const char *qmm_status_string(qmm_status status) {
@@ -600,9 +614,13 @@ void qmm_debug_set_wait_limit(uint32_t iterations) {
     qmm::gemm_small_set_wait_limit(iterations);
     qmm::stream_set_wait_limit(iterations);
     qmm::bitnet_gemm_set_wait_limit(iterations);
+    qmm::bitnet_small_set_wait_limit(iterations);
 }
 
-void qmm_debug_withhold_gemm_loads(int enable) { qmm::gemm_set_withhold_loads(enable); }
+void qmm_debug_withhold_gemm_loads(int enable) {
+    qmm::gemm_set_withhold_loads(enable);
+    qmm::bitnet_small_set_withhold_loads(enable);
+}
 
 void qmm_debug_withhold_gemv_loads(int enable) { qmm::stream_set_withhold_loads(enable); }
 

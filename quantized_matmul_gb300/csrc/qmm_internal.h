@@ -130,6 +130,18 @@ cudaError_t launch_bitnet_gemm(const uint32_t *w, float absmean, const int8_t *a
                                void *workspace, cudaStream_t s);
 void bitnet_gemm_set_wait_limit(uint32_t iterations);
 cudaError_t bitnet_gemm_read_and_clear_error(unsigned int *word, cudaStream_t s);
+// bitnet_small.cu: the BitNet product for a few tokens (m <= 32, k % 64 == 0,
+// k <= 131072) on the warp-level tensor-core MMA; launched by qmm_bitnet_gemm
+// for those shapes.  Its workspace holds the activations in the MMA's
+// fragment order, the per-group corrections and a row-set counter.
+bool bitnet_small_m_supported(int64_t m, int64_t n, int64_t k);
+size_t bitnet_small_m_workspace_bytes(int64_t m, int64_t k);
+cudaError_t launch_bitnet_small_m(const uint32_t *w, float absmean, const int8_t *aq,
+                                  const float *act_scale, float *y, int64_t m, int64_t n,
+                                  int64_t k, void *workspace, cudaStream_t s);
+void bitnet_small_set_wait_limit(uint32_t iterations);
+void bitnet_small_set_withhold_loads(int enable);
+cudaError_t bitnet_small_read_and_clear_error(unsigned int *word, cudaStream_t s);
 
 // gemv_q8.cu: Q8_0 weights (int8 [n, k] + fp16 scales [n, k/32]) x Q8_0
 // activations, m <= 16; same workspace rule as the Q4_0 GEMV; sumi != nullptr

@@ -962,3 +962,63 @@ def test_few_token_product_random_shapes_bit_exact(qmm, orc):
         if 3 <= m <= 16:
             y = to_np(gemv(*args))
             assert np.array_equal(y.view(np.uint32), ref.view(np.uint32)), (fmt, m, n, k, "gemv")
+
+
+# The BitNet product for a few tokens (qmm_bitnet_gemm with m <= 32:
+# warp-level MMAs over 64-row sets): one and two 8-token tiles, two 16-token
+# tiles, a ragged last stage (k not a multiple of 512), more row sets than
+# resident CTAs, the longest rows the entry takes (k = 131072).
+BITNET_SMALL_SHAPES = [(1, 1, 64), (2, 65, 576), (5, 6912, 2560), (8, 129, 1024),
+                       (9, 300, 4096), (16, 1000, 2560), (17, 64 * 152 * 2 + 7, 512),
+                       (32, 6912, 6912), (31, 100, 131072)]
+
+
+@pytest.mark.parametrize("m,n,k", BITNET_SMALL_SHAPES)
+def test_bitnet_small_m_bit_exact(qmm, orc, m, n, k):
+    tw, absmean, aq, scale, asum = _bitnet_operands(orc, 9300 + m + n, m, n, k)
+    y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), absmean, to_dev(aq), to_dev(scale)))
+    ref = orc.bitnet_gemv(tw, absmean, aq, scale, asum)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+def test_bitnet_small_m_extreme_activations_bit_exact(qmm, orc):
+    """Whole rows of the largest codes (+1) and of -1 against activations of
+    +127 and -127: the chained corrections at their largest magnitude, and
+    at the longest rows the entry takes the dots reach 127 k = 16,646,144,
+    just below 2^24."""
+    m, n, k = 8, 96, 131072
+    rng = np.random.default_rng(9400)
+    t = rng.integers(-1, 2, size=(n, k)).astype(np.int8)
+    t[:16] = 1
+    t[16:32] = -1
+    aq = rng.choice(np.array([-127, 127], dtype=np.int8), size=(m, k))
+    aq[:2] = 127
+    aq[2:4] = -127
+    scale = np.full(m, 0.25, dtype=np.float32)
+    asum = aq.astype(np.int64).sum(axis=1).astype(np.int32)
+    tw = orc.pack_ternary(t)
+    y = to_np(qmm.bitnet_gemm(to_dev(tw.view(np.int32)), 0.5, to_dev(aq), to_dev(scale)))
+    ref = orc.bitnet_gemv(tw, 0.5, aq, scale, asum)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+
+
+def test_bitnet_small_m_wait_timeout_reports_and_device_stays_usable(qmm, orc):
+    import torch
+    tw, absmean, aq, scale, asum = _bitnet_operands(orc, 9500, 16, 300, 1024)
+    args = (to_dev(tw.view(np.int32)), absmean, to_dev(aq), to_dev(scale))
+    assert qmm.check_device_error() == 0
+    try:
+        qmm.set_wait_limit(2000)
+        qmm.withhold_gemm_loads(True)
+        qmm.bitnet_gemm(*args)
+        torch.cuda.synchronize()
+        status = qmm.check_device_error()
+    finally:
+        qmm.withhold_gemm_loads(False)
+        qmm.set_wait_limit(0)
+    assert status == 7
+    y = to_np(qmm.bitnet_gemm(*args))
+    torch.cuda.synchronize()
+    assert qmm.check_device_error() == 0
+    ref = orc.bitnet_gemv(tw, absmean, aq, scale, asum)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
