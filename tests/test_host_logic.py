@@ -94,3 +94,16 @@ def test_run_identity_hashes_the_sources():
     bench = _bench()
     ident = bench.run_identity()
     assert len(ident["source_sha256"]) == 64
+
+
+def test_guarded_records_a_failing_measurement():
+    """A secondary config that raises is recorded in its place; the rest of
+    the line is still printed."""
+    bench = _bench()
+    assert bench.guarded(lambda: {"value": 1}) == {"value": 1}
+
+    def boom():
+        raise RuntimeError("no such kernel")
+
+    out = bench.guarded(boom)
+    assert out == {"error": "RuntimeError: no such kernel"}
