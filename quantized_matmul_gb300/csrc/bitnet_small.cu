@@ -250,10 +250,12 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        // B fragments of the group's 4 words for this 8-token tile
+                        // B fragments of the group's 4 words for this 8-token
+                        // tile: words 0-1 for all lanes, then words 2-3
+                        // (lane-contiguous 16 bytes, conflict-free)
                         const uint4 *bf = reinterpret_cast<const uint4 *>(
-                            at + ((q * MT + mt) * NT + nt) * 1024) + 2 * lane;
-                        const uint4 b01 = bf[0], b23 = bf[1];
+                            at + ((q * MT + mt) * NT + nt) * 1024);
+                        const uint4 b01 = bf[lane], b23 = bf[32 + lane];
                         const float2 cp = cor[(q * MT + mt) * 8 + nt * 4 + c];
                         // the group's dots, from its corrections; groups are
                         // independent chains, added to the running dots after
@@ -293,7 +295,8 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
 // ((group * mt_count + mt) * nt_count + nt) * 32 + lane covers token t = mt *
 // 16 + nt * 8 + g and group q (elements 64 q ..): for each of the group's 4
 // words j, the lane's registers (a[16j+2c], a[16j+2c+8]) and (a[16j+2c+1],
-// a[16j+2c+9]) as fp16 (exact: -127..127), 32 bytes.  The four lanes of a
+// a[16j+2c+9]) as fp16 (exact: -127..127): words 0-1 as 16 bytes at lane *
+// 16 of the unit's 1 KB, words 2-3 at 512 + lane * 16.  The four lanes of a
 // token hold all 64 of its group's activations, so their sum comes from two
 // shuffle steps; lane c = 0 writes cor = -1025 * sum as float (group *
 // mt_count + mt) * 16 + nt * 8 + g, so that the kernel reads tokens 2c, 2c+1
@@ -333,8 +336,8 @@ __global__ void bitnet_small_prep_kernel(const int8_t *__restrict__ aq, uint4 *_
             reg[2 * j] = *reinterpret_cast<const uint32_t *>(&lo);
             reg[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&hi);
         }
-        afrag[2 * u] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
-        afrag[2 * u + 1] = make_uint4(reg[4], reg[5], reg[6], reg[7]);
+        afrag[(u >> 5) * 64 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+        afrag[(u >> 5) * 64 + 32 + lane] = make_uint4(reg[4], reg[5], reg[6], reg[7]);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         if (c == 0) corrs[qm * 16 + nt * 8 + g] = (float)(-1025 * sum);
