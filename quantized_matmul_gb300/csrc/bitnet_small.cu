@@ -37,12 +37,17 @@
 // row: one tensor copy with 128-byte swizzle, so the 16-byte chunk q of row
 // r sits at chunk q ^ (r % 8) and the 8 rows a lane group reads fall in 8
 // bank groups) plus the stage's activation fragments and corrections (bulk
-// copies).  Four consumer warps own 16 rows each and keep their accumulators
-// in registers across k.  CTAs are persistent over 64-row sets: the first is
-// the block index, further ones come from a counter in the workspace (zeroed
-// by the prepass).  A last stage with row set -1 and no copies ends the
-// consumers.  The product is a programmatic dependent launch after the
-// prepass; every mbarrier wait is bounded.
+// copies).  Sixteen consumer warps in four quartets: warp w of quartet h
+// owns rows 16 w .. 16 w + 15 and groups 2 h, 2 h + 1 of every stage, and
+// keeps its partial dots in registers across k; at the end of a set
+// quartets 1-3 hand their partials to quartet 0 through shared memory, which
+// adds them (exact: integers below 2^24) and writes y.  Four warps per
+// sub-partition instead of one hide the MMA chains' and shared-memory loads'
+// latency, and each warp's work per stage is a quarter.  CTAs (one per SM) are persistent
+// over 64-row sets: the first is the block index, further ones come from a
+// counter in the workspace (zeroed by the prepass).  A last stage with row
+// set -1 and no copies ends the consumers.  The product is a programmatic
+// dependent launch after the prepass; every mbarrier wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -56,9 +61,11 @@ namespace qmm {
 namespace {
 
 constexpr int kBsRows = 64;         // weight rows per set (4 warps x one 16-row unit)
-constexpr int kBsWarps = 4;         // consumer warps
+constexpr int kBsQuartets = 4;      // consumer quartets, each on a quarter of a stage's groups
+constexpr int kBsWarps = 4 * kBsQuartets;  // consumer warps
 constexpr int kBsThreads = 32 * (kBsWarps + 1);
 constexpr int kBsGroups = 8;        // 64-element groups (16-byte chunks) per stage
+constexpr int kBsQGroups = kBsGroups / kBsQuartets;  // groups per quartet and stage
 constexpr int kBsStageElems = kBsGroups * 64;  // 512 elements, 128 bytes of codes per row
 
 __device__ unsigned int g_bitnet_small_error = 0;
@@ -70,15 +77,17 @@ struct BsPlan {
     static constexpr int kW = kBsRows * 128;                  // codes, 128-byte swizzle
     static constexpr int kA = kBsGroups * MT * NT * 1024;     // activation fragments
     static constexpr int kCor = kBsGroups * MT * 64;          // f32 corrections, 16 tokens
+    static constexpr int kPart = (kBsQuartets - 1) * 4 * MT * NT * 4 * 32 * 4;  // partial dots
     static constexpr int kOffW = 0;
     static constexpr int kOffA = kOffW + kStages * kW;
     static constexpr int kOffCor = kOffA + kStages * kA;
-    static constexpr int kOffBar = kOffCor + kStages * kCor;
-    static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+    static constexpr int kOffPart = kOffCor + kStages * kCor;
+    static constexpr int kOffBar = kOffPart + kPart;
+    static constexpr int kOffMisc = kOffBar + (2 * kStages + 8) * 8;
     static constexpr int kBytes = kOffMisc + 16 + 4 * kStages;  // abort flag, stage row sets
     static constexpr int kAlloc = kBytes + 1024;                 // slack for the 1024-byte round-up
     static_assert(kW % 1024 == 0 && kA % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
-    static_assert(2 * (kAlloc + 1024) <= 228 * 1024, "two CTAs fit one SM");
+    static_assert(kAlloc + 1024 <= 227 * 1024, "one CTA fits one SM");
 };
 
 __device__ __forceinline__ bool bs_wait(uint64_t *bar, uint32_t parity, uint32_t limit,
@@ -106,7 +115,7 @@ __device__ __forceinline__ uint4 decode_word_pair(uint32_t w0, uint32_t w1, int 
 }
 
 template <int MT, int NT>
-__global__ void __launch_bounds__(kBsThreads, 2)
+__global__ void __launch_bounds__(kBsThreads, 1)
 bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *__restrict__ afrag,
                       const uint8_t *__restrict__ corrs, const float *__restrict__ act_scale,
                       float absmean, float *__restrict__ y, unsigned int *set_counter, int m, int n,
@@ -117,6 +126,8 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar_full = reinterpret_cast<uint64_t *>(smem + P::kOffBar);
     uint64_t *bar_empty = bar_full + P::kStages;
+    uint64_t *bar_part = bar_empty + P::kStages;  // quartets 1.. have written a set's partials
+    uint64_t *bar_pfree = bar_part + 4;           // quartet 0 has read them
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::kOffMisc);
     int *stage_set = reinterpret_cast<int *>(smem + P::kOffMisc + 16);
 
@@ -128,6 +139,10 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
         for (int s = 0; s < P::kStages; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], kBsWarps);
+        }
+        for (int w = 0; w < 4; ++w) {
+            mbar_init(&bar_part[w], kBsQuartets - 1);
+            mbar_init(&bar_pfree[w], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -206,11 +221,16 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
     }
 
     // -------------------------------------------------------------------- consumers
-    // Warp w owns rows 16 w .. 16 w + 15 of every set (one MMA unit); lane
-    // (g, c) reads rows g and g + 8 of it, whose swizzle rows are both g.
+    // Warp w of quartet h owns rows 16 w .. 16 w + 15 of every set (one MMA
+    // unit) and groups 2 h, 2 h + 1 of every stage; lane (g, c) reads rows g
+    // and g + 8, whose swizzle rows are both g.
     const int g = lane >> 2, c = lane & 3;
+    const int quartet = warp >> 2, wq = warp & 3;
+    // partials of quartet h > 0 and warp w: MT * NT * 4 floats per lane, lane-contiguous
+    float *part = reinterpret_cast<float *>(smem + P::kOffPart) + wq * (MT * NT * 4 * 32) + lane;
+    constexpr int kPartStride = 4 * MT * NT * 4 * 32;  // floats per quartet
     float acc[MT][NT][4];
-    int it = 0;
+    int it = 0, sets = 0;
     bool ok = true;
     for (;;) {
         if (!bs_wait(&bar_full[it % P::kStages], (uint32_t)(it / P::kStages) & 1u, wait_limit,
@@ -233,11 +253,12 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
                 ok = false;
                 break;
             }
-            const uint8_t *wt = smem + P::kOffW + s * P::kW + (16 * warp + g) * 128;
+            const uint8_t *wt = smem + P::kOffW + s * P::kW + (16 * wq + g) * 128;
             const uint8_t *at = smem + P::kOffA + s * P::kA;
             const float2 *cor = reinterpret_cast<const float2 *>(smem + P::kOffCor + s * P::kCor);
-#pragma unroll 4
-            for (int q = 0; q < kBsGroups; ++q) {
+#pragma unroll
+            for (int qq = 0; qq < kBsQGroups; ++qq) {
+                const int q = quartet * kBsQGroups + qq;
                 // 4 packed words (64 elements) of rows g and g + 8
                 const uint4 w0 = *reinterpret_cast<const uint4 *>(wt + 16 * (q ^ g));
                 const uint4 w1 = *reinterpret_cast<const uint4 *>(wt + 8 * 128 + 16 * (q ^ g));
@@ -272,8 +293,39 @@ bitnet_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const uint8_t *_
             if (lane == 0) mbar_arrive(&bar_empty[s]);
         }
         if (!ok) break;
+        // quartets 1.. hand their partial dots to the warp of quartet 0 with
+        // the same rows (once that warp has read the previous set's), which
+        // adds them in quartet order and writes y
+        if (quartet > 0) {
+            if (sets > 0 && !bs_wait(&bar_pfree[wq], (uint32_t)(sets - 1) & 1u, wait_limit, abort_flag))
+                break;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        part[(quartet - 1) * kPartStride + ((mt * NT + nt) * 4 + i) * 32] = acc[mt][nt][i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_part[wq]);
+            ++sets;
+            continue;
+        }
+        if (!bs_wait(&bar_part[wq], (uint32_t)sets & 1u, wait_limit, abort_flag)) break;
+#pragma unroll
+        for (int h = 1; h < kBsQuartets; ++h)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        acc[mt][nt][i] += part[(h - 1) * kPartStride + ((mt * NT + nt) * 4 + i) * 32];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pfree[wq]);
+        ++sets;
         // y = ((float)dot * absmean) / scale, the ternary GEMV's rule
-        const int r0 = rs * kBsRows + 16 * warp + g;
+        const int r0 = rs * kBsRows + 16 * wq + g;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -368,8 +420,16 @@ cudaError_t launch_bs_tile(const CUtensorMap &tw, const uint8_t *afrag, const ui
     auto kern = bitnet_small_m_kernel<MT, NT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
+    // as many CTAs as fit at once (the first set of each is its index)
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int v = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kBsThreads, P::kAlloc);
+        if (e != cudaSuccess) return e;
+        per_sm = std::max(v, 1);
+    }
     const int64_t nsets = (n + kBsRows - 1) / kBsRows;
-    const int grid = (int)std::min<int64_t>(nsets, 2 * bs_num_sms());
+    const int grid = (int)std::min<int64_t>(nsets, (int64_t)per_sm * bs_num_sms());
     return launch_kernel(kern, dim3(grid), dim3(kBsThreads), P::kAlloc, s, true, tw, afrag, corrs,
                          scale, absmean, y, counter, (int)m, (int)n, nst, g_bs_wait_limit,
                          g_bs_withhold);
