@@ -725,7 +725,8 @@ def run_bitnet(q, steps, warmup, dist, peaks):
             "gemv_alone": {"value": round(gbs_g, 1), "unit": "GB/s",
                            "frac_hbm": round(gbs_g / dist.world / peaks["hbm_gbs"], 4),
                            "us_per_launch": round(ms_g * 1e3 / steps, 3),
-                           "algorithmic_bytes_per_launch": bitnet_bytes(1, n, k)}}
+                           "algorithmic_bytes_per_launch": bitnet_bytes(1, n, k),
+                           "traffic": recorded_traffic("bitnet_gemv_m1_kernel<1,8,0,0>")}}
 
 
 def run_bitnet_prefill(q, steps, warmup, dist, peaks):

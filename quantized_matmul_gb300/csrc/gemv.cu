@@ -383,6 +383,99 @@ bitnet_gemv_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *
     }
 }
 
+// The ternary GEMV for one token (m = 1, k % 64 == 0): the same dot and
+// output rule as bitnet_gemv_kernel, but the activation row is read from L2
+// once per CTA into shared memory, already transposed for the ternary dot
+// (word i, 16 elements, as the four ints t_s of ternary_dot16 at slot
+// [i % 4][i / 4], so that lanes reading consecutive 64-element chunks read
+// consecutive 16-byte slots), instead of once per warp: with one row per
+// warp the warps of a CTA share one copy.  The weight words are requested
+// before the row (and, with PDL, before the wait for the predecessor).
+template <int ROWS, int WARPS, bool EMIT, bool PDL>
+__global__ void __launch_bounds__(WARPS * 32, 6)
+bitnet_gemv_m1_kernel(const uint32_t *__restrict__ w, float absmean, const int8_t *__restrict__ aq,
+                      const float *__restrict__ scale, const int32_t *__restrict__ asum,
+                      float *__restrict__ y, int32_t *__restrict__ dot_out, int64_t n, int64_t k) {
+    extern __shared__ int4 act_t[];  // k / 16 slots
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t row0 = ((int64_t)blockIdx.x * WARPS + warp) * ROWS;
+    const int64_t kw = k / 16, kv = k / 64;
+    // two 64-element chunks per lane and row in flight: at 40 registers six
+    // 8-warp CTAs fit an SM, so the 864 CTAs of a 6912-row matrix run in one
+    // wave (four chunks: 48 registers, five CTAs, 4.15 against 3.35 us)
+    constexpr int kU = 2;
+    uint4 wv[kU][ROWS];
+    auto load_batch = [&](int64_t jj) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t j = jj + 32 * u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                wv[u][r] = (j < kv && row0 + r < n)
+                               ? ld_stream_v4(w + (row0 + r) * kw + j * 4)
+                               : make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+        }
+    };
+    load_batch(lane);
+    if (PDL) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    for (int64_t i = threadIdx.x; i < kw; i += WARPS * 32) {
+        const int4 a = __ldg(reinterpret_cast<const int4 *>(aq) + i);
+        int at[4];
+        transpose4x4(a.x, a.y, a.z, a.w, at);
+        act_t[(i & 3) * kv + (i >> 2)] = make_int4(at[0], at[1], at[2], at[3]);
+    }
+    __syncthreads();
+    if (row0 >= n) return;
+    int acc[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) acc[r] = 0;
+    for (int64_t jj = lane; jj < kv; jj += 32 * kU) {
+        if (jj != lane) load_batch(jj);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t j = jj + 32 * u;
+            if (j >= kv) break;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int4 t = act_t[q * kv + j];
+                const int at[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const uint32_t word = q == 0 ? wv[u][r].x
+                                        : q == 1 ? wv[u][r].y
+                                        : q == 2 ? wv[u][r].z
+                                                 : wv[u][r].w;
+                    acc[r] = ternary_dot16(word, at, acc[r]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        int v = acc[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[r] = v;
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            if (row0 + r >= n) break;
+            const int d = acc[r] - asum[0];
+            if (EMIT) {
+                dot_out[row0 + r] = d;
+            } else {
+                const float st = scale[0];
+                y[row0 + r] = st != 0.0f ? __fdiv_rn(__fmul_rn((float)d, absmean), st) : 0.0f;
+            }
+        }
+    }
+}
+
 // The BitNet decode step for one token (m = 1, k % 64 == 0) in one kernel.
 // Every CTA quantizes the activation row itself: the per-row scale needs
 // the whole row's maximum, and the row (k floats, read from L2) is small
@@ -642,7 +735,26 @@ cudaError_t launch_splitk_reduce(const float *partials, float *y, int64_t count,
 cudaError_t launch_bitnet_gemv(const uint32_t *w, float absmean, const int8_t *aq,
                                const float *scale, const int32_t *sum, float *y, int32_t *dot,
                                int64_t m, int64_t n, int64_t k, cudaStream_t s, bool pdl) {
-    // m = 1: four rows per warp (3.53 against 3.60 us for two at N=6912, K=2560)
+    // m = 1: the row staged once per CTA, one row per warp and 8 warps (at
+    // N=6912, K=2560: 3.35 us; rows x warps 2x8: 3.48, 1x16: 3.49, 4x4: 3.52,
+    // 2x2: 3.53, 1x4: 3.58, 4x2: 3.58, 2x4: 3.59, 4x8: 3.78, 2x16: 3.89; each
+    // warp reading the row from L2 itself, four rows per warp and 2 warps: 3.66)
+    if (m == 1 && k % 64 == 0 && k <= 32768) {
+        constexpr int kRows = 1, kW = 8;
+        const dim3 grid((unsigned)((n + kW * kRows - 1) / (kW * kRows)));
+        const size_t smem = (size_t)k;  // one byte per activation
+        if (dot) {
+            bitnet_gemv_m1_kernel<kRows, kW, true, false><<<grid, kW * 32, smem, s>>>(
+                w, absmean, aq, scale, sum, y, dot, n, k);
+            return cudaPeekAtLastError();
+        }
+        if (pdl)
+            return launch_kernel(bitnet_gemv_m1_kernel<kRows, kW, false, true>, grid, dim3(kW * 32),
+                                 smem, s, true, w, absmean, aq, scale, sum, y, dot, n, k);
+        bitnet_gemv_m1_kernel<kRows, kW, false, false><<<grid, kW * 32, smem, s>>>(
+            w, absmean, aq, scale, sum, y, dot, n, k);
+        return cudaPeekAtLastError();
+    }
     if (m == 1) return launch_bitnet<1, 4>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
     if (m == 2) return launch_bitnet<2, 2>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);
     if (m <= 4) return launch_bitnet<4, 1>(w, absmean, aq, scale, sum, y, dot, m, n, k, s, pdl);

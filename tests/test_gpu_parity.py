@@ -281,7 +281,11 @@ def test_gemm_and_gemv_agree_with_adversarial_activations(qmm, orc):
 # BitNet ternary
 
 BITNET_SHAPES = [(1, 1, 16), (1, 33, 48), (1, 6912, 2560), (2, 129, 2560), (3, 65, 160),
-                 (5, 100, 4096), (16, 31, 1024), (1, 40, 2576)]
+                 (5, 100, 4096), (16, 31, 1024), (1, 40, 2576),
+                 # one token with k % 64 == 0 and k <= 32768: the activation row
+                 # staged once per CTA (a ragged last CTA of 8 rows, the
+                 # largest k); past 32768 the per-warp form
+                 (1, 7, 64), (1, 300, 11008), (1, 1000, 32768), (1, 9, 32832)]
 
 
 @pytest.mark.parametrize("m,n,k", BITNET_SHAPES)
@@ -335,6 +339,34 @@ def test_linear_bitnet_bit_exact(qmm, orc, m, n, k, pdl):
     assert np.array_equal(to_np(aq), aq_ref)
     assert np.array_equal(to_np(sc).view(np.uint32), s_ref.view(np.uint32))
     assert np.array_equal(to_np(asum), asum_ref)
+    y_ref = orc.bitnet_gemv(tw_ref, absmean, aq_ref, s_ref, asum_ref)
+    assert np.array_equal(to_np(y).view(np.uint32), y_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_linear_bitnet_one_token_unaligned_row_bit_exact(qmm, orc, pdl):
+    """One token whose f32 row is not 16-byte aligned: the step runs as the
+    quantizer and then the one-token GEMV (with programmatic dependent
+    launch when asked), still bit for bit the oracle's."""
+    import torch
+    n, k = 1000, 2560
+    t, x, absmean = synthetic.bitnet_case(175, n, k, 1)
+    tw_ref = orc.pack_ternary(t)
+    aq_ref, s_ref, asum_ref = orc.quantize_act_bitnet(x)
+    tw = to_dev(tw_ref.view(np.int32))
+    xbuf = torch.full((k + 4,), 3.0e3, dtype=torch.float32, device="cuda")
+    xbuf[1:k + 1] = to_dev(x[0])
+    aq = torch.empty((1, k), dtype=torch.int8, device="cuda")
+    sc = torch.empty((1,), dtype=torch.float32, device="cuda")
+    asum = torch.empty((1,), dtype=torch.int32, device="cuda")
+    y = torch.full((1, n), float("nan"), dtype=torch.float32, device="cuda")
+    st = qmm.load().qmm_linear_bitnet(tw.data_ptr(), float(absmean), xbuf.data_ptr() + 4, k,
+                                      aq.data_ptr(), sc.data_ptr(), asum.data_ptr(), y.data_ptr(),
+                                      1, n, k, 1 if pdl else 0,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(aq), aq_ref)
     y_ref = orc.bitnet_gemv(tw_ref, absmean, aq_ref, s_ref, asum_ref)
     assert np.array_equal(to_np(y).view(np.uint32), y_ref.view(np.uint32))
 
