@@ -206,6 +206,166 @@ gemv_grouped_kernel(const __grid_constant__ LinearGroup tab) {
                                                   P.y, nullptr, tab.m, P.n, P.k, P.k / kQK, group, 0);
 }
 
+// One token (m = 1), the activation slice staged once per CTA.  At m = 1 a
+// row's int8 activations (k bytes) outweigh its weights (k/2 + k/16 bytes),
+// so warps that each read them from L2 (gemv_cta) move more bytes between
+// L2 and the SMs than the weight stream; here the CTA's threads read the
+// slice once into shared memory as one 48-byte record per block, {codes
+// 0-15, codes 16-31, {da as f32, -8 * (sum of the 32 codes), 0, 0}}, whose
+// 16-byte parts lanes reading consecutive blocks find in distinct banks.
+// The block sum, the scale product and the accumulation are gemv_cta's, in
+// the same lane order (lane l takes blocks l, l + 32, ...), so y has the
+// same bits.  The weight words of the first batch are requested before the
+// staging (and, with PDL, before the wait for the quantizer).  EMIT stores
+// the block sums instead (sumi [n, k/32]).
+template <int ROWS, bool PDL, int WARPS, bool EMIT = false>
+__device__ __forceinline__ void gemv_cta_m1_staged(const uint8_t *__restrict__ wq,
+                                                   const unsigned short *__restrict__ wd,
+                                                   const int8_t *__restrict__ aq,
+                                                   const unsigned short *__restrict__ ad,
+                                                   float *__restrict__ out,
+                                                   int32_t *__restrict__ sumi, int64_t n,
+                                                   int64_t k, int64_t kb_per_split,
+                                                   int64_t group, int64_t slice) {
+    extern __shared__ uint4 stg[];  // 3 x 16 bytes per block of the slice
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t kb = k / kQK;
+    const int64_t row0 = (group * WARPS + warp) * ROWS;
+    const int64_t kb0 = slice * kb_per_split;
+    const int64_t kb1 = min(kb, kb0 + kb_per_split);
+    const int64_t wrow = k / 2;
+    float acc[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) acc[r] = 0.0f;
+    uint4 wv[kUnroll][ROWS];
+    unsigned short dwv[kUnroll][ROWS];
+    auto load_batch = [&](int64_t bb) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t b = bb + 32 * u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const int64_t row = row0 + r;
+                if (b < kb1 && row < n) {
+                    wv[u][r] = ld_stream_v4(wq + row * wrow + b * 16);
+                    dwv[u][r] = EMIT ? (unsigned short)0 : __ldg(wd + row * kb + b);
+                } else {
+                    wv[u][r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                    dwv[u][r] = 0;
+                }
+            }
+        }
+    };
+    const int64_t first = kb0 + lane;
+    load_batch(first);
+    if (PDL) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    for (int64_t b = kb0 + threadIdx.x; b < kb1; b += WARPS * 32) {
+        const int4 a0 = __ldg(reinterpret_cast<const int4 *>(aq + b * kQK));
+        const int4 a1 = __ldg(reinterpret_cast<const int4 *>(aq + b * kQK + 16));
+        const float da = EMIT ? 0.0f : h2f(__ldg(ad + b));
+        int asum = dp4a_us(0x01010101u, a0.x, 0);
+        asum = dp4a_us(0x01010101u, a0.y, asum);
+        asum = dp4a_us(0x01010101u, a0.z, asum);
+        asum = dp4a_us(0x01010101u, a0.w, asum);
+        asum = dp4a_us(0x01010101u, a1.x, asum);
+        asum = dp4a_us(0x01010101u, a1.y, asum);
+        asum = dp4a_us(0x01010101u, a1.z, asum);
+        asum = dp4a_us(0x01010101u, a1.w, asum);
+        uint4 *rec = stg + 3 * (b - kb0);
+        rec[0] = make_uint4(a0.x, a0.y, a0.z, a0.w);
+        rec[1] = make_uint4(a1.x, a1.y, a1.z, a1.w);
+        rec[2] = make_uint4(__float_as_uint(da), (uint32_t)(-8 * asum), 0u, 0u);
+    }
+    __syncthreads();
+    if (row0 >= n) return;
+    for (int64_t bb = first; bb < kb1; bb += 32 * kUnroll) {
+        if (bb != first) load_batch(bb);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t b = bb + 32 * u;
+            if (b >= kb1) break;
+            const uint4 *rec = stg + 3 * (b - kb0);
+            const uint4 a0 = rec[0], a1 = rec[1], e = rec[2];
+            const float da = __uint_as_float(e.x);
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const uint4 w = wv[u][r];
+                int s = (int)e.y;
+                s = dp4a_us(w.x & 0x0F0F0F0Fu, (int)a0.x, s);
+                s = dp4a_us(w.y & 0x0F0F0F0Fu, (int)a0.y, s);
+                s = dp4a_us(w.z & 0x0F0F0F0Fu, (int)a0.z, s);
+                s = dp4a_us(w.w & 0x0F0F0F0Fu, (int)a0.w, s);
+                s = dp4a_us((w.x >> 4) & 0x0F0F0F0Fu, (int)a1.x, s);
+                s = dp4a_us((w.y >> 4) & 0x0F0F0F0Fu, (int)a1.y, s);
+                s = dp4a_us((w.z >> 4) & 0x0F0F0F0Fu, (int)a1.z, s);
+                s = dp4a_us((w.w >> 4) & 0x0F0F0F0Fu, (int)a1.w, s);
+                if (EMIT) {
+                    if (row0 + r < n) sumi[(row0 + r) * kb + b] = s;
+                } else {
+                    const float sc = __fmul_rn(h2f(dwv[u][r]), da);
+                    acc[r] = fmaf((float)s, sc, acc[r]);
+                }
+            }
+        }
+    }
+    if constexpr (!EMIT) {  // the emitting variant stores block sums only
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            float v = acc[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            acc[r] = v;
+        }
+        if (lane == 0) {
+            float *dst = out + slice * n;  // split slice (0 when unsplit)
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                if (row0 + r >= n) break;
+                dst[row0 + r] = acc[r];
+            }
+        }
+    }
+}
+
+// CTA shapes of the staged one-token GEMVs (rows per warp, warps per CTA).
+// Grouped (layer set): 2 x 4, 5477 GB/s against 5386 for the per-warp reads
+// (2 x 8: 5412, 4 x 4: 5344, 3 x 4: 5330, 4 x 8: 5166, 4 x 2: 5098, 2 x 2:
+// 4661, 1 x 8: 4560, 1 x 4: 4490, 1 x 16: 4187, 2 x 16: 3591).
+// Single matrix: each CTA stages the row once however few rows it has, so
+// the staging pays off with 8-row CTAs when there are many rows (vocabulary,
+// 128256 x 4096: 40.5 against 41.3 us per-warp, 52.5 with 4-row CTAs), and
+// 4-row CTAs are best for a few thousand rows (4096 x 4096: 3.69 against
+// 3.75 per-warp, 3.82 with 8-row CTAs).
+constexpr int kM1GroupRows = 2, kM1GroupWarps = 4;
+constexpr int kM1Warps = 4;
+constexpr int64_t kM1ManyRows = 16384;  // from here on 2 rows per warp, else 1
+
+template <int ROWS, bool PDL, int WARPS, bool EMIT>
+__global__ void __launch_bounds__(WARPS * 32)
+gemv_m1_staged_kernel(const uint8_t *__restrict__ wq, const unsigned short *__restrict__ wd,
+                      const int8_t *__restrict__ aq, const unsigned short *__restrict__ ad,
+                      float *__restrict__ out, int32_t *__restrict__ sumi, int64_t n, int64_t k,
+                      int64_t kb_per_split) {
+    gemv_cta_m1_staged<ROWS, PDL, WARPS, EMIT>(wq, wd, aq, ad, out, sumi, n, k, kb_per_split,
+                                               blockIdx.x, blockIdx.y);
+}
+
+template <int ROWS, bool PDL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+gemv_grouped_m1_staged_kernel(const __grid_constant__ LinearGroup tab) {
+    int p = 0;
+    while (p + 1 < tab.count && (int64_t)blockIdx.x >= tab.cta_end[p]) ++p;
+    const int64_t group = (int64_t)blockIdx.x - (p ? tab.cta_end[p - 1] : 0);
+    const LinearProblem &P = tab.p[p];
+    gemv_cta_m1_staged<ROWS, PDL, WARPS>(P.wq, reinterpret_cast<const unsigned short *>(P.wd), P.aq,
+                                         reinterpret_cast<const unsigned short *>(P.ad), P.y,
+                                         nullptr, P.n, P.k, P.k / kQK, group, 0);
+}
+
 // y[i] = sum over slices s = 0..S-1 of partials[s][i], in that order.
 template <bool PDL>
 __global__ void splitk_reduce_kernel(const float *__restrict__ partials, float *__restrict__ y,
@@ -651,9 +811,37 @@ cudaError_t launch_bitnet(const uint32_t *w, float absmean, const int8_t *aq, co
     return cudaPeekAtLastError();
 }
 
+template <int R>
+cudaError_t launch_m1_staged(const uint8_t *wq, const uint16_t *wd, const int8_t *aq,
+                             const uint16_t *ad, float *out, int32_t *sumi, int64_t n, int64_t k,
+                             int split, int64_t per, cudaStream_t s, bool pdl) {
+    constexpr int W = kM1Warps;
+    const dim3 grid((unsigned)((n + W * R - 1) / (W * R)), (unsigned)split);
+    const size_t smem = (size_t)per * 48;
+    const auto *wdp = reinterpret_cast<const unsigned short *>(wd);
+    const auto *adp = reinterpret_cast<const unsigned short *>(ad);
+    if (sumi) {
+        gemv_m1_staged_kernel<R, false, W, true><<<grid, W * 32, smem, s>>>(wq, wdp, aq, adp, out,
+                                                                            sumi, n, k, per);
+        return cudaPeekAtLastError();
+    }
+    if (pdl)
+        return launch_kernel(gemv_m1_staged_kernel<R, true, W, false>, grid, dim3(W * 32), smem, s,
+                             true, wq, wdp, aq, adp, out, sumi, n, k, per);
+    gemv_m1_staged_kernel<R, false, W, false><<<grid, W * 32, smem, s>>>(wq, wdp, aq, adp, out,
+                                                                         sumi, n, k, per);
+    return cudaPeekAtLastError();
+}
+
 template <int MT, int ROWS>
 cudaError_t launch_grouped(LinearGroup tab, bool pdl, cudaStream_t s) {
-    const int64_t rows_per_cta = (int64_t)kGroupedWarps * ROWS;
+    // m = 1: the staged form, while the longest row's records fit the 48 KB
+    // of shared memory a launch gets without opting in (k <= 32768)
+    int64_t kmax = 0;
+    for (int p = 0; p < tab.count; ++p) kmax = std::max(kmax, tab.p[p].k);
+    const bool staged = MT == 1 && kmax / kQK * 48 <= 48 * 1024;
+    const int64_t rows_per_cta =
+        staged ? (int64_t)kM1GroupWarps * kM1GroupRows : (int64_t)kGroupedWarps * ROWS;
     // Longest CTAs first: a CTA's time grows with its problem's k, and CTAs
     // start in index order, so the long ones must not form the last wave.
     // (The problems are independent; their order changes no result.)
@@ -663,6 +851,15 @@ cudaError_t launch_grouped(LinearGroup tab, bool pdl, cudaStream_t s) {
     for (int p = 0; p < tab.count; ++p) {
         total += (tab.p[p].n + rows_per_cta - 1) / rows_per_cta;
         tab.cta_end[p] = total;
+    }
+    if (staged) {
+        const size_t smem = (size_t)(kmax / kQK) * 48;
+        constexpr int R = kM1GroupRows, W = kM1GroupWarps;
+        if (pdl)
+            return launch_kernel(gemv_grouped_m1_staged_kernel<R, true, W>, dim3((unsigned)total),
+                                 dim3(W * 32), smem, s, true, tab);
+        gemv_grouped_m1_staged_kernel<R, false, W><<<(unsigned)total, W * 32, smem, s>>>(tab);
+        return cudaPeekAtLastError();
     }
     if (pdl)
         return launch_kernel(gemv_grouped_kernel<MT, ROWS, true>, dim3((unsigned)total),
@@ -708,7 +905,12 @@ cudaError_t launch_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd, const i
     }
     float *out = split > 1 ? partials : y;
     cudaError_t e;
-    if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
+    const int64_t per = (k / kQK + split - 1) / split;  // blocks per slice
+    if (m == 1 && per * 48 <= 48 * 1024) {
+        // one token: the staged form (also for the block sums)
+        e = n >= kM1ManyRows ? launch_m1_staged<2>(wq, wd, aq, ad, out, sumi, n, k, split, per, s, pdl)
+                             : launch_m1_staged<1>(wq, wd, aq, ad, out, sumi, n, k, split, per, s, pdl);
+    } else if (m == 1) e = launch_q4<1, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
     else if (m == 2) e = launch_q4<2, 2>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
     else if (m <= 4) e = launch_q4<4, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);
     else if (m <= 8) e = launch_q4<8, 1>(wq, wd, aq, ad, out, sumi, m, n, k, split, s, pdl);

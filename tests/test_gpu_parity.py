@@ -85,7 +85,11 @@ def test_quantize_weight_q4_0_bit_exact(qmm, orc, n, k):
 
 GEMV_SHAPES = [(1, 1, 32), (1, 31, 64), (1, 33, 4064), (1, 129, 4096), (2, 127, 4096),
                (3, 32, 96), (4, 128, 4096), (7, 65, 1024), (8, 17, 4096), (15, 33, 512),
-               (16, 129, 4096), (1, 4097, 256)]
+               (16, 129, 4096), (1, 4097, 256),
+               # one token: the staged form with 8-row CTAs (many rows, ragged
+               # last CTA), the largest staged slice (k = 32768), and past it
+               # the per-warp form unless the reduction is split
+               (1, 16384 + 5, 256), (1, 9, 32768), (1, 40, 32768 + 64)]
 
 
 @pytest.mark.parametrize("m,n,k", GEMV_SHAPES)
@@ -757,12 +761,15 @@ def test_linear_matches_separate_calls_and_oracle(qmm, orc, m, n, k, pdl):
 
 
 # at m >= 8 the first set streams through shared memory; the second (k/32
-# not a multiple of 8 in some problems) always streams through registers
+# not a multiple of 8 in some problems) always streams through registers; at
+# m = 1 the third (a row longer than 32768) takes the per-warp form, the
+# others stage each CTA's activation row in shared memory
 GROUP_SHAPE_SETS = {
     "streaming": [(129, 1024), (300, 2048), (1, 256), (4096, 1024), (40, 2048),
                   (1100, 512), (17, 512)],
     "register": [(129, 4096), (300, 11008), (65, 4064), (1, 32), (4096, 4096), (40, 96),
                  (11008, 4096)],
+    "long": [(40, 32768 + 64), (300, 4096), (7, 32768)],
 }
 
 

@@ -60,7 +60,7 @@ def test_committed_traffic_records_are_well_formed():
     for kernel, nbytes, sha, path in (l[:4] for l in lines):
         assert os.path.exists(os.path.join(ROOT, path)), path
         assert int(nbytes) > 0 and len(sha) == 64
-    assert "gemv_grouped_kernel<1,4,1>" in [l[0] for l in lines]
+    assert _bench().HEADLINE_KERNEL in [l[0] for l in lines]
 
 
 def test_rotation_exceeds_twice_the_l2():
