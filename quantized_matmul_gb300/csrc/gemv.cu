@@ -342,6 +342,13 @@ __device__ __forceinline__ void gemv_cta_m1_staged(const uint8_t *__restrict__ w
 // 3.75 per-warp, 3.82 with 8-row CTAs).
 constexpr int kM1GroupRows = 2, kM1GroupWarps = 4;
 constexpr int kM1Warps = 4;
+// The grouped kernel's registers are capped so that six 4-warp CTAs fit an
+// SM (80 registers, no spills; left free, the 2-row form took 96 and five
+// CTAs): more weight bytes in flight per SM. Layer set: 5619 against 5437
+// GB/s; seven CTAs (72 registers, spills) 5342, eight (64) 4285.  The same
+// cap on the single-matrix kernel let its 1-row form grow from 56 to 79
+// registers, and 4096 x 4096 took two waves: 4.22 against 3.70 us.
+constexpr int kM1CtasPerSm = 6;
 constexpr int64_t kM1ManyRows = 16384;  // from here on 2 rows per warp, else 1
 
 template <int ROWS, bool PDL, int WARPS, bool EMIT>
@@ -355,7 +362,7 @@ gemv_m1_staged_kernel(const uint8_t *__restrict__ wq, const unsigned short *__re
 }
 
 template <int ROWS, bool PDL, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, kM1CtasPerSm)
 gemv_grouped_m1_staged_kernel(const __grid_constant__ LinearGroup tab) {
     int p = 0;
     while (p + 1 < tab.count && (int64_t)blockIdx.x >= tab.cta_end[p]) ++p;
