@@ -59,8 +59,62 @@ __device__ __forceinline__ float h2f(unsigned short h) {
     return __half2float(__ushort_as_half(h));
 }
 
+// Sum of a block's 32 int8 activation codes (a0: codes 0-15, a1: 16-31).
+__device__ __forceinline__ int block_code_sum(const int4 &a0, const int4 &a1) {
+    int s = dp4a_us(0x01010101u, a0.x, 0);
+    s = dp4a_us(0x01010101u, a0.y, s);
+    s = dp4a_us(0x01010101u, a0.z, s);
+    s = dp4a_us(0x01010101u, a0.w, s);
+    s = dp4a_us(0x01010101u, a1.x, s);
+    s = dp4a_us(0x01010101u, a1.y, s);
+    s = dp4a_us(0x01010101u, a1.z, s);
+    return dp4a_us(0x01010101u, a1.w, s);
+}
+
+// s + the dot of a Q4_0 block's raw nibbles (16 bytes: element j in the low
+// nibble of byte j, element j + 16 in its high nibble) with its activation
+// codes; with s = -8 * block_code_sum this is the block sum of (v - 8) * q.
+__device__ __forceinline__ int q4_block_dot(const uint4 &w, const int4 &a0, const int4 &a1, int s) {
+    s = dp4a_us(w.x & 0x0F0F0F0Fu, a0.x, s);
+    s = dp4a_us(w.y & 0x0F0F0F0Fu, a0.y, s);
+    s = dp4a_us(w.z & 0x0F0F0F0Fu, a0.z, s);
+    s = dp4a_us(w.w & 0x0F0F0F0Fu, a0.w, s);
+    s = dp4a_us((w.x >> 4) & 0x0F0F0F0Fu, a1.x, s);
+    s = dp4a_us((w.y >> 4) & 0x0F0F0F0Fu, a1.y, s);
+    s = dp4a_us((w.z >> 4) & 0x0F0F0F0Fu, a1.z, s);
+    return dp4a_us((w.w >> 4) & 0x0F0F0F0Fu, a1.w, s);
+}
+
 // ---------------------------------------------------------------------------
 // Q4_0 x Q8_0
+
+// The weight blocks bb + 32 u (u < kUnroll) of rows row0 .. row0 + ROWS - 1,
+// up to block kb1: nibbles with streaming 16-byte loads, scales through the
+// read-only path (none when emitting block sums).  Blocks past the end read
+// as nibbles 8 (value 0) with scale 0.
+template <int ROWS, bool EMIT>
+__device__ __forceinline__ void load_q4_batch(uint4 (&wv)[kUnroll][ROWS],
+                                              unsigned short (&dwv)[kUnroll][ROWS],
+                                              const uint8_t *__restrict__ wq,
+                                              const unsigned short *__restrict__ wd, int64_t row0,
+                                              int64_t n, int64_t kb, int64_t kb1, int64_t bb) {
+    const int64_t wrow = kb * 16;  // bytes per weight row
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t b = bb + 32 * u;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const int64_t row = row0 + r;
+            if (b < kb1 && row < n) {
+                wv[u][r] = ld_stream_v4(wq + row * wrow + b * 16);
+                dwv[u][r] = EMIT ? (unsigned short)0 : __ldg(wd + row * kb + b);
+            } else {
+                wv[u][r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                dwv[u][r] = 0;
+            }
+        }
+    }
+}
 
 // One CTA's share of the GEMV: row group `group` (WARPS * ROWS rows), k
 // slice `slice`.  PDL: the warp loads its first batch of weight blocks and
@@ -82,7 +136,6 @@ __device__ __forceinline__ void gemv_cta(const uint8_t *__restrict__ wq,
     if (row0 >= n) return;
     const int64_t kb0 = slice * kb_per_split;
     const int64_t kb1 = min(kb, kb0 + kb_per_split);
-    const int64_t wrow = k / 2;  // bytes per weight row
 
     float acc[ROWS][MT];
 #pragma unroll
@@ -93,21 +146,7 @@ __device__ __forceinline__ void gemv_cta(const uint8_t *__restrict__ wq,
     uint4 wv[kUnroll][ROWS];
     unsigned short dwv[kUnroll][ROWS];
     auto load_batch = [&](int64_t bb) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t b = bb + 32 * u;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const int64_t row = row0 + r;
-                if (b < kb1 && row < n) {
-                    wv[u][r] = ld_stream_v4(wq + row * wrow + b * 16);
-                    dwv[u][r] = EMIT ? (unsigned short)0 : __ldg(wd + row * kb + b);  // no scales when emitting
-                } else {
-                    wv[u][r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                    dwv[u][r] = 0;
-                }
-            }
-        }
+        load_q4_batch<ROWS, EMIT>(wv, dwv, wq, wd, row0, n, kb, kb1, bb);
     };
     const int64_t first = kb0 + lane;
     if (PDL) {
@@ -127,26 +166,10 @@ __device__ __forceinline__ void gemv_cta(const uint8_t *__restrict__ wq,
                 const int4 a0 = __ldg(reinterpret_cast<const int4 *>(aq + t * k + b * kQK));
                 const int4 a1 = __ldg(reinterpret_cast<const int4 *>(aq + t * k + b * kQK + 16));
                 const float da = EMIT ? 0.0f : h2f(__ldg(ad + t * kb + b));
-                int asum = dp4a_us(0x01010101u, a0.x, 0);
-                asum = dp4a_us(0x01010101u, a0.y, asum);
-                asum = dp4a_us(0x01010101u, a0.z, asum);
-                asum = dp4a_us(0x01010101u, a0.w, asum);
-                asum = dp4a_us(0x01010101u, a1.x, asum);
-                asum = dp4a_us(0x01010101u, a1.y, asum);
-                asum = dp4a_us(0x01010101u, a1.z, asum);
-                asum = dp4a_us(0x01010101u, a1.w, asum);
+                const int asum = block_code_sum(a0, a1);
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const uint4 w = wv[u][r];
-                    int s = -8 * asum;
-                    s = dp4a_us(w.x & 0x0F0F0F0Fu, a0.x, s);
-                    s = dp4a_us(w.y & 0x0F0F0F0Fu, a0.y, s);
-                    s = dp4a_us(w.z & 0x0F0F0F0Fu, a0.z, s);
-                    s = dp4a_us(w.w & 0x0F0F0F0Fu, a0.w, s);
-                    s = dp4a_us((w.x >> 4) & 0x0F0F0F0Fu, a1.x, s);
-                    s = dp4a_us((w.y >> 4) & 0x0F0F0F0Fu, a1.y, s);
-                    s = dp4a_us((w.z >> 4) & 0x0F0F0F0Fu, a1.z, s);
-                    s = dp4a_us((w.w >> 4) & 0x0F0F0F0Fu, a1.w, s);
+                    const int s = q4_block_dot(wv[u][r], a0, a1, -8 * asum);
                     if (EMIT) {
                         if (row0 + r < n) sumi[((int64_t)t * n + row0 + r) * kb + b] = s;
                     } else {
@@ -234,28 +257,13 @@ __device__ __forceinline__ void gemv_cta_m1_staged(const uint8_t *__restrict__ w
     const int64_t row0 = (group * WARPS + warp) * ROWS;
     const int64_t kb0 = slice * kb_per_split;
     const int64_t kb1 = min(kb, kb0 + kb_per_split);
-    const int64_t wrow = k / 2;
     float acc[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) acc[r] = 0.0f;
     uint4 wv[kUnroll][ROWS];
     unsigned short dwv[kUnroll][ROWS];
     auto load_batch = [&](int64_t bb) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t b = bb + 32 * u;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) {
-                const int64_t row = row0 + r;
-                if (b < kb1 && row < n) {
-                    wv[u][r] = ld_stream_v4(wq + row * wrow + b * 16);
-                    dwv[u][r] = EMIT ? (unsigned short)0 : __ldg(wd + row * kb + b);
-                } else {
-                    wv[u][r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                    dwv[u][r] = 0;
-                }
-            }
-        }
+        load_q4_batch<ROWS, EMIT>(wv, dwv, wq, wd, row0, n, kb, kb1, bb);
     };
     const int64_t first = kb0 + lane;
     load_batch(first);
@@ -267,14 +275,7 @@ __device__ __forceinline__ void gemv_cta_m1_staged(const uint8_t *__restrict__ w
         const int4 a0 = __ldg(reinterpret_cast<const int4 *>(aq + b * kQK));
         const int4 a1 = __ldg(reinterpret_cast<const int4 *>(aq + b * kQK + 16));
         const float da = EMIT ? 0.0f : h2f(__ldg(ad + b));
-        int asum = dp4a_us(0x01010101u, a0.x, 0);
-        asum = dp4a_us(0x01010101u, a0.y, asum);
-        asum = dp4a_us(0x01010101u, a0.z, asum);
-        asum = dp4a_us(0x01010101u, a0.w, asum);
-        asum = dp4a_us(0x01010101u, a1.x, asum);
-        asum = dp4a_us(0x01010101u, a1.y, asum);
-        asum = dp4a_us(0x01010101u, a1.z, asum);
-        asum = dp4a_us(0x01010101u, a1.w, asum);
+        const int asum = block_code_sum(a0, a1);
         uint4 *rec = stg + 3 * (b - kb0);
         rec[0] = make_uint4(a0.x, a0.y, a0.z, a0.w);
         rec[1] = make_uint4(a1.x, a1.y, a1.z, a1.w);
@@ -289,20 +290,13 @@ __device__ __forceinline__ void gemv_cta_m1_staged(const uint8_t *__restrict__ w
             const int64_t b = bb + 32 * u;
             if (b >= kb1) break;
             const uint4 *rec = stg + 3 * (b - kb0);
-            const uint4 a0 = rec[0], a1 = rec[1], e = rec[2];
+            const uint4 r0 = rec[0], r1 = rec[1], e = rec[2];
+            const int4 a0 = make_int4((int)r0.x, (int)r0.y, (int)r0.z, (int)r0.w);
+            const int4 a1 = make_int4((int)r1.x, (int)r1.y, (int)r1.z, (int)r1.w);
             const float da = __uint_as_float(e.x);
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const uint4 w = wv[u][r];
-                int s = (int)e.y;
-                s = dp4a_us(w.x & 0x0F0F0F0Fu, (int)a0.x, s);
-                s = dp4a_us(w.y & 0x0F0F0F0Fu, (int)a0.y, s);
-                s = dp4a_us(w.z & 0x0F0F0F0Fu, (int)a0.z, s);
-                s = dp4a_us(w.w & 0x0F0F0F0Fu, (int)a0.w, s);
-                s = dp4a_us((w.x >> 4) & 0x0F0F0F0Fu, (int)a1.x, s);
-                s = dp4a_us((w.y >> 4) & 0x0F0F0F0Fu, (int)a1.y, s);
-                s = dp4a_us((w.z >> 4) & 0x0F0F0F0Fu, (int)a1.z, s);
-                s = dp4a_us((w.w >> 4) & 0x0F0F0F0Fu, (int)a1.w, s);
+                const int s = q4_block_dot(wv[u][r], a0, a1, (int)e.y);
                 if (EMIT) {
                     if (row0 + r < n) sumi[(row0 + r) * kb + b] = s;
                 } else {
