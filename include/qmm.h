@@ -118,8 +118,10 @@ qmm_status qmm_quantize_weight_q4_0(const float *w, int64_t n, int64_t k,
  * With one slice and 8 <= m, when k/32 is a multiple of 8, wq, wd, aq and
  * ad are 16-byte aligned and the quantized activations fit in shared memory,
  * a persistent kernel streams the weights through shared memory with tensor
- * copies; otherwise each warp streams them through registers.  Both give
- * the same bits. */
+ * copies; otherwise each warp streams them through registers.  At m = 1 with
+ * at most 1024 blocks per slice (k <= 32768 unsplit) each CTA first reads
+ * the activation slice once into shared memory for all its warps.  All of
+ * these give the same bits. */
 qmm_status qmm_gemv_q4_0_q8_0(const uint8_t *wq, const uint16_t *wd,
                               const int8_t *aq, const uint16_t *ad, float *y,
                               int64_t m, int64_t n, int64_t k, int split_k,
