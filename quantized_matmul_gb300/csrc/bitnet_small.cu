@@ -399,19 +399,6 @@ __global__ void bitnet_small_prep_kernel(const int8_t *__restrict__ aq, uint4 *_
 uint32_t g_bs_wait_limit = kDefaultWaitLimit;
 int g_bs_withhold = 0;
 
-int bs_num_sms() {
-    static int count = 0;
-    if (count == 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            count = v;
-        else
-            return 152;
-    }
-    return count;
-}
-
 template <int MT, int NT>
 cudaError_t launch_bs_tile(const CUtensorMap &tw, const uint8_t *afrag, const uint8_t *corrs,
                            const float *scale, float absmean, float *y, unsigned int *counter,
@@ -421,15 +408,17 @@ cudaError_t launch_bs_tile(const CUtensorMap &tw, const uint8_t *afrag, const ui
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
     // as many CTAs as fit at once (the first set of each is its index)
-    static int per_sm = 0;
+    static std::atomic<int> per_sm_cache{0};  // the same for every GB300
+    int per_sm = per_sm_cache.load(std::memory_order_relaxed);
     if (per_sm == 0) {
         int v = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kBsThreads, P::kAlloc);
         if (e != cudaSuccess) return e;
         per_sm = std::max(v, 1);
+        per_sm_cache.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t nsets = (n + kBsRows - 1) / kBsRows;
-    const int grid = (int)std::min<int64_t>(nsets, (int64_t)per_sm * bs_num_sms());
+    const int grid = (int)std::min<int64_t>(nsets, (int64_t)per_sm * device_sm_count());
     return launch_kernel(kern, dim3(grid), dim3(kBsThreads), P::kAlloc, s, true, tw, afrag, corrs,
                          scale, absmean, y, counter, (int)m, (int)n, nst, g_bs_wait_limit,
                          g_bs_withhold);

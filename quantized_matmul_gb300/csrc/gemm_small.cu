@@ -578,19 +578,6 @@ __global__ void gemm_small_prep_kernel(const int8_t *__restrict__ aq, const unsi
 uint32_t g_small_wait_limit = kDefaultWaitLimit;
 int g_small_withhold = 0;
 
-int num_sms() {
-    static int count = 0;
-    if (count == 0) {
-        int dev = 0, v = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            count = v;
-        else
-            return 152;
-    }
-    return count;
-}
-
 template <int WB, int MT, int NT, bool EMIT>
 cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, const uint8_t *afrag,
                               const uint8_t *dafrag, float *y, int32_t *sumi, unsigned int *counter,
@@ -600,7 +587,7 @@ cudaError_t launch_small_tile(const CUtensorMap &tw, const CUtensorMap &tdw, con
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::kAlloc);
     if (e != cudaSuccess) return e;
     const int64_t nsets = (n + kSmRows - 1) / kSmRows;
-    const int grid = (int)std::min<int64_t>(nsets, sm_ctas<WB, MT, NT>() * num_sms());
+    const int grid = (int)std::min<int64_t>(nsets, sm_ctas<WB, MT, NT>() * device_sm_count());
     // programmatic dependent launch: the CTAs start their weight copies
     // while the prepass before them still runs
     return launch_kernel(kern, dim3(grid), dim3(kSmThreads), P::kAlloc, s, true, tw, tdw, afrag,

@@ -3,11 +3,27 @@
 // C ABI; they enqueue kernels on `stream` and return the launch status.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace qmm {
+
+// The current device's SM count, queried once per device and cached (152,
+// a GB300's count, if the query fails).  Safe to call from several host
+// threads.
+inline int device_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return 152;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
 
 constexpr int kQK = 32;  // elements per quantization block
 
