@@ -108,7 +108,14 @@ def _torch():
 
 
 def _stream() -> int:
+    """The current CUDA stream of the current device, as a raw handle.  The
+    raw accessor costs ~0.3 us a call against ~2.9 us for building a
+    torch.cuda.Stream object (measured on the GB300 host), a fifth of a
+    decode step's host time; the public call is the fallback."""
     torch = _torch()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device())
     return torch.cuda.current_stream().cuda_stream
 
 
