@@ -680,12 +680,28 @@ bitnet_linear_m1_kernel(const uint32_t *__restrict__ w, float absmean, const flo
         pdl_wait();
         pdl_launch_dependents();
     }
-    // the row's maximum magnitude
+    // the row's maximum magnitude.  With at most one 16-element group per
+    // thread (k <= 16 * threads) each thread reads its group once and keeps
+    // it in registers for the quantization below, so x crosses from L2 once
+    // instead of twice (the maximum is the same whatever the order)
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    const bool one_group = kw <= kThreads;
+    float4 xg[4] = {};
     float amax = 0.0f;
-    for (int64_t i = threadIdx.x; i < k / 4; i += kThreads) {
-        const float4 v = __ldg(x4 + i);
-        amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+    if (one_group) {
+        if (threadIdx.x < kw) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                xg[h] = __ldg(x4 + threadIdx.x * 4 + h);
+                const float4 v = xg[h];
+                amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+            }
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < k / 4; i += kThreads) {
+            const float4 v = __ldg(x4 + i);
+            amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -702,7 +718,7 @@ bitnet_linear_m1_kernel(const uint32_t *__restrict__ w, float absmean, const flo
         uint32_t q4[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            const float4 v = __ldg(x4 + gi * 4 + h);
+            const float4 v = one_group ? xg[h] : __ldg(x4 + gi * 4 + h);
             const float f[4] = {v.x, v.y, v.z, v.w};
             uint32_t packed = 0;
 #pragma unroll
@@ -973,10 +989,12 @@ bool bitnet_linear_fused_supported(int64_t m, int64_t k, int64_t ldx, const void
 cudaError_t launch_bitnet_linear_fused(const uint32_t *w, float absmean, const float *x, int8_t *aq,
                                        float *scale, int32_t *sum, float *y, int64_t n, int64_t k,
                                        cudaStream_t s, bool pdl) {
-    // 3 rows per warp, 8 warps: 3.96 us per step at N=6912, K=2560 (rows x
-    // warps 2x8: 4.01, 4x16: 4.12, 4x8: 4.36, 2x6: 4.48, 4x4: 4.63, 8x8: 4.63,
-    // 2x4: 5.39, 4x2: 5.87, 1x16: 6.05, 1x8: 6.47, 16x4: 8.57; two launches,
-    // quantizer then GEMV: 5.03)
+    // 3 rows per warp, 8 warps: 3.71 us per step at N=6912, K=2560 with the
+    // row read from L2 once (rows x warps 3x16: 3.79, 4x8: 3.89, 2x8: 4.10,
+    // 4x4: 4.61, 2x16: 5.84).  Reading it twice, 3x8 took 3.96-4.05 (2x8:
+    // 4.01, 4x16: 4.12, 4x8: 4.36, 2x6: 4.48, 4x4: 4.63, 8x8: 4.63, 2x4: 5.39,
+    // 4x2: 5.87, 1x16: 6.05, 1x8: 6.47, 16x4: 8.57); two launches, quantizer
+    // then GEMV: 5.03)
     constexpr int kRows = 3, kW = 8;
     const dim3 grid((unsigned)((n + kW * kRows - 1) / (kW * kRows)));
     const size_t smem = (size_t)k;  // one byte per code
