@@ -107,3 +107,21 @@ def test_guarded_records_a_failing_measurement():
 
     out = bench.guarded(boom)
     assert out == {"error": "RuntimeError: no such kernel"}
+
+
+def test_stream_handle_uses_the_raw_accessor_and_falls_back(monkeypatch):
+    """The binding passes the current stream as a raw handle: through
+    torch's raw accessor for the current device where it exists, else through
+    torch.cuda.current_stream()."""
+    import types
+    import torch
+    sys.path.insert(0, ROOT)
+    import quantized_matmul_gb300 as q
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 3)
+    calls = []
+    monkeypatch.setattr(torch._C, "_cuda_getCurrentRawStream",
+                        lambda dev: calls.append(dev) or 0xABC0, raising=False)
+    assert q._stream() == 0xABC0 and calls == [3]
+    monkeypatch.delattr(torch._C, "_cuda_getCurrentRawStream")
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda: types.SimpleNamespace(cuda_stream=0xDEF0))
+    assert q._stream() == 0xDEF0
